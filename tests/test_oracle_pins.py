@@ -1,0 +1,374 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Kinds of pin used: hand-derived worked examples (tests/golden), closed forms,
+brute force on tiny inputs, library routines (numpy matmul / einsum, torch's
+bf16 conversion and scaled_dot_product_attention in fp64) and invariants the
+method's definition fixes (budget k = n gives dense attention, weights sum to
+one, neighbour fetching yields a superset).
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+
+def _f64(bits):
+    return oracle.bf16_bits_to_f64(bits)
+
+
+def _rand_bf16(shape, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ bf16
+
+def test_bf16_golden(golden_dir):
+    with open(os.path.join(golden_dir, "bf16_rounding.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        x = math.ldexp(c["m"], c["e"])
+        got = int(oracle.bf16_round([x])[0])
+        assert got == int(c["bits"], 16), (c["x"], hex(got))
+
+
+def test_bf16_matches_torch_on_binary32_values():
+    # Values exactly representable in binary32 round once either way, so the
+    # oracle must agree with torch's RNE conversion bit for bit.
+    g = torch.Generator().manual_seed(7)
+    x32 = torch.cat([torch.randn(20000, generator=g) * 10.0 ** torch.randint(-30, 30, (20000,), generator=g),
+                     torch.tensor([0.0, -0.0, 1.0, -1.0, 65504.0, 3.0e38, -3.0e38, 1e-40, -1e-42])])
+    ref = x32.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_round(x32.double().numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_widening_is_exact():
+    bits = np.arange(0, 1 << 16, 97, dtype=np.uint16)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for b, v in zip(bits[:400], t[:400]):
+        w = oracle.bf16_to_double(int(b))
+        assert (w == v) or (math.isnan(w) and math.isnan(v))
+
+
+# ------------------------------------------------------------------ projection
+
+def test_project_integer_brute_force():
+    # Integer-valued inputs small enough that every sum is an exact bf16.
+    B, Hkv, n, D, dp = 2, 3, 5, 8, 4
+    K = synth.integer_valued((B, Hkv, n, D), -3, 3, seed=1)
+    W = synth.integer_valued((Hkv, D, dp), -3, 3, seed=2)
+    Kp, Kp64 = oracle.project(K, W)
+    Ki = K.float().int().tolist()
+    Wi = W.float().int().tolist()
+    for b, h, t, j in itertools.product(range(B), range(Hkv), range(n), range(dp)):
+        acc = 0
+        for d in range(D):
+            acc += Ki[b][h][t][d] * Wi[h][d][j]
+        assert Kp64[b, h, t, j] == acc
+        assert _f64(Kp[b, h, t, j]) == acc
+
+
+def test_project_matches_numpy_matmul():
+    B, Hkv, n, D, dp = 1, 2, 300, 64, 16
+    K = _rand_bf16((B, Hkv, n, D), 3)
+    W = _rand_bf16((Hkv, D, dp), 4, std=1 / 8)
+    Kp, Kp64 = oracle.project(K, W)
+    ref = np.matmul(K.double().numpy(), W.double().numpy()[None])
+    assert np.allclose(Kp64, ref, rtol=1e-13, atol=1e-13)
+    # torch rounds fp64 -> bf16 through binary32 (two steps); they may differ
+    # only where the value sits within 2^-24 relative of a rounding tie.
+    tref = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    diff = Kp != tref
+    assert diff.mean() < 1e-3
+    assert np.all(np.abs(_f64(Kp) - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+
+
+# ------------------------------------------------------------------ scores
+
+@pytest.mark.parametrize("agg", [oracle.AGG_MEAN, oracle.AGG_MAX])
+def test_score_integer_brute_force(agg):
+    B, Hq, Hkv, n, dp = 2, 6, 2, 7, 8
+    G = Hq // Hkv
+    qi = synth.integer_valued((B, Hq, dp), -4, 4, seed=5)
+    Kp = synth.integer_valued((B, Hkv, n, dp), -4, 4, seed=6)
+    s, l1 = oracle.score(qi, Kp, agg)
+    Q = qi.float().int().tolist()
+    P = Kp.float().int().tolist()
+    for b, h, t in itertools.product(range(B), range(Hkv), range(n)):
+        dots = [sum(Q[b][h * G + g][i] * P[b][h][t][i] for i in range(dp)) for g in range(G)]
+        mags = [sum(abs(Q[b][h * G + g][i] * P[b][h][t][i]) for i in range(dp)) for g in range(G)]
+        if agg == oracle.AGG_MEAN:
+            assert s[b, h, t] == sum(dots) / G
+            assert l1[b, h, t] == sum(mags) / G
+        else:
+            assert s[b, h, t] == max(dots)
+            assert l1[b, h, t] == max(mags)
+
+
+def test_score_mean_is_group_mean_query_and_einsum():
+    B, Hq, Hkv, n, dp = 2, 8, 2, 500, 32
+    qi = _rand_bf16((B, Hq, dp), 8)
+    Kp = _rand_bf16((B, Hkv, n, dp), 9)
+    s_mean, _ = oracle.score(qi, Kp, oracle.AGG_MEAN)
+    s_max, _ = oracle.score(qi, Kp, oracle.AGG_MAX)
+    q = qi.double().numpy().reshape(B, Hkv, Hq // Hkv, dp)
+    P = Kp.double().numpy()
+    per_g = np.einsum("bhgi,bhti->bhgt", q, P)
+    assert np.allclose(s_mean, per_g.mean(2), rtol=1e-12, atol=1e-12)
+    assert np.allclose(s_max, per_g.max(2), rtol=0, atol=0)
+    qbar = q.mean(2)
+    assert np.allclose(s_mean, np.einsum("bhi,bhti->bht", qbar, P), rtol=1e-12, atol=1e-12)
+    assert np.all(s_max >= s_mean - 1e-12)
+
+
+def test_score_group_of_one_mean_equals_max():
+    qi = _rand_bf16((1, 4, 16), 10)
+    Kp = _rand_bf16((1, 4, 100, 16), 11)
+    a, _ = oracle.score(qi, Kp, oracle.AGG_MEAN)
+    b, _ = oracle.score(qi, Kp, oracle.AGG_MAX)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ top-k
+
+def _brute_topk(s_row, k):
+    # i is selected iff fewer than k elements beat it under (score desc, index asc).
+    # O(n^2) rank count: a different algorithm from the oracle's sort.
+    n = len(s_row)
+    sel = []
+    for i in range(n):
+        better = 0
+        for j in range(n):
+            if s_row[j] > s_row[i] or (s_row[j] == s_row[i] and j < i):
+                better += 1
+        if better < k:
+            sel.append(i)
+    return sel
+
+
+def test_topk_golden(golden_dir):
+    with open(os.path.join(golden_dir, "topk_worked.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        s = np.array([float(v) for v in c["scores"]], dtype=np.float64)
+        got = oracle.topk(s[None], c["k"])[0].tolist()
+        assert got == c["idx"], c["why"]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_topk_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    rows, n = 4, 257
+    s = rng.standard_normal((rows, n))
+    for k in [1, 2, 17, 128, 256, 257]:
+        got = oracle.topk(s, k)
+        for r in range(rows):
+            assert got[r].tolist() == _brute_topk(s[r].tolist(), k)
+
+
+def test_topk_tie_stress():
+    rng = np.random.default_rng(5)
+    n = 300
+    s = rng.integers(0, 4, size=(3, n)).astype(np.float64)
+    for k in [1, 50, 75, 76, 150, 299]:
+        got = oracle.topk(s, k)
+        for r in range(3):
+            assert got[r].tolist() == _brute_topk(s[r].tolist(), k)
+
+
+def test_topk_shift_invariance_and_full_budget():
+    rng = np.random.default_rng(6)
+    s = rng.standard_normal((2, 400))
+    a = oracle.topk(s, 40)
+    b = oracle.topk(s + 1024.0, 40)   # exact shift: 1024 + N(0,1) loses no ordering info at this size
+    assert np.array_equal(a, b)
+    full = oracle.topk(s, 400)
+    assert np.array_equal(full, np.tile(np.arange(400, dtype=np.int32), (2, 1)))
+    assert oracle.topk(s, 0).shape == (2, 0)
+
+
+def test_topk_rejects_nan():
+    s = np.array([[1.0, float("nan"), 0.0]])
+    with pytest.raises(ValueError):
+        oracle.topk(s, 1)
+
+
+# ------------------------------------------------------------------ expand
+
+def test_expand_golden(golden_dir):
+    with open(os.path.join(golden_dir, "expand_worked.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        sel, cnt = oracle.expand(np.array([c["idx"]], dtype=np.int32), c["r"], c["n_pred"], c["n_t"])
+        assert sel[0, : cnt[0]].tolist() == c["sel"], c["why"]
+
+
+@pytest.mark.parametrize("r", [0, 1, 2, 5])
+def test_expand_brute_force_and_invariants(r):
+    rng = np.random.default_rng(10 + r)
+    n_pred, k = 200, 30
+    for trial in range(5):
+        idx = np.sort(rng.choice(n_pred, size=(k,), replace=False)).astype(np.int32)[None]
+        n_t = n_pred + trial
+        sel, cnt = oracle.expand(idx, r, n_pred, n_t)
+        got = sel[0, : cnt[0]].tolist()
+        want = set()
+        for i in idx[0].tolist():
+            want.update(t for t in range(i - r, i + r + 1) if 0 <= t < n_pred)
+        want = sorted(want) + list(range(n_pred, n_t))
+        assert got == want
+        body = got[: len(got) - (n_t - n_pred)]
+        assert set(idx[0].tolist()) <= set(body)                       # superset
+        assert k <= len(body) <= min(n_pred, k * (2 * r + 1))          # bounds
+        assert all(a < b for a, b in zip(got, got[1:]))                # sorted, unique
+        if r == 0:
+            assert body == idx[0].tolist()
+
+
+# ------------------------------------------------------------------ attention
+
+def test_attn_golden(golden_dir):
+    with open(os.path.join(golden_dir, "attn_closed_form.json")) as f:
+        cases = json.load(f)["cases"]
+    e = math.e
+    for c in cases:
+        D = c["D"]
+        q = torch.tensor([[c["q"]]], dtype=torch.bfloat16)
+        K = torch.tensor([[c["K"]]], dtype=torch.bfloat16)
+        V = torch.tensor([[c["V"]]], dtype=torch.bfloat16)
+        sel = np.array([[c["sel"]]], dtype=np.int32)
+        cnt = np.array([[len(c["sel"])]], dtype=np.int32)
+        out = oracle.attn(q, K, V, sel, cnt, c["scale"])
+        want = [eval(expr.replace("^", "**"), {"e": e}) for expr in c["out"]]
+        assert np.allclose(out[0, 0, :D], want, rtol=1e-14, atol=1e-14)
+
+
+def _sdpa_ref(q, K, V, sel, scale):
+    """torch scaled_dot_product_attention in fp64 on the gathered rows, one (b, h) row."""
+    Kg = K[sel].double()[None, None]
+    Vg = V[sel].double()[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(
+        q.double()[None, :, None, :].transpose(0, 1).reshape(1, -1, 1, q.shape[-1]),
+        Kg.expand(1, q.shape[0], -1, -1), Vg.expand(1, q.shape[0], -1, -1), scale=scale)[0, :, 0, :]
+
+
+def test_attn_matches_sdpa_fp64():
+    w = synth.small(B=2, Hq=8, Hkv=2, D=32, dp=8, N=300, k=40, seed=3)
+    L = synth.make_layer(w)
+    rng = np.random.default_rng(3)
+    sel = np.stack([np.stack([np.sort(rng.choice(w.N, 40, replace=False)) for _ in range(w.Hkv)])
+                    for _ in range(w.B)]).astype(np.int32)
+    cnt = np.full((w.B, w.Hkv), 40, dtype=np.int32)
+    out, wsum = oracle.attn(L["q"], L["K"], L["V"], sel, cnt, w.scale, with_wsum=True)
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            qh = L["q"][b, h * w.G:(h + 1) * w.G]
+            ref = _sdpa_ref(qh, L["K"][b, h], L["V"][b, h], torch.from_numpy(sel[b, h]).long(), w.scale)
+            assert np.allclose(out[b, h * w.G:(h + 1) * w.G], ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.all(np.abs(wsum - 1.0) <= 1e-12)
+
+
+def test_attn_special_cases():
+    w = synth.small(B=1, Hq=4, Hkv=2, D=16, dp=8, N=50, seed=4)
+    L = synth.make_layer(w)
+    Vf = L["V"].double().numpy()
+    # one selected row: the output is that V row exactly
+    sel = np.array([[[7], [33]]], dtype=np.int32)
+    cnt = np.ones((1, 2), dtype=np.int32)
+    out = oracle.attn(L["q"], L["K"], L["V"], sel, cnt, w.scale)
+    assert np.array_equal(out[0, 0], Vf[0, 0, 7]) and np.array_equal(out[0, 3], Vf[0, 1, 33])
+    # zero query: uniform weights, the output is the mean of the selected V rows
+    sel = np.array([[[1, 4, 9, 20], [0, 2, 3, 49]]], dtype=np.int32)
+    cnt = np.full((1, 2), 4, dtype=np.int32)
+    q0 = torch.zeros_like(L["q"])
+    out = oracle.attn(q0, L["K"], L["V"], sel, cnt, w.scale)
+    assert np.allclose(out[0, 1], Vf[0, 0, [1, 4, 9, 20]].mean(0), rtol=1e-14, atol=1e-14)
+    # permuting the selection changes nothing (up to fp64 summation order)
+    perm = sel[:, :, ::-1].copy()
+    a = oracle.attn(L["q"], L["K"], L["V"], sel, cnt, w.scale)
+    b = oracle.attn(L["q"], L["K"], L["V"], perm, cnt, w.scale)
+    assert np.allclose(a, b, rtol=1e-13, atol=1e-14)
+
+
+def test_full_budget_reproduces_dense():
+    w = synth.small(B=1, Hq=8, Hkv=2, D=32, dp=8, N=200, seed=5)
+    L = synth.make_layer(w)
+    Kp, _ = oracle.project(L["K"], L["Wk"])
+    s, _ = oracle.score(L["q_imp"], Kp)
+    idx = oracle.topk(s, w.N)
+    sel, cnt = oracle.expand(idx, 0, w.N, w.N)
+    sparse = oracle.attn(L["q"], L["K"], L["V"], sel, cnt, w.scale)
+    dense = oracle.dense_attn(L["q"], L["K"], L["V"], w.N, w.scale)
+    assert np.array_equal(sparse, dense)
+    for b, h in itertools.product(range(w.B), range(w.Hkv)):
+        ref = _sdpa_ref(L["q"][b, h * w.G:(h + 1) * w.G], L["K"][b, h], L["V"][b, h],
+                        torch.arange(w.N), w.scale)
+        assert np.allclose(dense[b, h * w.G:(h + 1) * w.G], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_planted_heavy_hitters_are_selected():
+    # The long-context recipe plants tokens whose keys align with the group's
+    # importance query; every one of them must make the budget.
+    w = synth.Workload("planted-small", B=1, Hq=8, Hkv=2, D=64, dp=16, N=4096, k=64,
+                       outliers=4, planted=16, seed=9)
+    L = synth.make_layer(w)
+    Kp, _ = oracle.project(L["K"], L["Wk"])
+    s, _ = oracle.score(L["q_imp"], Kp)
+    idx = oracle.topk(s, w.k)
+    for h in range(w.Hkv):
+        assert set(L["planted_pos"][0, h].tolist()) <= set(idx[0, h].tolist())
+
+
+# ------------------------------------------------------------------ decode steps
+
+def _run_steps(w, T, r, steps, k):
+    L = synth.make_layer(w, cap=w.N + steps, n=w.N)
+    K = oracle.as_u16(L["K"]).copy()
+    V = oracle.as_u16(L["V"]).copy()
+    Kp = np.zeros((w.B, w.Hkv, w.N + steps, w.dp), dtype=np.uint16)
+    Kp[:, :, : w.N], _ = oracle.project(np.ascontiguousarray(K[:, :, : w.N]), L["Wk"])
+    st = oracle.DecodeState()
+    outs = []
+    for t in range(steps):
+        d = synth.make_step(w, 0, t, L["outlier_ch"])
+        out, sel, cnt = oracle.decode_step(st, t, w.N + t, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"],
+                                           V_new=d["V_new"], Wk=L["Wk"], K=K, V=V, Kp=Kp, k=k, T=T, r=r,
+                                           agg=oracle.AGG_MEAN, scale=w.scale)
+        outs.append((out, sel, cnt, st.idx.copy(), st.n_pred))
+    return outs, (K, V, Kp, L)
+
+
+def test_decode_interval_one_is_per_step_selection():
+    w = synth.small(B=1, Hq=4, Hkv=2, D=16, dp=8, N=120, seed=11)
+    outs, (K, V, Kp, L) = _run_steps(w, T=1, r=0, steps=4, k=10)
+    for t, (out, sel, cnt, idx, n_pred) in enumerate(outs):
+        n_t = w.N + t + 1
+        assert n_pred == n_t
+        d = synth.make_step(w, 0, t, L["outlier_ch"])
+        s, _ = oracle.score(d["q_imp"], np.ascontiguousarray(Kp[:, :, :n_t]))
+        want = oracle.topk(s, 10)
+        assert np.array_equal(sel[:, :, :10], want) and np.all(cnt == 10)
+
+
+def test_decode_interval_reuse_superset_and_tail():
+    w = synth.small(B=1, Hq=4, Hkv=2, D=16, dp=8, N=150, seed=12)
+    T, r, k = 4, 1, 12
+    outs, _ = _run_steps(w, T=T, r=r, steps=9, k=k)
+    for t, (out, sel, cnt, idx, n_pred) in enumerate(outs):
+        t0 = (t // T) * T
+        assert n_pred == w.N + t0 + 1
+        n_t = w.N + t + 1
+        for b, h in itertools.product(range(w.B), range(w.Hkv)):
+            s = sel[b, h, : cnt[b, h]].tolist()
+            assert set(idx[b, h].tolist()) <= set(s)
+            assert s[len(s) - (n_t - n_pred):] == list(range(n_pred, n_t))
+            body = len(s) - (n_t - n_pred)
+            assert k <= body <= min(n_pred, k * (2 * r + 1))
