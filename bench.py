@@ -1,0 +1,417 @@
+"""Benchmark of the TokenButler decode-time hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one decode step of one Llama-3-8B-shaped attention layer at
+N = 32768 cached tokens with a 10% budget (k = 3277 per KV head): append the
+new token (K/V rows and its projected key), score all N tokens with the
+importance query, keep the top k per KV head, and attend over the gathered
+rows. Inputs are seeded synthetic tensors already resident in HBM. The step
+rotates over R copies of the layer's caches so that consecutive steps never
+find their data in the 126 MB L2 (R x the step's bytes >= 4 x L2).
+
+Prints one JSON line (rank 0). With --gpus N > 1 (torchrun) every rank runs
+its own replica of the workload (the (batch, KV head) rows are independent;
+there is no collective on the path) and value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "decode steps/sec & tokens/s at N=32K, budget 10%; achieved HBM GB/s vs ~8 TB/s"
+UNIT = "decode steps/s"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=synth.WORKLOADS[1].name)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def _workload(name):
+    for w in synth.WORKLOADS:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        mhz = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist_init(n):
+    if n <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    dist.init_process_group("nccl")
+    rank = dist.get_rank()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+    return rank, dist.get_world_size(), dist
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def _oracle_setup(w):
+    import oracle
+    n0 = w.N - 1
+    L = synth.make_layer(w, cap=w.N, n=n0)
+    oK = oracle.as_u16(L["K"]).copy()
+    oV = oracle.as_u16(L["V"]).copy()
+    oKp = np.zeros((w.B, w.Hkv, w.N, w.dp), dtype=np.uint16)
+    oKp[:, :, :n0], _ = oracle.project(np.ascontiguousarray(oK[:, :, :n0]), L["Wk"])
+    d = synth.make_step(w, 0, 0, L["outlier_ch"])
+    return L, oK, oV, oKp, n0, d
+
+
+def _oracle_step(w, L, d, oK, oV, oKp, n0):
+    """One whole decode step in the oracle (append, score, top-k, attention; OpenMP over rows)."""
+    import oracle
+    st = oracle.DecodeState()
+    oracle.decode_step(st, 0, n0, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=L["Wk"],
+                       K=oK, V=oV, Kp=oKp, k=w.k, T=1, r=0, agg=oracle.AGG_MEAN, scale=w.scale)
+
+
+def _oracle_cores(w) -> int:
+    import oracle
+    return min(oracle.num_threads(), w.B * w.Hq)
+
+
+def cpu_baseline(w, seconds: float):
+    """The oracle as it stands, timed on this host's cores on a bounded sample of whole decode steps."""
+    L, oK, oV, oKp, n0, d = _oracle_setup(w)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        _oracle_step(w, L, d, oK, oV, oKp, n0)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": _oracle_cores(w), "kind": "oracle",
+            "sample": f"{done} whole decode steps at N={w.N}, k={w.k} in {el:.1f} s (fp64 C, OpenMP over "
+                      f"(batch, head) rows)"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    L, oK, oV, oKp, n0, d = _oracle_setup(w)
+    t1 = time.perf_counter()
+    _oracle_step(w, L, d, oK, oV, oKp, n0)
+    per_step = time.perf_counter() - t1
+    warm = max(0, min(args.warmup, 3))
+    for _ in range(warm):
+        _oracle_step(w, L, d, oK, oV, oKp, n0)
+    # the number of steps timed is capped so the run ends within a few minutes
+    timed = max(1, min(args.steps, int(120.0 / max(per_step, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(timed):
+        _oracle_step(w, L, d, oK, oV, oKp, n0)
+    el = time.perf_counter() - t0
+    val = timed / el
+    sample = f"{timed} whole decode steps at N={w.N}, k={w.k} (of {args.steps} requested), fp64 C, OpenMP"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": timed, "steps_requested": args.steps, "warmup": warm, "ms_per_step": 1e3 / val,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "N": w.N, "k": w.k, "B": w.B},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": _oracle_cores(w), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, w):
+    import predicted_token_importance_tb_b300 as tb
+
+    rank, world, dist = _dist_init(args.gpus)
+    if dist is None:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tb.load_library()
+    n0 = w.N - 1                     # tokens before the step's append: the step scores N
+    cap = w.N
+    shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, cap)
+    L = synth.make_layer(w, cap=cap, n=n0)
+    Wk = L["Wk"].cuda()
+    K0, V0 = L["K"].cuda(), L["V"].cuda()
+    Kp0 = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
+    tb.tb_project_append(shape, K0, cap, Wk, Kp0, 0, n0)
+    torch.cuda.synchronize()
+
+    # bytes one step moves (algorithmic): Kp stream, the gathered K/V rows,
+    # q / q_imp / out, and the append (new K/V rows in and out, Wk, new Kp row)
+    rows = w.B * w.Hkv
+    kp_bytes = rows * w.N * w.dp * 2
+    gather_bytes = rows * w.k * 2 * w.D * 2
+    qio_bytes = (w.B * w.Hq * w.D * 2) * 2 + w.B * w.Hq * w.dp * 2
+    append_bytes = rows * w.D * 2 * 2 * 2 + w.Hkv * w.D * w.dp * 2 + rows * w.dp * 2
+    step_bytes = kp_bytes + gather_bytes + qio_bytes + append_bytes
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(4, math.ceil(4 * l2 / step_bytes))
+    Ks = [K0] + [K0.clone() for _ in range(R - 1)]
+    Vs = [V0] + [V0.clone() for _ in range(R - 1)]
+    Kps = [Kp0] + [Kp0.clone() for _ in range(R - 1)]
+    steps_in = [synth.make_step(w, 0, i, L["outlier_ch"]) for i in range(R)]
+    dins = [{k: v.cuda() for k, v in d.items()} for d in steps_in]
+    dec = tb.DecodeLayer(shape, w.k, T=1, r=0, scale=w.scale, n_max=n0)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        j = i % R
+        d = dins[j]
+        dec.step(0, n0, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=Wk, K=Ks[j], V=Vs[j],
+                 Kp=Kps[j], out=out)
+
+    # eager sanity pass, then capture M steps as one CUDA graph
+    for i in range(R):
+        step(i)
+    torch.cuda.synchronize()
+    tb.check_dev_status(dec.status, "bench warm-up")
+    M = min(max(R, (1000 // R) * R), max(args.steps, 1))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graphs = {}
+
+    def graph_of(m):
+        if m not in graphs:
+            g = torch.cuda.CUDAGraph(keep_graph=True)
+            with torch.cuda.graph(g, stream=s):
+                for i in range(m):
+                    step(i)
+            g.instantiate()
+            graphs[m] = g
+        return graphs[m]
+
+    gM = graph_of(M)
+    kernel_nodes = _count_kernel_nodes(gM)
+    kernels_per_step = kernel_nodes / M if kernel_nodes is not None else None
+    rem = args.steps % M
+    g_rem = graph_of(rem) if rem else None
+    torch.cuda.synchronize()
+    # warm-up W steps
+    for _ in range(args.warmup // M):
+        gM.replay()
+    if args.warmup % M:
+        graph_of(args.warmup % M).replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    _barrier(dist)
+    e0.record()
+    for _ in range(args.steps // M):
+        gM.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record()
+    _barrier(dist)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop() if clocks else None
+    tb.check_dev_status(dec.status, "bench timed region")
+    ms = _max_over_ranks(dist, ms)
+    sec = ms / 1e3
+    steps_per_s_rank = args.steps / sec
+    total_steps_per_s = steps_per_s_rank * world
+
+    # realised gathered rows (from counts) for the byte accounting
+    real_gather = int(dec.counts.sum().item()) * 2 * w.D * 2
+    step_bytes_real = kp_bytes + real_gather + qio_bytes + append_bytes
+    hbm_peak, peak_kind = _peaks()
+    per_step_s = sec / args.steps
+    achieved = step_bytes_real / per_step_s / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(tb, w, shape, dec, Wk, Ks[0], Vs[0], Kps[0], n0, steps_in, dist, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": total_steps_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "dp": w.dp, "N": w.N,
+                       "k": w.k, "T": 1, "r": 0, "rotation_sets": R,
+                       "l2_defeat": f"inputs rotate over {R} cache copies ({R * step_bytes / 1e6:.0f} MB >= 4 x L2)",
+                       "parallelism": f"replicas x{world}"},
+            "tokens_per_s": total_steps_per_s * w.B,
+            "hbm_gbs": achieved * world,
+            "bytes_per_step": step_bytes_real,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "kernel": "tb decode step, %s kernel(s) per step" % kernels_per_step,
+                         "peak_source": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(round(args.steps * kernels_per_step)) if kernels_per_step else None,
+            "kernels_per_step": kernels_per_step,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _count_kernel_nodes(g) -> int | None:
+    """Kernel nodes in a captured CUDA graph (the launches one replay makes)."""
+    try:
+        from cuda.bindings import runtime as rt
+        graph = g.raw_cuda_graph()
+        err, _, n = rt.cudaGraphGetNodes(graph, 0)
+        err, nodes, n = rt.cudaGraphGetNodes(graph, n)
+        kinds = [rt.cudaGraphNodeGetType(x)[1] for x in nodes[:n]]
+        return sum(1 for k in kinds if k == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel)
+    except Exception:
+        return None
+
+
+def _e2e(tb, w, shape, dec, Wk, K, V, Kp, n0, steps_in, dist, world, n_steps=300):
+    """Same step through the Python API: pinned host inputs copied in, output copied out, every step."""
+    host = [{k: v.pin_memory() for k, v in d.items()} for d in steps_in]
+    dev_in = {k: torch.empty_like(v, device="cuda") for k, v in steps_in[0].items()}
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in steps_in[0].values())
+    d2h = out.numel() * out.element_size()
+
+    def one(i):
+        hs = host[i % len(host)]
+        for k, v in hs.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        dec.step(0, n0, q=dev_in["q"], q_imp=dev_in["q_imp"], K_new=dev_in["K_new"], V_new=dev_in["V_new"], Wk=Wk,
+                 K=K, V=V, Kp=Kp, out=out)
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(20):
+        one(i)
+    _barrier(dist)
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        one(i)
+    el = time.perf_counter() - t0
+    el = _max_over_ranks(dist, el)
+    return {"value": n_steps * world / el, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n_steps, "note": "per step: H2D of q, q_imp, K_new, V_new from pinned memory, tb_decode_step, "
+                                      "D2H of out, stream synchronize"}
+
+
+def main():
+    args = _args()
+    w = _workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

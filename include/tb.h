@@ -1,0 +1,198 @@
+/*
+ * tb.h -- C ABI of the TokenButler decode-time hot path on one B300 (sm_103a).
+ *
+ * The method ("TokenButler: Token Importance is Predictable"; arXiv abstract
+ * and the gist.science technical summary): every KV head keeps a
+ * low-dimensional copy of its keys, Kp = K . Wk. At a decode step an
+ * importance query scores all cached tokens against Kp, a fixed budget of k
+ * individual tokens per KV head is kept, optionally reused for T steps and
+ * widened by +-r neighbours, and exact softmax attention runs over only those
+ * full-precision K/V rows while the whole cache stays in device memory.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - bf16 tensors travel as raw 16-bit patterns (tb_bf16). All tensor
+ *    pointers are DEVICE pointers, 16-byte aligned, dense row-major.
+ *  - Shapes: B batch, Hq query heads, Hkv KV heads (G = Hq/Hkv query heads
+ *    share one KV head), D head dim, dp projected dim, cap cache rows.
+ *      K, V  : [B, Hkv, cap, D]        Kp : [B, Hkv, cap, dp]
+ *      Wk    : [Hkv, D, dp]            q  : [B, Hq, D]
+ *      q_imp : [B, Hq, dp]             s  : [B, Hkv, n] (fp32)
+ *      idx   : [B, Hkv, k] (int32)     sel: [B, Hkv, sel_stride] (int32)
+ *      out   : [B, Hq, D]
+ *  - Limits: D and dp multiples of 8, D <= 256, dp <= 256, Hq % Hkv == 0,
+ *    G <= 16, cap < 2^31. Violations return TB_ERR_UNSUPPORTED or
+ *    TB_ERR_INVALID_ARG before anything is enqueued.
+ *  - The caller owns all memory; the library allocates none. Scratch comes
+ *    from a caller-provided workspace of tb_workspace_size() bytes that must
+ *    be zero-filled before its first use (tb_workspace_init); every call that
+ *    completes puts the control words it used back to zero, so later calls
+ *    need no re-initialisation. One workspace may serve every call, but calls
+ *    sharing a workspace must not overlap on the GPU.
+ *  - Every call is asynchronous on the caller's stream. The returned status
+ *    covers argument checks and the launch. Errors found on the device
+ *    (a bad index, a NaN score, a wait that timed out) are written to
+ *    *dev_status (a device int32, may be NULL) as a tb_status code; the first
+ *    one written sticks until the caller resets the word to 0. After
+ *    TB_ERR_TIMEOUT the workspace must be zero-filled again.
+ *  - No call aborts, traps or throws across this boundary.
+ */
+#ifndef TB_H_
+#define TB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TB_API __attribute__((visibility("default")))
+#else
+#define TB_API
+#endif
+
+typedef uint16_t tb_bf16;
+
+typedef enum {
+    TB_OK = 0,
+    TB_ERR_INVALID_ARG = 1,   /* bad pointer, size, index or combination */
+    TB_ERR_UNSUPPORTED = 2,   /* shape or alignment outside the limits above */
+    TB_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    TB_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, attribute) */
+    TB_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
+    TB_ERR_NONFINITE = 6      /* a NaN importance score */
+} tb_status;
+
+#define TB_AGG_MEAN 0  /* group score = mean of the G query heads' dot products */
+#define TB_AGG_MAX 1   /* group score = max of them */
+
+typedef struct {
+    int32_t B, Hq, Hkv, D, dp;
+    int64_t cap;
+} tb_shape;
+
+/* Per-layer decode settings. */
+typedef struct {
+    int32_t k;      /* budget per (batch, KV head), 1 <= k */
+    int32_t T;      /* prediction interval in steps, >= 1 */
+    int32_t r;      /* neighbour radius, >= 0 */
+    int32_t agg;    /* TB_AGG_MEAN or TB_AGG_MAX */
+    float scale;    /* softmax scale, normally 1/sqrt(D) */
+} tb_step_params;
+
+/* Text for a status code (static storage). */
+TB_API const char *tb_status_string(tb_status st);
+
+/* ABI version, currently 1. */
+TB_API int32_t tb_version(void);
+
+/*
+ * Bytes of workspace that any call below needs for shapes up to `shape`,
+ * token counts up to n_max, budgets up to k_max and selections of up to
+ * sel_stride_max rows. Written to *bytes.
+ */
+TB_API tb_status tb_workspace_size(const tb_shape *shape, int64_t n_max, int32_t k_max,
+                            int32_t sel_stride_max, size_t *bytes);
+
+/* Zero-fill a workspace on `stream` (needed once, and after TB_ERR_TIMEOUT). */
+TB_API tb_status tb_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Key projection into the low-dimensional cache ("Core Architecture",
+ * Key-Cache Projection: a learned matrix maps the real keys of a consumer
+ * layer to the importance space; "Optimizations", Batching: projections are
+ * made for a batch of tokens at a time).
+ *
+ *   Kp[b,h,pos0+i,:] = RNE_bf16( K_src[b,h,i,:] . Wk[h] )   0 <= i < n_new
+ *
+ * fp32 accumulation. K_src row i of head (b,h) is at
+ * K_src + ((b*Hkv + h)*src_stride + i)*D, so passing the cache itself with
+ * src_stride = cap and K_src = K + pos0*D projects rows already stored there.
+ * Requires pos0 + n_new <= cap and n_new <= src_stride.
+ * Large n_new runs on the tensor cores (tcgen05, TMA-fed).
+ */
+TB_API tb_status tb_project_append(const tb_shape *shape, const tb_bf16 *K_src, int64_t src_stride,
+                            const tb_bf16 *Wk, tb_bf16 *Kp, int64_t pos0, int64_t n_new,
+                            void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Importance scores ("Core Architecture", Scoring: the predicted queries are
+ * dotted with the projected keys).
+ *
+ *   s[b,h,t] = agg_{g<G} sum_i q_imp[b,h*G+g,i] * Kp[b,h,t,i]    0 <= t < n
+ *
+ * fp32; agg is TB_AGG_MEAN or TB_AGG_MAX. s is dense [B, Hkv, n].
+ */
+TB_API tb_status tb_score(const tb_shape *shape, const tb_bf16 *q_imp, const tb_bf16 *Kp, int64_t n,
+                   int32_t agg, float *s, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Fixed-budget per-token selection (arXiv abstract: dynamic per-token
+ * selection under a fixed budget). For each (b,h) row of s [B,Hkv,n], idx
+ * receives the k tokens with the largest scores, ties to the lower index,
+ * in ascending index order. 0 <= k <= n. -0.0 ties with +0.0; a NaN score
+ * writes TB_ERR_NONFINITE to *dev_status (the NaN then ranks lowest).
+ * Exact: the result is bit-identical to a full sort of the fp32 scores.
+ */
+TB_API tb_status tb_topk(const tb_shape *shape, const float *s, int64_t n, int32_t k, int32_t *idx,
+                  void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Neighbour fetching and the prediction-interval tail ("Optimizations",
+ * Prediction Interval & Neighbor Fetching). For each row, from idx [.,k]
+ * (strictly ascending, within [0, n_pred)):
+ *   sel = sorted unique union of [i-r, i+r] clipped to [0, n_pred), followed
+ *         by n_pred, n_pred+1, ..., n_t-1 (tokens appended since prediction)
+ *   counts = its length (<= sel_stride, else TB_ERR_INVALID_ARG on device).
+ */
+TB_API tb_status tb_expand(const tb_shape *shape, const int32_t *idx, int32_t k, int32_t r,
+                    int64_t n_pred, int64_t n_t, int32_t *sel, int32_t sel_stride,
+                    int32_t *counts, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Exact attention over the selected rows (arXiv abstract; "Significance":
+ * the full cache is kept and only the relevant tokens are read).
+ *
+ *   out[b,hq,:] = sum_{j in sel[b,h]} softmax_j(scale * q[b,hq].K[b,h,j]) V[b,h,j]
+ *
+ * with h = hq / G; the first counts[b,h] entries of each sel row are used
+ * (counts == NULL: all sel_stride). fp32 online softmax split over the
+ * selection, merged in-kernel. An entry outside [0, cap) or an empty row is
+ * skipped and writes TB_ERR_INVALID_ARG to *dev_status.
+ */
+TB_API tb_status tb_sparse_decode_attn(const tb_shape *shape, const tb_bf16 *q, const tb_bf16 *K,
+                                const tb_bf16 *V, const int32_t *sel, const int32_t *counts,
+                                int32_t sel_stride, float scale, tb_bf16 *out,
+                                void *ws, size_t ws_bytes, int32_t *dev_status,
+                                cudaStream_t stream);
+
+/*
+ * One decode step of one layer, all of the above in order ("Optimizations":
+ * the predictor runs once every T steps, its selection is reused in between
+ * and widened by neighbours).
+ *   1. append: K[.,.,n] = K_new, V[.,.,n] = V_new, Kp[.,.,n] = RNE(K_new . Wk)
+ *   2. if t % T == 0: score the n+1 tokens, keep the top k in idx_state,
+ *      *n_pred = n+1 (host scalar), then sel = expand(idx_state, r, n_pred, n+1)
+ *      else sel += [n] (the tail since the prediction)
+ *   3. out = attention of q over sel.
+ * K_new, V_new: [B, Hkv, D]. idx_state [B,Hkv,k], sel [B,Hkv,sel_stride] and
+ * counts [B,Hkv] persist across the steps of an interval; sel_stride must be
+ * >= min(n+1, k(2r+1)) + T - 1. The steps of an interval must be issued in
+ * order with consecutive t and n. With T == 1 and r == 0 the whole step runs
+ * as one fused kernel.
+ */
+TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *params, int64_t t, int64_t n,
+                         const tb_bf16 *q, const tb_bf16 *q_imp, const tb_bf16 *K_new,
+                         const tb_bf16 *V_new, const tb_bf16 *Wk, tb_bf16 *K, tb_bf16 *V,
+                         tb_bf16 *Kp, int32_t *idx_state, int64_t *n_pred, int32_t *sel,
+                         int32_t sel_stride, int32_t *counts, tb_bf16 *out,
+                         void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TB_H_ */

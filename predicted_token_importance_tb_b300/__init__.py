@@ -1,0 +1,266 @@
+"""Python binding of libtb, the C-ABI library of the TokenButler decode-time hot path.
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``libtb.so`` (built in-tree for sm_103a by ``build.py``). There is no CPU or
+PyTorch fallback; if the library is missing the first call raises.
+
+Functions keep the C names (``tb_score``, ``tb_topk``, ...) and take torch
+tensors on the current CUDA device; streams default to the current torch
+stream. bf16 tensors are passed as raw pointers to their 16-bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtb.so")
+
+TB_OK = 0
+TB_ERR_INVALID_ARG = 1
+TB_ERR_UNSUPPORTED = 2
+TB_ERR_WORKSPACE = 3
+TB_ERR_CUDA = 4
+TB_ERR_TIMEOUT = 5
+TB_ERR_NONFINITE = 6
+
+TB_AGG_MEAN = 0
+TB_AGG_MAX = 1
+
+EXPORTED = (
+    "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
+    "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step",
+)
+
+
+class TBError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("dp", ctypes.c_int32), ("cap", ctypes.c_int64)]
+
+
+class _StepParams(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_int32), ("T", ctypes.c_int32), ("r", ctypes.c_int32),
+                ("agg", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+@dataclass(frozen=True)
+class Shape:
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    dp: int
+    cap: int
+
+    def c(self) -> _Shape:
+        return _Shape(self.B, self.Hq, self.Hkv, self.D, self.dp, self.cap)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libtb.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               f"`python -m predicted_token_importance_tb_b300.build`")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        SP = ctypes.POINTER(_Shape)
+        lib.tb_status_string.argtypes = [ctypes.c_int]
+        lib.tb_status_string.restype = ctypes.c_char_p
+        lib.tb_version.restype = i32
+        lib.tb_workspace_size.argtypes = [SP, i64, i32, i32, ctypes.POINTER(sz)]
+        lib.tb_workspace_init.argtypes = [P, sz, P]
+        lib.tb_project_append.argtypes = [SP, P, i64, P, P, i64, i64, P, sz, P, P]
+        lib.tb_score.argtypes = [SP, P, P, i64, i32, P, P, P]
+        lib.tb_topk.argtypes = [SP, P, i64, i32, P, P, sz, P, P]
+        lib.tb_expand.argtypes = [SP, P, i32, i32, i64, i64, P, i32, P, P, P]
+        lib.tb_sparse_decode_attn.argtypes = [SP, P, P, P, P, P, i32, f32, P, P, sz, P, P]
+        lib.tb_decode_step.argtypes = [SP, ctypes.POINTER(_StepParams), i64, i64, P, P, P, P, P, P, P, P, P,
+                                       ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
+        for name in EXPORTED:
+            if name != "tb_status_string" and name != "tb_version":
+                getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(st: int) -> str:
+    try:
+        return load_library().tb_status_string(int(st)).decode()
+    except Exception:  # library not loadable: still give a readable message
+        return f"status {st}"
+
+
+def _check(st: int, what: str):
+    if st != TB_OK:
+        raise TBError(st, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16(t, name):
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    return _ptr(t)
+
+
+def _i32(t, name):
+    if t is not None and t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32, got {t.dtype}")
+    return _ptr(t)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _status_ptr(dev_status):
+    return _i32(dev_status, "dev_status") if dev_status is not None else None
+
+
+# ------------------------------------------------------------------ workspace
+
+def tb_workspace_size(shape: Shape, n_max: int, k_max: int, sel_stride_max: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().tb_workspace_size(ctypes.byref(shape.c()), n_max, k_max, sel_stride_max,
+                                            ctypes.byref(out)), "tb_workspace_size")
+    return int(out.value)
+
+
+def tb_workspace_init(ws: torch.Tensor, stream=None):
+    _check(load_library().tb_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "tb_workspace_init")
+
+
+def workspace(shape: Shape, n_max: int, k_max: int, sel_stride_max: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (uint8 tensor) large enough for every call at these sizes."""
+    nbytes = tb_workspace_size(shape, n_max, k_max, sel_stride_max)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def dev_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_dev_status(st: torch.Tensor, what: str = "device"):
+    v = int(st.item())
+    if v != TB_OK:
+        raise TBError(v, what)
+
+
+# ------------------------------------------------------------------ calls
+
+def tb_project_append(shape: Shape, K_src, src_stride: int, Wk, Kp, pos0: int, n_new: int, ws=None,
+                      dev_status=None, stream=None, K_src_offset_rows: int = 0):
+    """Kp[:, :, pos0:pos0+n_new] = RNE(K_src rows . Wk). K_src is [B,Hkv,src_stride,D] (rows from K_src_offset_rows)."""
+    lib = load_library()
+    if K_src.dtype != torch.bfloat16:
+        raise TypeError("K_src must be bfloat16")
+    base = _ptr(K_src).value + K_src_offset_rows * shape.D * 2
+    wsp = _ptr(ws) if ws is not None else None
+    wsb = ws.numel() if ws is not None else 0
+    _check(lib.tb_project_append(ctypes.byref(shape.c()), ctypes.c_void_p(base), src_stride, _bf16(Wk, "Wk"),
+                                 _bf16(Kp, "Kp"), pos0, n_new, wsp, wsb, _status_ptr(dev_status),
+                                 _stream(stream)), "tb_project_append")
+
+
+def tb_score(shape: Shape, q_imp, Kp, n: int, s, agg: int = TB_AGG_MEAN, dev_status=None, stream=None):
+    if s.dtype != torch.float32:
+        raise TypeError("s must be float32")
+    _check(load_library().tb_score(ctypes.byref(shape.c()), _bf16(q_imp, "q_imp"), _bf16(Kp, "Kp"), n, agg,
+                                   _ptr(s), _status_ptr(dev_status), _stream(stream)), "tb_score")
+
+
+def tb_topk(shape: Shape, s, n: int, k: int, idx, ws, dev_status=None, stream=None):
+    if s.dtype != torch.float32:
+        raise TypeError("s must be float32")
+    _check(load_library().tb_topk(ctypes.byref(shape.c()), _ptr(s), n, k, _i32(idx, "idx"), _ptr(ws), ws.numel(),
+                                  _status_ptr(dev_status), _stream(stream)), "tb_topk")
+
+
+def tb_expand(shape: Shape, idx, k: int, r: int, n_pred: int, n_t: int, sel, sel_stride: int, counts,
+              dev_status=None, stream=None):
+    _check(load_library().tb_expand(ctypes.byref(shape.c()), _i32(idx, "idx"), k, r, n_pred, n_t,
+                                    _i32(sel, "sel"), sel_stride, _i32(counts, "counts"),
+                                    _status_ptr(dev_status), _stream(stream)), "tb_expand")
+
+
+def tb_sparse_decode_attn(shape: Shape, q, K, V, sel, counts, sel_stride: int, scale: float, out, ws,
+                          dev_status=None, stream=None):
+    _check(load_library().tb_sparse_decode_attn(
+        ctypes.byref(shape.c()), _bf16(q, "q"), _bf16(K, "K"), _bf16(V, "V"), _i32(sel, "sel"),
+        _i32(counts, "counts"), sel_stride, scale, _bf16(out, "out"), _ptr(ws), ws.numel(),
+        _status_ptr(dev_status), _stream(stream)), "tb_sparse_decode_attn")
+
+
+def tb_decode_step(shape: Shape, k: int, T: int, r: int, agg: int, scale: float, t: int, n: int, *, q, q_imp,
+                   K_new, V_new, Wk, K, V, Kp, idx_state, n_pred: "ctypes.c_int64", sel, sel_stride: int, counts,
+                   out, ws, dev_status=None, stream=None):
+    """One decode step of one layer (see include/tb.h). n_pred is a ctypes.c_int64 carried across steps."""
+    params = _StepParams(k, T, r, agg, scale)
+    _check(load_library().tb_decode_step(
+        ctypes.byref(shape.c()), ctypes.byref(params), t, n, _bf16(q, "q"), _bf16(q_imp, "q_imp"),
+        _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"), _bf16(K, "K"), _bf16(V, "V"),
+        _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.byref(n_pred), _i32(sel, "sel"), sel_stride,
+        _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), ws.numel(), _status_ptr(dev_status),
+        _stream(stream)), "tb_decode_step")
+
+
+def sel_stride_for(k: int, T: int, r: int, n_max: int) -> int:
+    """Selection row length that every step of an interval fits in."""
+    return min(n_max + 1, k * (2 * r + 1)) + T - 1
+
+
+class DecodeLayer:
+    """Per-layer decode state on the device: the selection reused across a prediction interval."""
+
+    def __init__(self, shape: Shape, k: int, T: int = 1, r: int = 0, agg: int = TB_AGG_MEAN,
+                 scale: float | None = None, n_max: int | None = None, device=None):
+        self.shape, self.k, self.T, self.r, self.agg = shape, k, T, r, agg
+        self.scale = scale if scale is not None else shape.D ** -0.5
+        n_max = shape.cap - 1 if n_max is None else n_max
+        dev = device or "cuda"
+        rows = (shape.B, shape.Hkv)
+        self.sel_stride = sel_stride_for(k, T, r, n_max)
+        self.idx_state = torch.zeros(rows + (k,), dtype=torch.int32, device=dev)
+        self.sel = torch.zeros(rows + (self.sel_stride,), dtype=torch.int32, device=dev)
+        self.counts = torch.zeros(rows, dtype=torch.int32, device=dev)
+        self.n_pred = ctypes.c_int64(0)
+        self.ws = workspace(shape, n_max, k, self.sel_stride, device=dev)
+        self.status = dev_status(dev)
+
+    def step(self, t: int, n: int, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, out, stream=None):
+        tb_decode_step(self.shape, self.k, self.T, self.r, self.agg, self.scale, t, n, q=q, q_imp=q_imp,
+                       K_new=K_new, V_new=V_new, Wk=Wk, K=K, V=V, Kp=Kp, idx_state=self.idx_state,
+                       n_pred=self.n_pred, sel=self.sel, sel_stride=self.sel_stride, counts=self.counts, out=out,
+                       ws=self.ws, dev_status=self.status, stream=stream)
+        return out

@@ -1,0 +1,45 @@
+// Launchers of the libtb kernels (host side, internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tb.h"
+#include "ws_layout.cuh"
+
+namespace tb {
+
+cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16_t *Kp, int64_t n, int agg,
+                         float *s, int64_t lds, cudaStream_t st);
+
+// rows x n scores (row stride lds) -> rows x k ascending indices.
+cudaError_t launch_topk(int rows, const float *s, int64_t lds, int64_t n, int32_t k, int32_t *idx, RowCtl *ctl,
+                        int32_t *dev_status, cudaStream_t st);
+
+cudaError_t launch_expand(int rows, const int32_t *idx, int32_t k, int32_t r, int64_t n_pred, int64_t n_t,
+                          int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status, cudaStream_t st);
+
+cudaError_t launch_attn(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                        const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale, uint16_t *out,
+                        uint32_t *attn_ctl, float *partials, int32_t *dev_status, cudaStream_t st);
+
+// One new row per (b, h): cache writes, its projection and (optionally) the
+// tail entry of the selection.
+cudaError_t launch_append(const tb_shape &sh, const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk,
+                          uint16_t *K, uint16_t *V, uint16_t *Kp, int64_t pos, int32_t *sel, int32_t sel_stride,
+                          int32_t *counts, int32_t *dev_status, cudaStream_t st);
+
+// Kp rows [pos0, pos0 + n_new) from K_src (row stride src_stride per head).
+cudaError_t launch_project(const tb_shape &sh, const uint16_t *K_src, int64_t src_stride, const uint16_t *Wk,
+                           uint16_t *Kp, int64_t pos0, int64_t n_new, int32_t *dev_status, cudaStream_t st);
+
+// The whole decode step (T == 1, r == 0) as one cooperative kernel.
+bool fused_step_supported(const tb_shape &sh, int64_t n_tokens, int32_t k);
+int64_t fused_chunks(const tb_shape &sh, int64_t n_tokens);
+cudaError_t launch_fused_step(const tb_shape &sh, const tb_step_params &p, int64_t n, const uint16_t *q,
+                              const uint16_t *q_imp, const uint16_t *K_new, const uint16_t *V_new,
+                              const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx_state,
+                              int32_t *sel, int32_t *counts, uint16_t *out, RowCtl *ctl, uint32_t *attn_ctl,
+                              float *partials, int32_t *dev_status, cudaStream_t st);
+
+}  // namespace tb

@@ -1,0 +1,226 @@
+// C ABI of libtb: argument checks, workspace carving and launches.
+#include <cuda_runtime.h>
+
+#include "kernels.cuh"
+#include "tb_internal.cuh"
+#include "ws_layout.cuh"
+
+namespace tb {
+
+const DevInfo &dev_info() {
+    static thread_local DevInfo info;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return info;
+    if (info.device != dev) {
+        info.device = dev;
+        cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&info.l2_bytes, cudaDevAttrL2CacheSize, dev);
+        cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    }
+    return info;
+}
+
+static tb_status check_shape(const tb_shape *s) {
+    if (!s) return TB_ERR_INVALID_ARG;
+    if (s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->D <= 0 || s->dp <= 0 || s->cap <= 0) return TB_ERR_INVALID_ARG;
+    if (s->Hq % s->Hkv != 0) return TB_ERR_INVALID_ARG;
+    if (s->Hq / s->Hkv > 16) return TB_ERR_UNSUPPORTED;
+    if (s->D % 8 != 0 || s->dp % 8 != 0 || s->D > 256 || s->dp > 256) return TB_ERR_UNSUPPORTED;
+    // attention groups of D/8 lanes must tile a warp
+    const int tpg = s->D / 8;
+    if (32 % tpg != 0) return TB_ERR_UNSUPPORTED;
+    if (s->cap >= (int64_t)1 << 31) return TB_ERR_UNSUPPORTED;
+    if ((int64_t)s->B * s->Hkv > (1 << 16)) return TB_ERR_UNSUPPORTED;
+    return TB_OK;
+}
+
+static tb_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return TB_OK;
+    if (e == cudaErrorInvalidValue) return TB_ERR_UNSUPPORTED;
+    return TB_ERR_CUDA;
+}
+
+#define TB_CHECK(x)                      \
+    do {                                 \
+        tb_status _st = (x);             \
+        if (_st != TB_OK) return _st;    \
+    } while (0)
+
+#define TB_PTR(p)                                                   \
+    do {                                                            \
+        if (!(p)) return TB_ERR_INVALID_ARG;                        \
+        if (!aligned16(p)) return TB_ERR_UNSUPPORTED;               \
+    } while (0)
+
+static WsLayout layout_for(const tb_shape &s, int64_t n_scores, int64_t sel_stride, int64_t fused_chunks_max) {
+    return ws_layout(s, n_scores, sel_stride, fused_chunks_max);
+}
+
+}  // namespace tb
+
+using namespace tb;
+
+extern "C" {
+
+const char *tb_status_string(tb_status st) {
+    switch (st) {
+        case TB_OK: return "ok";
+        case TB_ERR_INVALID_ARG: return "invalid argument";
+        case TB_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+        case TB_ERR_WORKSPACE: return "workspace missing or too small";
+        case TB_ERR_CUDA: return "CUDA runtime error";
+        case TB_ERR_TIMEOUT: return "device-side wait timed out";
+        case TB_ERR_NONFINITE: return "non-finite (NaN) importance score";
+    }
+    return "unknown status";
+}
+
+int32_t tb_version(void) { return 1; }
+
+tb_status tb_workspace_size(const tb_shape *shape, int64_t n_max, int32_t k_max, int32_t sel_stride_max,
+                            size_t *bytes) {
+    TB_CHECK(check_shape(shape));
+    if (!bytes || n_max < 0 || k_max < 0 || sel_stride_max < 0) return TB_ERR_INVALID_ARG;
+    int64_t ss = sel_stride_max > k_max ? sel_stride_max : k_max;
+    const int64_t n_tok = n_max + 1;   // a decode step scores the appended token too
+    *bytes = layout_for(*shape, n_tok, ss, fused_chunks(*shape, n_tok)).total;
+    return TB_OK;
+}
+
+tb_status tb_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!ws || ws_bytes == 0) return TB_ERR_INVALID_ARG;
+    return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+}
+
+tb_status tb_project_append(const tb_shape *shape, const tb_bf16 *K_src, int64_t src_stride, const tb_bf16 *Wk,
+                            tb_bf16 *Kp, int64_t pos0, int64_t n_new, void *ws, size_t ws_bytes,
+                            int32_t *dev_status, cudaStream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    TB_CHECK(check_shape(shape));
+    if (n_new < 0 || pos0 < 0 || pos0 + n_new > shape->cap || n_new > src_stride) return TB_ERR_INVALID_ARG;
+    if (n_new == 0) return TB_OK;
+    TB_PTR(K_src);
+    TB_PTR(Wk);
+    TB_PTR(Kp);
+    const size_t smem = ((size_t)shape->D * shape->dp + 64 * (size_t)(shape->D + 1)) * sizeof(float);
+    if (smem > 227 * 1024) return TB_ERR_UNSUPPORTED;
+    return from_cuda(launch_project(*shape, K_src, src_stride, Wk, Kp, pos0, n_new, dev_status, stream));
+}
+
+tb_status tb_score(const tb_shape *shape, const tb_bf16 *q_imp, const tb_bf16 *Kp, int64_t n, int32_t agg,
+                   float *s, int32_t *dev_status, cudaStream_t stream) {
+    (void)dev_status;
+    TB_CHECK(check_shape(shape));
+    if (n < 0 || n > shape->cap) return TB_ERR_INVALID_ARG;
+    if (agg != TB_AGG_MEAN && agg != TB_AGG_MAX) return TB_ERR_INVALID_ARG;
+    if (n == 0) return TB_OK;
+    TB_PTR(q_imp);
+    TB_PTR(Kp);
+    if (!s) return TB_ERR_INVALID_ARG;
+    return from_cuda(launch_score(*shape, q_imp, Kp, n, agg, s, n, stream));
+}
+
+tb_status tb_topk(const tb_shape *shape, const float *s, int64_t n, int32_t k, int32_t *idx, void *ws,
+                  size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    TB_CHECK(check_shape(shape));
+    if (n < 0 || k < 0 || k > n) return TB_ERR_INVALID_ARG;
+    if (k == 0) return TB_OK;
+    if (!s || !idx) return TB_ERR_INVALID_ARG;
+    if (n >= ((int64_t)1 << 31) - 1) return TB_ERR_UNSUPPORTED;
+    const WsLayout L = layout_for(*shape, 0, 1, 0);
+    if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
+    RowCtl *ctl = reinterpret_cast<RowCtl *>(static_cast<uint8_t *>(ws) + L.rowctl_off);
+    return from_cuda(launch_topk(shape->B * shape->Hkv, s, n, n, k, idx, ctl, dev_status, stream));
+}
+
+tb_status tb_expand(const tb_shape *shape, const int32_t *idx, int32_t k, int32_t r, int64_t n_pred, int64_t n_t,
+                    int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status, cudaStream_t stream) {
+    TB_CHECK(check_shape(shape));
+    if (k < 0 || r < 0 || n_pred < 0 || n_t < n_pred || sel_stride <= 0 || n_t > shape->cap) return TB_ERR_INVALID_ARG;
+    if ((k > 0 && !idx) || !sel || !counts) return TB_ERR_INVALID_ARG;
+    return from_cuda(launch_expand(shape->B * shape->Hkv, idx, k, r, n_pred, n_t, sel, sel_stride, counts,
+                                   dev_status, stream));
+}
+
+tb_status tb_sparse_decode_attn(const tb_shape *shape, const tb_bf16 *q, const tb_bf16 *K, const tb_bf16 *V,
+                                const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
+                                tb_bf16 *out, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                cudaStream_t stream) {
+    TB_CHECK(check_shape(shape));
+    if (sel_stride <= 0 || !sel) return TB_ERR_INVALID_ARG;
+    TB_PTR(q);
+    TB_PTR(K);
+    TB_PTR(V);
+    TB_PTR(out);
+    const WsLayout L = layout_for(*shape, 0, sel_stride, 0);
+    if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    return from_cuda(launch_attn(*shape, q, K, V, sel, counts, sel_stride, scale, out,
+                                 reinterpret_cast<uint32_t *>(w + L.attn_ctl_off),
+                                 reinterpret_cast<float *>(w + L.part_off), dev_status, stream));
+}
+
+tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t t, int64_t n, const tb_bf16 *q,
+                         const tb_bf16 *q_imp, const tb_bf16 *K_new, const tb_bf16 *V_new, const tb_bf16 *Wk,
+                         tb_bf16 *K, tb_bf16 *V, tb_bf16 *Kp, int32_t *idx_state, int64_t *n_pred, int32_t *sel,
+                         int32_t sel_stride, int32_t *counts, tb_bf16 *out, void *ws, size_t ws_bytes,
+                         int32_t *dev_status, cudaStream_t stream) {
+    TB_CHECK(check_shape(shape));
+    if (!p || !n_pred || !idx_state || !sel || !counts) return TB_ERR_INVALID_ARG;
+    if (p->T < 1 || p->r < 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
+    if (t < 0 || n < 0 || n + 1 > shape->cap) return TB_ERR_INVALID_ARG;
+    TB_PTR(q);
+    TB_PTR(q_imp);
+    TB_PTR(K_new);
+    TB_PTR(V_new);
+    TB_PTR(Wk);
+    TB_PTR(K);
+    TB_PTR(V);
+    TB_PTR(Kp);
+    TB_PTR(out);
+    const int64_t n_t = n + 1;
+    const bool predict = (t % p->T) == 0;
+    if (predict && p->k > n_t) return TB_ERR_INVALID_ARG;
+    if (!predict && (*n_pred <= 0 || *n_pred > n)) return TB_ERR_INVALID_ARG;   // a step of this interval is missing
+    const int64_t np = predict ? n_t : *n_pred;
+    int64_t body = (int64_t)p->k * (2 * (int64_t)p->r + 1);
+    if (body > np) body = np;
+    if ((int64_t)sel_stride < body + (n_t - np)) return TB_ERR_INVALID_ARG;
+    const int rows = shape->B * shape->Hkv;
+    const bool fused = predict && p->T == 1 && p->r == 0 && fused_step_supported(*shape, n_t, p->k);
+    const WsLayout L = layout_for(*shape, n_t, sel_stride, fused ? fused_chunks(*shape, n_t) : 0);
+    if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    RowCtl *ctl = reinterpret_cast<RowCtl *>(w + L.rowctl_off);
+    uint32_t *actl = reinterpret_cast<uint32_t *>(w + L.attn_ctl_off);
+    float *part = reinterpret_cast<float *>(w + L.part_off);
+    float *scores = reinterpret_cast<float *>(w + L.scores_off);
+    cudaError_t e;
+    if (fused) {
+        e = launch_fused_step(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, sel, counts, out, ctl,
+                              actl, part, dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        *n_pred = n_t;
+        return TB_OK;
+    }
+    // 1. append (and, inside an interval, the tail entry of the selection)
+    e = launch_append(*shape, K_new, V_new, Wk, K, V, Kp, n, predict ? nullptr : sel, sel_stride, counts,
+                      dev_status, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (predict) {
+        // 2. score the n+1 tokens, select, widen
+        e = launch_score(*shape, q_imp, Kp, n_t, p->agg, scores, n_t, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = launch_topk(rows, scores, n_t, n_t, p->k, idx_state, ctl, dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = launch_expand(rows, idx_state, p->k, p->r, n_t, n_t, sel, sel_stride, counts, dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        *n_pred = n_t;
+    }
+    // 3. attention over the selection
+    e = launch_attn(*shape, q, K, V, sel, counts, sel_stride, p->scale, out, actl, part, dev_status, stream);
+    return from_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,282 @@
+// Distributed exact top-k (radix select) over one row held by a group of CTAs.
+//
+// Selection rule ("TokenButler: Token Importance is Predictable", arXiv
+// abstract: per-token selection under a fixed budget): keep the k tokens of
+// the row with the largest scores; ties go to the lower token index. Ordering
+// is by the 64-bit composite (key << 32) | (~token), key the order-preserving
+// image of the fp32 score, so every element has a distinct rank and the
+// selection is exactly that of a full sort.
+//
+// A row of n scores is split into C consecutive chunks of L tokens, one per
+// CTA. Each CTA holds its chunk's keys in shared memory. Radix passes over
+// 11-bit digits build a global histogram per pass (one group barrier each)
+// until the bin holding the k-th element is small enough to be resolved from
+// a candidate list (one more barrier), which every CTA of the group then
+// resolves redundantly in shared memory. No CTA waits for a second launch.
+#pragma once
+
+#include "tb_internal.cuh"
+#include "ws_layout.cuh"
+
+namespace tb {
+
+// Shared-memory working set of one CTA of the group.
+struct SelectSmem {
+    uint32_t *keys;     // [L]   keys of this chunk
+    uint32_t *hist;     // [kRadixBins]
+    uint32_t *ckey;     // [kCandCap] candidate keys
+    uint32_t *cidx;     // [kCandCap] candidate tokens
+    uint32_t *ccount;   // [kMaxChunks] per-chunk count of selected candidates / prefix
+    uint32_t *scan;     // [33]
+    uint32_t *misc;     // [8]
+    int *abort_flag;    // [1]
+};
+
+// Result of the threshold search, identical in every CTA of the group.
+struct SelectResult {
+    int mode;           // 0: take composite >= compT; 1: ties by index (TIE)
+    uint64_t compT;     // mode 0 threshold
+    uint32_t tkey;      // mode 1: the tied key
+    uint32_t take;      // mode 1: tied elements this CTA keeps (lowest tokens first)
+    uint32_t offset;    // first output slot of this CTA
+    uint32_t count;     // outputs of this CTA
+    bool ok;            // false when a wait timed out
+};
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t tok) {
+    return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - tok);
+}
+
+// Find the bin b of `hist` (nbins <= kRadixBins, counts in smem) such that
+// the elements in bins above b number fewer than `need` and those in bins >= b
+// number at least `need`. Writes misc[0] = b, misc[1] = count above b,
+// misc[2] = count in b. All threads must call it (barriers inside).
+__device__ __forceinline__ void find_threshold_bin(const uint32_t *hist, uint32_t need, uint32_t *scan,
+                                                   uint32_t *misc) {
+    const int per = kRadixBins / blockDim.x;  // bins per thread, from the top
+    const int hi = kRadixBins - 1 - threadIdx.x * per;
+    uint32_t local = 0;
+    for (int j = 0; j < per; ++j) local += hist[hi - j];
+    uint32_t total;
+    uint32_t above = block_exclusive_scan(local, scan, total);
+    if (above < need && need <= above + local) {
+        uint32_t a = above;
+        for (int j = 0; j < per; ++j) {
+            uint32_t c = hist[hi - j];
+            if (need <= a + c) {
+                misc[0] = (uint32_t)(hi - j);
+                misc[1] = a;
+                misc[2] = c;
+                break;
+            }
+            a += c;
+        }
+    }
+    __syncthreads();
+}
+
+// Radix select among `m` candidates in smem over the low `rbits` (<= 64)
+// bits of their composites (the bits above are equal for all of them).
+// Returns the composite threshold's low part: exactly `need` candidates have
+// low part >= the result. All threads must call it.
+__device__ __forceinline__ uint64_t local_select(const uint32_t *ckey, const uint32_t *cidx, uint32_t m,
+                                                 uint32_t need, int shift, SelectSmem &S) {
+    // low part of a candidate: ((key & (2^shift - 1)) << 32) | ~token  (shift + 32 bits)
+    const uint32_t kmask = shift >= 32 ? 0xFFFFFFFFu : ((1u << shift) - 1u);
+    int rem = shift + 32;
+    uint64_t pre = 0;
+    uint32_t need_l = need;
+    while (rem > 0) {
+        const int bits = rem >= kRadixBits ? kRadixBits : rem;
+        rem -= bits;
+        for (int b = threadIdx.x; b < kRadixBins; b += blockDim.x) S.hist[b] = 0;
+        __syncthreads();
+        const int upper = rem + bits;
+        for (uint32_t e = threadIdx.x; e < m; e += blockDim.x) {
+            uint64_t v = ((uint64_t)(ckey[e] & kmask) << 32) | (uint64_t)(0xFFFFFFFFu - cidx[e]);
+            uint64_t top = upper >= 64 ? 0 : (v >> upper);
+            if (top == pre) atomicAdd(&S.hist[(uint32_t)(v >> rem) & ((1u << bits) - 1u)], 1u);
+        }
+        __syncthreads();
+        find_threshold_bin(S.hist, need_l, S.scan, S.misc);
+        const uint32_t b = S.misc[0], above = S.misc[1], cnt = S.misc[2];
+        need_l -= above;
+        pre = (pre << bits) | b;
+        __syncthreads();
+        if (cnt == need_l) return pre << rem;   // the whole bin is kept
+    }
+    return pre;
+}
+
+// The group's threshold search. Keys of this CTA's chunk are in S.keys[0..Lc).
+// chunk c of C, chunk length L (tokens c*L .. c*L+Lc-1), budget k (1 <= k <= n).
+__device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S, int Lc, int L, int c, int C,
+                                                     uint32_t k, int32_t *dev_status) {
+    SelectResult R;
+    R.ok = true;
+    uint32_t prefix = 0, need = k, bincount = 0;
+    int shift = 32;
+    int nbar = 0;
+    // ---- global radix passes
+    for (int pass = 0; pass < 3; ++pass) {
+        const int bits = pass < 2 ? kRadixBits : 32 - 2 * kRadixBits;
+        const int upper = shift;   // bits above this pass's digit are fixed to `prefix`
+        shift -= bits;
+        for (int b = threadIdx.x; b < kRadixBins; b += blockDim.x) S.hist[b] = 0;
+        __syncthreads();
+        for (int e = threadIdx.x; e < Lc; e += blockDim.x) {
+            uint32_t key = S.keys[e];
+            bool match = (upper >= 32) || ((key >> upper) == prefix);
+            if (match) atomicAdd(&S.hist[(key >> shift) & ((1u << bits) - 1u)], 1u);
+        }
+        __syncthreads();
+        for (int b = threadIdx.x; b < kRadixBins; b += blockDim.x) {
+            uint32_t v = S.hist[b];
+            if (v) atomicAdd(&ctl->hist[pass][b], v);
+        }
+        ++nbar;
+        if (!group_barrier(&ctl->bar, (uint32_t)(nbar * C), S.abort_flag, dev_status)) { R.ok = false; return R; }
+        for (int b = threadIdx.x; b < kRadixBins; b += blockDim.x) S.hist[b] = __ldcg(&ctl->hist[pass][b]);
+        __syncthreads();
+        find_threshold_bin(S.hist, need, S.scan, S.misc);
+        const uint32_t b = S.misc[0], above = S.misc[1];
+        bincount = S.misc[2];
+        need -= above;
+        prefix = (prefix << bits) | b;
+        __syncthreads();
+        if (bincount <= (uint32_t)kCandCap || bincount == need) break;
+    }
+    // ---- classify this chunk against the threshold bin, publish counts
+    const int mode_all = (bincount == need);
+    const int mode_cand = !mode_all && bincount <= (uint32_t)kCandCap;
+    uint32_t my_above = 0, my_eq = 0;
+    for (int e = threadIdx.x; e < Lc; e += blockDim.x) {
+        uint32_t top = S.keys[e] >> shift;   // shift < 32 here
+        if (top > prefix) {
+            ++my_above;
+        } else if (top == prefix) {
+            ++my_eq;
+            if (mode_cand) {
+                uint32_t slot = atomicAdd(&ctl->ncand, 1u);
+                if (slot < (uint32_t)kCandCap) ctl->cand[slot] = make_uint2(S.keys[e], (uint32_t)(c * L + e));
+            }
+        }
+    }
+    uint32_t tot;
+    (void)block_exclusive_scan(my_above, S.scan, tot);
+    const uint32_t chunk_above = tot;
+    (void)block_exclusive_scan(my_eq, S.scan, tot);
+    const uint32_t chunk_eq = tot;
+    if (threadIdx.x == 0) {
+        ctl->above[c] = chunk_above;
+        ctl->eq[c] = chunk_eq;
+    }
+    ++nbar;
+    if (!group_barrier(&ctl->bar, (uint32_t)(nbar * C), S.abort_flag, dev_status)) { R.ok = false; return R; }
+    // ---- every CTA resolves the threshold and all chunk counts
+    if (mode_cand) {
+        const uint32_t m = bincount;
+        for (uint32_t e = threadIdx.x; e < m; e += blockDim.x) {
+            uint2 v = __ldcg(&ctl->cand[e]);
+            S.ckey[e] = v.x;
+            S.cidx[e] = v.y;
+        }
+        for (int j = threadIdx.x; j < C; j += blockDim.x) S.ccount[j] = 0;
+        __syncthreads();
+        const uint64_t low = local_select(S.ckey, S.cidx, m, need, shift, S);
+        const uint64_t hi_part = (uint64_t)(prefix << shift) << 32;   // shift <= 21 here
+        R.compT = hi_part + low;
+        for (uint32_t e = threadIdx.x; e < m; e += blockDim.x)
+            if (composite(S.ckey[e], S.cidx[e]) >= R.compT) atomicAdd(&S.ccount[S.cidx[e] / (uint32_t)L], 1u);
+        __syncthreads();
+        for (int j = threadIdx.x; j < C; j += blockDim.x) S.ccount[j] += __ldcg(&ctl->above[j]);
+        R.mode = 0;
+    } else if (mode_all) {
+        R.compT = (uint64_t)(prefix << shift) << 32;
+        for (int j = threadIdx.x; j < C; j += blockDim.x) S.ccount[j] = __ldcg(&ctl->above[j]) + __ldcg(&ctl->eq[j]);
+        R.mode = 0;
+    } else {
+        // all 32 key bits resolved (shift == 0) and more tied elements than
+        // the budget has room for: keep the lowest tokens, chunk by chunk
+        R.mode = 1;
+        R.tkey = prefix;
+        if (threadIdx.x == 0) {
+            uint32_t left = need;
+            for (int j = 0; j < C; ++j) {
+                uint32_t e = __ldcg(&ctl->eq[j]);
+                uint32_t t = e < left ? e : left;
+                left -= t;
+                S.ccount[j] = __ldcg(&ctl->above[j]) + t;
+                if (j == c) S.misc[3] = t;
+            }
+        }
+    }
+    __syncthreads();
+    if (R.mode == 1) R.take = S.misc[3];
+    // exclusive prefix over chunks -> this CTA's output offset
+    if (threadIdx.x == 0) {
+        uint32_t off = 0;
+        for (int j = 0; j < c; ++j) off += S.ccount[j];
+        S.misc[4] = off;
+        S.misc[5] = S.ccount[c];
+    }
+    __syncthreads();
+    R.offset = S.misc[4];
+    R.count = S.misc[5];
+    __syncthreads();
+    return R;
+}
+
+// Is element e (key, token) of this chunk kept? For mode 1 the caller passes
+// the number of tied elements before it in the chunk.
+__device__ __forceinline__ bool is_kept(const SelectResult &R, uint32_t key, uint32_t tok, uint32_t tied_before) {
+    if (R.mode == 0) return composite(key, tok) >= R.compT;
+    if (key > R.tkey) return true;
+    return key == R.tkey && tied_before < R.take;
+}
+
+// Write the kept tokens of this chunk, ascending, to out[R.offset ...]. The
+// chunk's keys are in S.keys; token of element e is tok0 + e.
+__device__ __forceinline__ void write_kept(const SelectResult &R, SelectSmem &S, int Lc, uint32_t tok0,
+                                          int32_t *out) {
+    uint32_t base_kept = 0, base_tied = 0;
+    for (int t0 = 0; t0 < Lc; t0 += blockDim.x) {
+        const int e = t0 + threadIdx.x;
+        uint32_t key = 0;
+        uint32_t tied = 0;
+        if (e < Lc) {
+            key = S.keys[e];
+            tied = (R.mode == 1 && key == R.tkey) ? 1u : 0u;
+        }
+        uint32_t ttot;
+        const uint32_t tied_before = base_tied + block_exclusive_scan(tied, S.scan, ttot);
+        const uint32_t kept = (e < Lc && is_kept(R, key, tok0 + (uint32_t)e, tied_before)) ? 1u : 0u;
+        uint32_t ktot;
+        const uint32_t pos = block_exclusive_scan(kept, S.scan, ktot);
+        if (kept) out[R.offset + base_kept + pos] = (int32_t)(tok0 + (uint32_t)e);
+        base_kept += ktot;
+        base_tied += ttot;
+    }
+}
+
+// Last CTA of the group to arrive puts the row's control block back to zero.
+__device__ __forceinline__ void group_release(RowCtl *ctl, int C, SelectSmem &S) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        uint32_t prev = atomicAdd(&ctl->done, 1u);
+        S.misc[6] = (prev == (uint32_t)(C - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (S.misc[6]) {
+        __threadfence();
+        for (int b = threadIdx.x; b < 3 * kRadixBins; b += blockDim.x) (&ctl->hist[0][0])[b] = 0;
+        if (threadIdx.x == 0) {
+            ctl->bar = 0;
+            ctl->ncand = 0;
+            ctl->done = 0;
+        }
+    }
+}
+
+}  // namespace tb

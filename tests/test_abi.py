@@ -1,0 +1,65 @@
+"""The C-ABI library builds, loads and exports every entry point include/tb.h declares (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "tb.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"TB_API\s+[\w\s\*]*?\b(tb_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from predicted_token_importance_tb_b300 import build
+    return build.build()
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for n in ["tb_project_append", "tb_score", "tb_topk", "tb_sparse_decode_attn", "tb_decode_step"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], check=True, capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(tb_\w+)$", out, re.M))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+    lib = ctypes.CDLL(lib_path)
+    for n in _declared():
+        assert hasattr(lib, n)
+
+
+def test_binding_loads_and_reports(lib_path):
+    import predicted_token_importance_tb_b300 as tb
+    lib = tb.load_library()
+    assert lib.tb_version() == 1
+    assert tb.status_string(tb.TB_ERR_WORKSPACE) == "workspace missing or too small"
+    for n in tb.EXPORTED:
+        assert n in _declared()
+
+
+def test_host_validation_without_gpu(lib_path):
+    # Argument checks run before any CUDA call, so they answer on a CPU-only host.
+    import predicted_token_importance_tb_b300 as tb
+    lib = tb.load_library()
+    bad = tb.Shape(1, 6, 4, 128, 32, 100).c()       # Hq not a multiple of Hkv
+    sz = ctypes.c_size_t(0)
+    assert lib.tb_workspace_size(ctypes.byref(bad), 10, 4, 4, ctypes.byref(sz)) == tb.TB_ERR_INVALID_ARG
+    odd = tb.Shape(1, 8, 8, 60, 16, 100).c()        # D not a multiple of 8
+    assert lib.tb_workspace_size(ctypes.byref(odd), 10, 4, 4, ctypes.byref(sz)) == tb.TB_ERR_UNSUPPORTED
+    ok = tb.Shape(1, 32, 8, 128, 32, 32768).c()
+    assert lib.tb_workspace_size(ctypes.byref(ok), 32767, 3277, 3277, ctypes.byref(sz)) == tb.TB_OK
+    assert sz.value > 0
+    # k > n is rejected before launch; so is a missing workspace
+    assert lib.tb_topk(ctypes.byref(ok), ctypes.c_void_p(16), 10, 11, ctypes.c_void_p(16), None, 0, None,
+                       None) == tb.TB_ERR_INVALID_ARG
+    assert lib.tb_topk(ctypes.byref(ok), ctypes.c_void_p(16), 10, 5, ctypes.c_void_p(16), None, 0, None,
+                       None) == tb.TB_ERR_WORKSPACE

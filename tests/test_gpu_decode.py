@@ -1,0 +1,107 @@
+"""GPU parity of the whole decode step (append, predict every T steps, widen, attend) against the oracle."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import OUT_ATOL, assert_topk_end_to_end, bf16_ulp_diff, u16
+
+tb = pytest.importorskip("predicted_token_importance_tb_b300")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tb.load_library()
+
+
+def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=None, check_rows=None):
+    """Drive `steps` decode steps per layer on the GPU and check every step against the oracle.
+
+    The oracle starts from the GPU-projected prefix of Kp (identical inputs),
+    projects each appended row itself, and makes its own selections; top-k
+    sets are compared under the tie band, the selection rows exactly against
+    the oracle's expansion of the GPU's prediction, and the output against the
+    oracle's attention over the GPU's selection.
+    """
+    k = w.k if k is None else k
+    cap = n0 + steps
+    shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, cap)
+    for layer in layers:
+        L = synth.make_layer(w, layer=layer, cap=cap, n=n0)
+        K, V, Wk = L["K"].cuda(), L["V"].cuda(), L["Wk"].cuda()
+        Kp = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
+        tb.tb_project_append(shape, K, cap, Wk, Kp, 0, n0)
+        dec = tb.DecodeLayer(shape, k, T=w.T, r=w.r, scale=w.scale, n_max=cap - 1)
+        out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+        oK, oV = u16(L["K"]).copy(), u16(L["V"]).copy()
+        oKp = u16(Kp).copy()
+        st = oracle.DecodeState()
+        for t in range(steps):
+            n = n0 + t
+            d = synth.make_step(w, layer, t, L["outlier_ch"])
+            dec.step(t, n, q=d["q"].cuda(), q_imp=d["q_imp"].cuda(), K_new=d["K_new"].cuda(),
+                     V_new=d["V_new"].cuda(), Wk=Wk, K=K, V=V, Kp=Kp, out=out)
+            torch.cuda.synchronize()
+            tb.check_dev_status(dec.status, f"layer {layer} step {t}")
+            ref_out, ref_sel, ref_cnt = oracle.decode_step(
+                st, t, n, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=L["Wk"], K=oK, V=oV,
+                Kp=oKp, k=k, T=w.T, r=w.r, agg=oracle.AGG_MEAN, scale=w.scale)
+            # appended rows
+            gKp = u16(Kp[:, :, n])
+            assert bf16_ulp_diff(gKp, oKp[:, :, n]).max() <= 1
+            assert np.array_equal(u16(K[:, :, n]), oK[:, :, n])
+            n_t = n + 1
+            assert dec.n_pred.value == st.n_pred
+            gidx = dec.idx_state.cpu().numpy()
+            if t % w.T == 0:
+                s_ref, _ = oracle.score(d["q_imp"], np.ascontiguousarray(oKp[:, :, :n_t]))
+                assert_topk_end_to_end(gidx, s_ref, k)
+            # selection = the oracle's expansion of the GPU's prediction, plus the tail
+            want_sel, want_cnt = oracle.expand(gidx, w.r, st.n_pred, n_t, sel_stride=dec.sel_stride)
+            gcnt = dec.counts.cpu().numpy()
+            gsel = dec.sel.cpu().numpy()
+            assert np.array_equal(gcnt, want_cnt)
+            for b in range(w.B):
+                for h in range(w.Hkv):
+                    assert np.array_equal(gsel[b, h, :gcnt[b, h]], want_sel[b, h, :gcnt[b, h]])
+            # output over the GPU's selection
+            ref_g = oracle.attn(d["q"], oK, oV, gsel, gcnt, w.scale)
+            got = out.float().cpu().numpy()
+            assert np.abs(got - ref_g).max() <= OUT_ATOL, (layer, t)
+            # and the end-to-end output where the predictions agree
+            if np.array_equal(gidx, st.idx):
+                assert np.abs(got - ref_out).max() <= OUT_ATOL
+
+
+def test_decode_small_per_step():
+    w = synth.WORKLOADS[0]
+    run_decode_parity(w, n0=w.N - 1, steps=3)
+
+
+def test_decode_small_interval_with_neighbours():
+    w = synth.small(B=2, Hq=8, Hkv=2, D=128, dp=32, N=3000, k=100, T=4, r=1, seed=31, outliers=4)
+    run_decode_parity(w, n0=w.N, steps=10)
+
+
+def test_decode_interval_r2_group_of_one():
+    w = synth.small(B=1, Hq=4, Hkv=4, D=64, dp=16, N=1500, k=40, T=3, r=2, seed=32)
+    run_decode_parity(w, n0=w.N, steps=7)
+
+
+def test_decode_llama_layer_step():
+    # the 32K-token Llama-3-8B-shaped layer: one step at N = 32768 after the append
+    w = synth.WORKLOADS[1]
+    run_decode_parity(w, n0=w.N - 1, steps=2)
+
+
+def test_decode_32layer_stack_interval_sampled_layers():
+    # the 32-layer B=8 stack at full per-layer shape: layers 0 and 31, all 64 steps
+    w = synth.WORKLOADS[2]
+    run_decode_parity(w, n0=w.N, steps=w.steps, layers=(0, 31))
