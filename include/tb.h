@@ -81,7 +81,12 @@ typedef struct {
     int32_t r;      /* neighbour radius, >= 0 */
     int32_t agg;    /* TB_AGG_MEAN or TB_AGG_MAX */
     float scale;    /* softmax scale, normally 1/sqrt(D) */
+    int32_t flags;  /* 0, or TB_STEP_UNFUSED */
 } tb_step_params;
+
+/* tb_step_params.flags: run the step as separate kernels even where the
+   single fused launch applies (same results; for comparison and debugging). */
+#define TB_STEP_UNFUSED 1
 
 /* Text for a status code (static storage). */
 TB_API const char *tb_status_string(tb_status st);

@@ -31,6 +31,8 @@ TB_ERR_NONFINITE = 6
 TB_AGG_MEAN = 0
 TB_AGG_MAX = 1
 
+TB_STEP_UNFUSED = 1
+
 EXPORTED = (
     "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
     "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step",
@@ -50,7 +52,7 @@ class _Shape(ctypes.Structure):
 
 class _StepParams(ctypes.Structure):
     _fields_ = [("k", ctypes.c_int32), ("T", ctypes.c_int32), ("r", ctypes.c_int32),
-                ("agg", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("agg", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -224,9 +226,9 @@ def tb_sparse_decode_attn(shape: Shape, q, K, V, sel, counts, sel_stride: int, s
 
 def tb_decode_step(shape: Shape, k: int, T: int, r: int, agg: int, scale: float, t: int, n: int, *, q, q_imp,
                    K_new, V_new, Wk, K, V, Kp, idx_state, n_pred: "ctypes.c_int64", sel, sel_stride: int, counts,
-                   out, ws, dev_status=None, stream=None):
+                   out, ws, dev_status=None, stream=None, flags: int = 0):
     """One decode step of one layer (see include/tb.h). n_pred is a ctypes.c_int64 carried across steps."""
-    params = _StepParams(k, T, r, agg, scale)
+    params = _StepParams(k, T, r, agg, scale, flags)
     _check(load_library().tb_decode_step(
         ctypes.byref(shape.c()), ctypes.byref(params), t, n, _bf16(q, "q"), _bf16(q_imp, "q_imp"),
         _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"), _bf16(K, "K"), _bf16(V, "V"),
@@ -244,8 +246,9 @@ class DecodeLayer:
     """Per-layer decode state on the device: the selection reused across a prediction interval."""
 
     def __init__(self, shape: Shape, k: int, T: int = 1, r: int = 0, agg: int = TB_AGG_MEAN,
-                 scale: float | None = None, n_max: int | None = None, device=None):
+                 scale: float | None = None, n_max: int | None = None, device=None, fused: bool = True):
         self.shape, self.k, self.T, self.r, self.agg = shape, k, T, r, agg
+        self.flags = 0 if fused else TB_STEP_UNFUSED
         self.scale = scale if scale is not None else shape.D ** -0.5
         n_max = shape.cap - 1 if n_max is None else n_max
         dev = device or "cuda"
@@ -262,5 +265,5 @@ class DecodeLayer:
         tb_decode_step(self.shape, self.k, self.T, self.r, self.agg, self.scale, t, n, q=q, q_imp=q_imp,
                        K_new=K_new, V_new=V_new, Wk=Wk, K=K, V=V, Kp=Kp, idx_state=self.idx_state,
                        n_pred=self.n_pred, sel=self.sel, sel_stride=self.sel_stride, counts=self.counts, out=out,
-                       ws=self.ws, dev_status=self.status, stream=stream)
+                       ws=self.ws, dev_status=self.status, stream=stream, flags=self.flags)
         return out

@@ -40,6 +40,6 @@ cudaError_t launch_fused_step(const tb_shape &sh, const tb_step_params &p, int64
                               const uint16_t *q_imp, const uint16_t *K_new, const uint16_t *V_new,
                               const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx_state,
                               int32_t *sel, int32_t *counts, uint16_t *out, RowCtl *ctl, uint32_t *attn_ctl,
-                              float *partials, int32_t *dev_status, cudaStream_t st);
+                              float *partials, int32_t sel_stride, int32_t *dev_status, cudaStream_t st);
 
 }  // namespace tb

@@ -188,7 +188,8 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     if (body > np) body = np;
     if ((int64_t)sel_stride < body + (n_t - np)) return TB_ERR_INVALID_ARG;
     const int rows = shape->B * shape->Hkv;
-    const bool fused = predict && p->T == 1 && p->r == 0 && fused_step_supported(*shape, n_t, p->k);
+    const bool fused = predict && p->T == 1 && p->r == 0 && !(p->flags & TB_STEP_UNFUSED) &&
+                       fused_step_supported(*shape, n_t, p->k);
     const WsLayout L = layout_for(*shape, n_t, sel_stride, fused ? fused_chunks(*shape, n_t) : 0);
     if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -199,7 +200,7 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     cudaError_t e;
     if (fused) {
         e = launch_fused_step(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, sel, counts, out, ctl,
-                              actl, part, dev_status, stream);
+                              actl, part, sel_stride, dev_status, stream);
         if (e != cudaSuccess) return from_cuda(e);
         *n_pred = n_t;
         return TB_OK;

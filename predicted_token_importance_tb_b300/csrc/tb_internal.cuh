@@ -55,15 +55,20 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
 // Longest a device-side wait may spin before it gives up (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// Arrive on a counter shared by a group of CTAs and wait until it reaches
-// `target`. Bounded: after kWaitLimitNs the wait gives up, *abort (shared)
-// is set and TB_ERR_TIMEOUT is recorded. Returns false on timeout.
-__device__ __forceinline__ bool group_barrier(uint32_t *ctr, uint32_t target, int *abort_flag,
-                                              int32_t *dev_status) {
+// Split-phase group barrier on a counter shared by a group of CTAs: every CTA
+// arrives once per phase; a CTA waits until the counter reaches `target`
+// (phase count x group size). The wait is bounded: after kWaitLimitNs it
+// gives up, sets *abort_flag (shared) and records TB_ERR_TIMEOUT.
+__device__ __forceinline__ void group_arrive(uint32_t *ctr) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(ctr, 1u);
+    }
+}
+
+__device__ __forceinline__ bool group_wait(uint32_t *ctr, uint32_t target, int *abort_flag, int32_t *dev_status) {
+    if (threadIdx.x == 0) {
         uint64_t t0 = global_ns();
         while (ld_acquire(ctr) < target) {
             if (global_ns() - t0 > kWaitLimitNs) {
@@ -71,12 +76,18 @@ __device__ __forceinline__ bool group_barrier(uint32_t *ctr, uint32_t target, in
                 set_status(dev_status, TB_ERR_TIMEOUT);
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(32);
         }
         __threadfence();
     }
     __syncthreads();
     return *abort_flag == 0;
+}
+
+__device__ __forceinline__ bool group_barrier(uint32_t *ctr, uint32_t target, int *abort_flag,
+                                              int32_t *dev_status) {
+    group_arrive(ctr);
+    return group_wait(ctr, target, abort_flag, dev_status);
 }
 
 // ------------------------------------------------------------------ scans

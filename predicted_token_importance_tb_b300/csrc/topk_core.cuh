@@ -108,16 +108,30 @@ __device__ __forceinline__ uint64_t local_select(const uint32_t *ckey, const uin
     return pre;
 }
 
-// The group's threshold search. Keys of this CTA's chunk are in S.keys[0..Lc).
-// chunk c of C, chunk length L (tokens c*L .. c*L+Lc-1), budget k (1 <= k <= n).
-__device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S, int Lc, int L, int c, int C,
-                                                     uint32_t k, int32_t *dev_status) {
-    SelectResult R;
-    R.ok = true;
+// State carried from group_select_begin to group_select_end.
+struct SelectBegin {
+    uint32_t prefix;    // resolved top bits of the threshold bin
+    int shift;          // bits below them
+    uint32_t need;      // elements still needed from the bin
+    uint32_t bincount;  // elements in the bin (whole row)
+    int mode_all, mode_cand;
+    int nbar;           // group barriers used so far (the last one only arrived)
+    bool ok;
+};
+
+// First half of the group's threshold search: the global radix passes, then
+// this chunk's counts and candidates are published and the CTA ARRIVES on
+// the final barrier without waiting, so it can work on tokens that are kept
+// whatever the exact threshold (those above the bin) in the meantime.
+// Keys of this CTA's chunk are in S.keys[0..Lc). Chunk c of C covers tokens
+// c*L .. c*L+Lc-1; budget k with 1 <= k <= n.
+__device__ __forceinline__ SelectBegin group_select_begin(RowCtl *ctl, SelectSmem &S, int Lc, int L, int c, int C,
+                                                          uint32_t k, int32_t *dev_status) {
+    SelectBegin B;
+    B.ok = true;
     uint32_t prefix = 0, need = k, bincount = 0;
     int shift = 32;
     int nbar = 0;
-    // ---- global radix passes
     for (int pass = 0; pass < 3; ++pass) {
         const int bits = pass < 2 ? kRadixBits : 32 - 2 * kRadixBits;
         const int upper = shift;   // bits above this pass's digit are fixed to `prefix`
@@ -135,7 +149,7 @@ __device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S,
             if (v) atomicAdd(&ctl->hist[pass][b], v);
         }
         ++nbar;
-        if (!group_barrier(&ctl->bar, (uint32_t)(nbar * C), S.abort_flag, dev_status)) { R.ok = false; return R; }
+        if (!group_barrier(&ctl->bar, (uint32_t)(nbar * C), S.abort_flag, dev_status)) { B.ok = false; return B; }
         for (int b = threadIdx.x; b < kRadixBins; b += blockDim.x) S.hist[b] = __ldcg(&ctl->hist[pass][b]);
         __syncthreads();
         find_threshold_bin(S.hist, need, S.scan, S.misc);
@@ -146,7 +160,7 @@ __device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S,
         __syncthreads();
         if (bincount <= (uint32_t)kCandCap || bincount == need) break;
     }
-    // ---- classify this chunk against the threshold bin, publish counts
+    // classify this chunk against the threshold bin, publish counts
     const int mode_all = (bincount == need);
     const int mode_cand = !mode_all && bincount <= (uint32_t)kCandCap;
     uint32_t my_above = 0, my_eq = 0;
@@ -172,10 +186,31 @@ __device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S,
         ctl->eq[c] = chunk_eq;
     }
     ++nbar;
-    if (!group_barrier(&ctl->bar, (uint32_t)(nbar * C), S.abort_flag, dev_status)) { R.ok = false; return R; }
-    // ---- every CTA resolves the threshold and all chunk counts
-    if (mode_cand) {
-        const uint32_t m = bincount;
+    group_arrive(&ctl->bar);
+    B.prefix = prefix;
+    B.shift = shift;
+    B.need = need;
+    B.bincount = bincount;
+    B.mode_all = mode_all;
+    B.mode_cand = mode_cand;
+    B.nbar = nbar;
+    return B;
+}
+
+// Is this key above the threshold bin (kept whatever the exact threshold)?
+__device__ __forceinline__ bool above_bin(const SelectBegin &B, uint32_t key) { return (key >> B.shift) > B.prefix; }
+
+// Second half: wait for every chunk's counts, resolve the exact threshold
+// and this CTA's output slots (identically in every CTA of the group).
+__device__ __forceinline__ SelectResult group_select_end(RowCtl *ctl, SelectSmem &S, const SelectBegin &B, int L,
+                                                         int c, int C, int32_t *dev_status) {
+    SelectResult R;
+    R.ok = true;
+    if (!group_wait(&ctl->bar, (uint32_t)(B.nbar * C), S.abort_flag, dev_status)) { R.ok = false; return R; }
+    const uint32_t prefix = B.prefix, need = B.need;
+    const int shift = B.shift;
+    if (B.mode_cand) {
+        const uint32_t m = B.bincount;
         for (uint32_t e = threadIdx.x; e < m; e += blockDim.x) {
             uint2 v = __ldcg(&ctl->cand[e]);
             S.ckey[e] = v.x;
@@ -191,7 +226,7 @@ __device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S,
         __syncthreads();
         for (int j = threadIdx.x; j < C; j += blockDim.x) S.ccount[j] += __ldcg(&ctl->above[j]);
         R.mode = 0;
-    } else if (mode_all) {
+    } else if (B.mode_all) {
         R.compT = (uint64_t)(prefix << shift) << 32;
         for (int j = threadIdx.x; j < C; j += blockDim.x) S.ccount[j] = __ldcg(&ctl->above[j]) + __ldcg(&ctl->eq[j]);
         R.mode = 0;
@@ -225,6 +260,18 @@ __device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S,
     R.count = S.misc[5];
     __syncthreads();
     return R;
+}
+
+// The whole threshold search (both halves back to back).
+__device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S, int Lc, int L, int c, int C,
+                                                     uint32_t k, int32_t *dev_status) {
+    SelectBegin B = group_select_begin(ctl, S, Lc, L, c, C, k, dev_status);
+    if (!B.ok) {
+        SelectResult R;
+        R.ok = false;
+        return R;
+    }
+    return group_select_end(ctl, S, B, L, c, C, dev_status);
 }
 
 // Is element e (key, token) of this chunk kept? For mode 1 the caller passes

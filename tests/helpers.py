@@ -31,6 +31,29 @@ def bf16_ulp_diff(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     return np.abs(ordered(a_bits) - ordered(b_bits))
 
 
+def assert_kp_close(got_bits: np.ndarray, kp64: np.ndarray, l1: np.ndarray):
+    """Projected keys: within one bf16 ulp of RNE(exact), or, where the sum
+    cancels, within half a bf16 ulp plus the fp32 summation bound
+    1e-5 * sum_d |K_d W_dj| (D <= 256 terms: D * 2^-24 <= 1.6e-5, and the
+    kernels sum in blocks, which keeps them well inside it)."""
+    got = oracle.bf16_bits_to_f64(got_bits)
+    want_bits = oracle.bf16_round(kp64) if kp64.size < 4096 else None
+    err = np.abs(got - kp64)
+    half_ulp = np.maximum(np.abs(got), 2.0 ** -126) * 2.0 ** -8
+    ok = err <= 2 * half_ulp + 1e-30
+    ok |= err <= half_ulp + 1e-5 * l1
+    assert ok.all(), f"{(~ok).sum()} projected values out of tolerance, worst {err[~ok].max()}"
+    if want_bits is not None:
+        assert (got_bits != want_bits).mean() < 0.05
+
+
+def kp_l1(K_bits: np.ndarray, W_bits: np.ndarray) -> np.ndarray:
+    """sum_d |K[b,h,t,d] * W[h,d,j]| in fp64, the scale of the projection's rounding bound."""
+    Kf = np.abs(oracle.bf16_bits_to_f64(K_bits))
+    Wf = np.abs(oracle.bf16_bits_to_f64(W_bits))
+    return np.einsum("bhtd,hdj->bhtj", Kf, Wf)
+
+
 def assert_scores_close(s_gpu: np.ndarray, s_ref: np.ndarray, l1: np.ndarray):
     d = np.abs(s_gpu.astype(np.float64) - s_ref)
     ok = (d <= SCORE_REL * np.abs(s_ref)) | (d <= SCORE_ABS_L1 * l1)

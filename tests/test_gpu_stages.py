@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import synth
-from helpers import OUT_ATOL, assert_scores_close, bf16_ulp_diff, u16
+from helpers import OUT_ATOL, assert_kp_close, assert_scores_close, bf16_ulp_diff, kp_l1, u16
 
 tb = pytest.importorskip("predicted_token_importance_tb_b300")
 
@@ -42,8 +42,9 @@ def test_project_within_one_ulp(B, Hkv, n_new, D, dp, pos0):
     torch.cuda.synchronize()
     tb.check_dev_status(st)
     got = u16(Kp)[:, :, pos0:pos0 + n_new]
-    want, _ = oracle.project(np.ascontiguousarray(u16(K)[:, :, pos0:pos0 + n_new]), Wk)
-    assert bf16_ulp_diff(got, want).max() <= 1
+    Kin = np.ascontiguousarray(u16(K)[:, :, pos0:pos0 + n_new])
+    want, want64 = oracle.project(Kin, Wk)
+    assert_kp_close(got, want64, kp_l1(Kin, u16(Wk)))
     assert (got != want).mean() < 0.01
     # rows outside [pos0, pos0 + n_new) untouched
     assert not u16(Kp)[:, :, :pos0].any() and not u16(Kp)[:, :, pos0 + n_new:].any()

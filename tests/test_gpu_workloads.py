@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from helpers import OUT_ATOL, assert_scores_close, assert_topk_end_to_end, bf16_ulp_diff, u16
+from helpers import OUT_ATOL, assert_kp_close, assert_scores_close, assert_topk_end_to_end, kp_l1, u16
 
 tb = pytest.importorskip("predicted_token_importance_tb_b300")
 
@@ -52,8 +52,9 @@ def test_long_context_planted_heavy_hitters():
     gKp = u16(Kp)
     # projection: a sample of rows per head against the oracle
     rows = np.random.default_rng(0).choice(w.N, 1024, replace=False)
-    want, _ = oracle.project(np.ascontiguousarray(u16(L["K"])[:, :, rows]), L["Wk"])
-    assert bf16_ulp_diff(gKp[:, :, rows], want).max() <= 1
+    Kin = np.ascontiguousarray(u16(L["K"])[:, :, rows])
+    want, want64 = oracle.project(Kin, L["Wk"])
+    assert_kp_close(gKp[:, :, rows], want64, kp_l1(Kin, u16(L["Wk"])))
     s, idx, out = _select_attend(w, shape, L, K, V, Kp, w.k)
     s_ref, l1 = oracle.score(L["q_imp"], gKp)
     assert_scores_close(s, s_ref, l1)
@@ -71,8 +72,11 @@ def test_prefill_then_budget_sweep():
     shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, w.N)
     K, V, Wk, Kp = _prefill(w, L, shape)
     gKp = u16(Kp)
-    want, _ = oracle.project(L["K"], L["Wk"])
-    assert bf16_ulp_diff(gKp, want).max() <= 1
+    want, want64 = oracle.project(L["K"], L["Wk"])
+    rows = np.random.default_rng(1).choice(w.N, 2048, replace=False)
+    assert_kp_close(gKp[:, :, rows], want64[:, :, rows], kp_l1(np.ascontiguousarray(u16(L["K"])[:, :, rows]),
+                                                               u16(L["Wk"])))
+    assert (gKp != want).mean() < 0.01
     s_ref_own, _ = oracle.score(L["q_imp"], want)        # scores on the oracle's own Kp
     dense = oracle.dense_attn(L["q"], L["K"], L["V"], w.N, w.scale)
     for p in w.budgets:
