@@ -49,6 +49,7 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rotate", type=int, default=0, help="cache copies to rotate over (0: enough to defeat L2)")
     return ap.parse_args()
 
 
@@ -248,7 +249,7 @@ def run_ours(args, w):
     step_bytes = kp_bytes + gather_bytes + qio_bytes + append_bytes
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    R = max(4, math.ceil(4 * l2 / step_bytes))
+    R = args.rotate if args.rotate > 0 else max(4, math.ceil(4 * l2 / step_bytes))
     Ks = [K0] + [K0.clone() for _ in range(R - 1)]
     Vs = [V0] + [V0.clone() for _ in range(R - 1)]
     Kps = [Kp0] + [Kp0.clone() for _ in range(R - 1)]
@@ -340,7 +341,8 @@ def run_ours(args, w):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "dp": w.dp, "N": w.N,
                        "k": w.k, "T": 1, "r": 0, "rotation_sets": R,
-                       "l2_defeat": f"inputs rotate over {R} cache copies ({R * step_bytes / 1e6:.0f} MB >= 4 x L2)",
+                       "l2_defeat": f"inputs rotate over {R} cache copies ({R * step_bytes / 1e6:.0f} MB touched per "
+                                    f"rotation, L2 {l2 / 1e6:.0f} MB)",
                        "parallelism": f"replicas x{world}"},
             "tokens_per_s": total_steps_per_s * w.B,
             "hbm_gbs": achieved * world,

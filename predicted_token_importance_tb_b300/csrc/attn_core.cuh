@@ -187,21 +187,49 @@ __device__ __forceinline__ void attn_block_combine(AttnLane<GM> &A, int G, int D
 }
 
 // Merge nsplit partial states (each G x (2 + D) floats, consecutive) into the
-// G output rows (bf16). Returns through dev_status when a row saw no token.
+// G output rows (bf16). sm: shared scratch of 2 * nsplit * G + G floats.
+// The (max, sum) pairs are gathered into shared memory with one load per
+// thread, so the merge costs a few L2 round trips, not one per split.
+// Records TB_ERR_INVALID_ARG when a row saw no token. All threads must call it.
 __device__ __forceinline__ void attn_merge(const float *part, int nsplit, int G, int D, uint16_t *out_rows,
-                                           int32_t *dev_status) {
+                                           int32_t *dev_status, float *sm) {
     const int sg = 2 + D;
+    float *wm = sm;                       // [nsplit * G] max, then weight
+    float *ls = sm + nsplit * G;          // [nsplit * G] sums
+    float *Mg = ls + nsplit * G;          // [G]
+    for (int i = threadIdx.x; i < nsplit * G; i += blockDim.x) {
+        wm[i] = __ldcg(part + (int64_t)i * sg);
+        ls[i] = __ldcg(part + (int64_t)i * sg + 1);
+    }
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, wm[sp * G + g]);
+        Mg[g] = M;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nsplit * G; i += blockDim.x) wm[i] = rescale_w(wm[i], Mg[i % G]);
+    __syncthreads();
     for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
         const int g = x / D, d = x % D;
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(part + ((int64_t)sp * G + g) * sg));
         float L = 0.f, Acc = 0.f;
-#pragma unroll 4
-        for (int sp = 0; sp < nsplit; ++sp) {
-            const float *src = part + ((int64_t)sp * G + g) * sg;
-            const float wt = rescale_w(__ldcg(src), M);
-            L += wt * __ldcg(src + 1);
-            Acc += wt * __ldcg(src + 2 + d);
+        const float *src = part + (int64_t)g * sg + 2 + d;
+        int sp = 0;
+        for (; sp + 8 <= nsplit; sp += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (int64_t)(sp + u) * G * sg);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float w = wm[(sp + u) * G + g];
+                L += w * ls[(sp + u) * G + g];
+                Acc += w * v[u];
+            }
+        }
+        for (; sp < nsplit; ++sp) {
+            const float w = wm[sp * G + g];
+            L += w * ls[sp * G + g];
+            Acc += w * __ldcg(src + (int64_t)sp * G * sg);
         }
         if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
         out_rows[(int64_t)g * D + d] = f_to_bf16(L > 0.f ? Acc / L : 0.f);

@@ -287,7 +287,8 @@ fused_step_kernel(const FusedArgs a) {
     __syncthreads();
     if (!S.misc[6]) return;
     __threadfence();
-    attn_merge(prow, C, G, D, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * D, a.dev_status);
+    attn_merge(prow, C, G, D, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * D, a.dev_status,
+               reinterpret_cast<float *>(S.ckey));
     for (int x = threadIdx.x; x < 3 * kRadixBins; x += blockDim.x) (&rc->hist[0][0])[x] = 0;
     if (threadIdx.x == 0) {
         rc->bar = 0;
@@ -322,6 +323,9 @@ static FusedPlan plan_fused(const tb_shape &sh, int64_t n_tokens, int sms, int b
     const int G = sh.Hq / sh.Hkv;
     int64_t C = (int64_t)blocks_per_sm * sms / rows;
     const int64_t maxC = (n_tokens + 31) / 32;
+    // the merge keeps 2 * C * G + G floats in the candidate area (2 * kCandCap words)
+    const int64_t maxC_merge = (2 * kCandCap - G) / (2 * G);
+    if (C > maxC_merge) C = maxC_merge;
     if (C > maxC) C = maxC;
     if (C > kMaxChunks) C = kMaxChunks;
     if (C < 1) return P;

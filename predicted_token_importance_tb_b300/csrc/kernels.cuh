@@ -30,8 +30,10 @@ cudaError_t launch_append(const tb_shape &sh, const uint16_t *K_new, const uint1
                           int32_t *counts, int32_t *dev_status, cudaStream_t st);
 
 // Kp rows [pos0, pos0 + n_new) from K_src (row stride src_stride per head).
+// path: 0 automatic, 1 CUDA cores, 2 tensor cores (tcgen05).
 cudaError_t launch_project(const tb_shape &sh, const uint16_t *K_src, int64_t src_stride, const uint16_t *Wk,
-                           uint16_t *Kp, int64_t pos0, int64_t n_new, int32_t *dev_status, cudaStream_t st);
+                           uint16_t *Kp, int64_t pos0, int64_t n_new, int32_t *dev_status, cudaStream_t st,
+                           int path = 0);
 
 // The whole decode step (T == 1, r == 0) as one cooperative kernel.
 bool fused_step_supported(const tb_shape &sh, int64_t n_tokens, int32_t k);

@@ -3,7 +3,7 @@
 // Core Architecture: Key-Cache Projection; Optimizations: Batching).
 //
 // CUDA-core path: one CTA projects 64 rows of one (b, h). Used for batches
-// that the tensor-core kernel does not take.
+// that the tensor-core kernel (project_tc.cu) does not take.
 #include "tb_internal.cuh"
 #include "kernels.cuh"
 
@@ -59,9 +59,19 @@ cudaError_t launch_project_simple(const tb_shape &sh, const uint16_t *K_src, int
     return cudaGetLastError();
 }
 
+bool project_tc_supported(const tb_shape &sh, int64_t n_new);
+cudaError_t launch_project_tc(const tb_shape &sh, const uint16_t *K_src, int64_t src_stride, const uint16_t *Wk,
+                              uint16_t *Kp, int64_t pos0, int64_t n_new, int32_t *dev_status, cudaStream_t st);
+
 cudaError_t launch_project(const tb_shape &sh, const uint16_t *K_src, int64_t src_stride, const uint16_t *Wk,
-                           uint16_t *Kp, int64_t pos0, int64_t n_new, int32_t *dev_status, cudaStream_t st) {
-    (void)dev_status;
+                           uint16_t *Kp, int64_t pos0, int64_t n_new, int32_t *dev_status, cudaStream_t st,
+                           int path) {
+    // path: 0 automatic (tensor cores for batches of >= 128 rows), 1 CUDA cores, 2 tensor cores
+    const bool tc = path == 2 || (path == 0 && project_tc_supported(sh, n_new));
+    if (tc) {
+        if (!project_tc_supported(sh, n_new)) return cudaErrorInvalidValue;
+        return launch_project_tc(sh, K_src, src_stride, Wk, Kp, pos0, n_new, dev_status, st);
+    }
     return launch_project_simple(sh, K_src, src_stride, Wk, Kp, pos0, n_new, st);
 }
 

@@ -12,7 +12,8 @@ constexpr int kRadixBits = 11;
 constexpr int kRadixBins = 1 << kRadixBits;  // 2048 bins per radix digit
 constexpr int kCandCap = 4096;                // largest threshold bin resolved by candidates
 constexpr int kMaxChunks = 512;               // CTAs that may share one row
-constexpr int kAttnSplitTok = 64;             // selected tokens per attention split
+constexpr int kAttnSplitTok = 64;             // fewest selected tokens per attention split
+constexpr int kAttnMaxSplits = 128;           // most splits per row
 
 // Per-row control block of the distributed radix select. Zero between calls.
 struct RowCtl {
@@ -37,8 +38,16 @@ struct WsLayout {
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Tokens per split: at least kAttnSplitTok, more when the row would need
+// over kAttnMaxSplits splits.
+inline int64_t attn_split_tokens(int64_t sel_stride) {
+    int64_t t = (sel_stride + kAttnMaxSplits - 1) / kAttnMaxSplits;
+    return t < kAttnSplitTok ? kAttnSplitTok : t;
+}
+
 inline int64_t attn_splits(int64_t sel_stride) {
-    return (sel_stride + kAttnSplitTok - 1) / kAttnSplitTok;
+    const int64_t t = attn_split_tokens(sel_stride);
+    return (sel_stride + t - 1) / t;
 }
 
 inline WsLayout ws_layout(const tb_shape &s, int64_t n_max, int64_t sel_stride_max, int64_t fused_chunks_max) {
