@@ -196,6 +196,34 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
                          int32_t sel_stride, int32_t *counts, tb_bf16 *out,
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
+/*
+ * tb_topk without a workspace. The paper has no counterpart to this call; it
+ * exists for callers that cannot allocate device memory at all, so cannot
+ * hand tb_topk its scratch: code embedded in a host runtime that owns every
+ * device allocation and gives its plug-ins none, or a serving process whose
+ * memory is fixed once at start-up.
+ *
+ * Same arguments and results as tb_topk (bit-identical idx), minus ws and
+ * ws_bytes. The selection's scratch is a static device array compiled into
+ * the library, sized for TB_TOPK_NOALLOC_MAX_ROWS rows of B*Hkv; every GPU
+ * that loads the library holds it (about 3.9 MB) until the process exits.
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine. It clears the part of the array it uses (an asynchronous
+ * memset on `stream`) before its kernel runs.
+ *
+ * Errors: B*Hkv > TB_TOPK_NOALLOC_MAX_ROWS returns TB_ERR_UNSUPPORTED; the
+ * other checks and device-side errors are those of tb_topk.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. All calls on a device share the one array, so
+ * calls that overlap on the GPU (concurrent streams, or several host threads)
+ * race and give wrong results: serialise them.
+ */
+#define TB_TOPK_NOALLOC_MAX_ROWS 64
+
+TB_API tb_status tb_topk_noalloc(const tb_shape *shape, const float *s, int64_t n, int32_t k, int32_t *idx,
+                                 int32_t *dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,8 +35,10 @@ TB_STEP_UNFUSED = 1
 
 EXPORTED = (
     "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
-    "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step",
+    "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step", "tb_topk_noalloc",
 )
+
+TB_TOPK_NOALLOC_MAX_ROWS = 64
 
 
 class TBError(RuntimeError):
@@ -92,6 +94,7 @@ def load_library(path: str = LIB_PATH):
         lib.tb_project_append.argtypes = [SP, P, i64, P, P, i64, i64, P, sz, P, P]
         lib.tb_score.argtypes = [SP, P, P, i64, i32, P, P, P]
         lib.tb_topk.argtypes = [SP, P, i64, i32, P, P, sz, P, P]
+        lib.tb_topk_noalloc.argtypes = [SP, P, i64, i32, P, P, P]
         lib.tb_expand.argtypes = [SP, P, i32, i32, i64, i64, P, i32, P, P, P]
         lib.tb_sparse_decode_attn.argtypes = [SP, P, P, P, P, P, i32, f32, P, P, sz, P, P]
         lib.tb_decode_step.argtypes = [SP, ctypes.POINTER(_StepParams), i64, i64, P, P, P, P, P, P, P, P, P,
@@ -207,6 +210,14 @@ def tb_topk(shape: Shape, s, n: int, k: int, idx, ws, dev_status=None, stream=No
         raise TypeError("s must be float32")
     _check(load_library().tb_topk(ctypes.byref(shape.c()), _ptr(s), n, k, _i32(idx, "idx"), _ptr(ws), ws.numel(),
                                   _status_ptr(dev_status), _stream(stream)), "tb_topk")
+
+
+def tb_topk_noalloc(shape: Shape, s, n: int, k: int, idx, dev_status=None, stream=None):
+    """tb_topk for callers that cannot allocate: its scratch is a static array inside libtb."""
+    if s.dtype != torch.float32:
+        raise TypeError("s must be float32")
+    _check(load_library().tb_topk_noalloc(ctypes.byref(shape.c()), _ptr(s), n, k, _i32(idx, "idx"),
+                                          _status_ptr(dev_status), _stream(stream)), "tb_topk_noalloc")
 
 
 def tb_expand(shape: Shape, idx, k: int, r: int, n_pred: int, n_t: int, sel, sel_stride: int, counts,
