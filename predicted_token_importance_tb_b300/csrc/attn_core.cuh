@@ -124,6 +124,60 @@ __device__ __forceinline__ void attn_tokens(AttnLane<GM> &A, int G, int D, int c
     }
 }
 
+// Attend rows already staged in shared memory: row(j) points at the K row of
+// entry j (D bf16), its V row follows at +D. Same lane layout and warp rule
+// as attn_tokens.
+template <int GM, class RowFn>
+__device__ __forceinline__ void attn_stage_rows(AttnLane<GM> &A, int G, int D, int cnt, RowFn row) {
+    const int TPG = D / 8;
+    const int gpw = 32 / TPG;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gi = lane / TPG, gl = lane % TPG;
+    const int ngroups = (blockDim.x >> 5) * gpw;
+    for (int jw = warp * gpw; jw < cnt; jw += ngroups) {
+        const int j = jw + gi;
+        const bool valid = j < cnt;
+        float kf[8];
+        uint4 vv = make_uint4(0, 0, 0, 0);
+        if (valid) {
+            const uint16_t *r = row(j);
+            unpack8(*reinterpret_cast<const uint4 *>(r + 8 * gl), kf);
+            vv = *reinterpret_cast<const uint4 *>(r + D + 8 * gl);
+        } else {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) kf[x] = 0.f;
+        }
+        float z[GM];
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            float acc = 0.f;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) acc = fmaf(A.qv[g][x], kf[x], acc);
+            z[g] = acc;
+        }
+        for (int o = TPG / 2; o > 0; o >>= 1) {
+#pragma unroll
+            for (int g = 0; g < GM; ++g) z[g] += __shfl_xor_sync(0xFFFFFFFFu, z[g], o);
+        }
+        if (valid) {
+            float vf[8];
+            unpack8(vv, vf);
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                if (g < G) {
+                    const float mn = fmaxf(A.m[g], z[g]);
+                    const float corr = exp2f(A.m[g] - mn);
+                    const float p = exp2f(z[g] - mn);
+                    A.l[g] = fmaf(A.l[g], corr, p);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) A.acc[g][x] = fmaf(A.acc[g][x], corr, p * vf[x]);
+                    A.m[g] = mn;
+                }
+            }
+        }
+    }
+}
+
 // Merge the lane groups of the CTA into one partial state per query head and
 // store it at dst[g * (2 + D)] = (m, l, acc[D]). comb: shared scratch of
 // (blockDim/32) * G * (2 + D) floats. All threads must call it.
@@ -188,51 +242,52 @@ __device__ __forceinline__ void attn_block_combine(AttnLane<GM> &A, int G, int D
 
 // Merge nsplit partial states (each G x (2 + D) floats, consecutive) into the
 // G output rows (bf16). sm: shared scratch of 2 * nsplit * G + G floats.
-// The (max, sum) pairs are gathered into shared memory with one load per
-// thread, so the merge costs a few L2 round trips, not one per split.
-// Records TB_ERR_INVALID_ARG when a row saw no token. All threads must call it.
+// Each thread first issues the loads of its outputs' accumulators for a batch
+// of up to 32 splits, then the (max, sum) pairs go to shared memory with one
+// load per thread, so a batch costs one L2 round trip. Records
+// TB_ERR_INVALID_ARG when a row saw no token. All threads must call it.
 __device__ __forceinline__ void attn_merge(const float *part, int nsplit, int G, int D, uint16_t *out_rows,
                                            int32_t *dev_status, float *sm) {
+    constexpr int kBatch = 32;
     const int sg = 2 + D;
-    float *wm = sm;                       // [nsplit * G] max, then weight
-    float *ls = sm + nsplit * G;          // [nsplit * G] sums
-    float *Mg = ls + nsplit * G;          // [G]
-    for (int i = threadIdx.x; i < nsplit * G; i += blockDim.x) {
-        wm[i] = __ldcg(part + (int64_t)i * sg);
-        ls[i] = __ldcg(part + (int64_t)i * sg + 1);
-    }
-    __syncthreads();
-    for (int g = threadIdx.x; g < G; g += blockDim.x) {
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, wm[sp * G + g]);
-        Mg[g] = M;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < nsplit * G; i += blockDim.x) wm[i] = rescale_w(wm[i], Mg[i % G]);
-    __syncthreads();
-    for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
-        const int g = x / D, d = x % D;
-        float L = 0.f, Acc = 0.f;
-        const float *src = part + (int64_t)g * sg + 2 + d;
-        int sp = 0;
-        for (; sp + 8 <= nsplit; sp += 8) {
-            float v[8];
+    float *ms = sm;                      // [nsplit * G] max
+    float *ls = sm + nsplit * G;         // [nsplit * G] sums
+    for (int x0 = 0; x0 < G * D; x0 += blockDim.x) {
+        const int x = x0 + threadIdx.x;
+        const bool active = x < G * D;
+        const int g = active ? x / D : 0, d = active ? x % D : 0;
+        float M = -INFINITY, L = 0.f, Acc = 0.f;
+        for (int sp0 = 0; sp0 < nsplit; sp0 += kBatch) {
+            float av[kBatch];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (int64_t)(sp + u) * G * sg);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float w = wm[(sp + u) * G + g];
-                L += w * ls[(sp + u) * G + g];
-                Acc += w * v[u];
+            for (int u = 0; u < kBatch; ++u)
+                av[u] = (active && sp0 + u < nsplit) ? __ldcg(part + ((int64_t)(sp0 + u) * G + g) * sg + 2 + d) : 0.f;
+            __syncthreads();
+            const int nb = nsplit - sp0 < kBatch ? nsplit - sp0 : kBatch;
+            for (int i = threadIdx.x; i < nb * G; i += blockDim.x) {
+                ms[i] = __ldcg(part + ((int64_t)sp0 * G + i) * sg);
+                ls[i] = __ldcg(part + ((int64_t)sp0 * G + i) * sg + 1);
             }
+            __syncthreads();
+            float Mb = M;
+            for (int u = 0; u < nb; ++u) Mb = fmaxf(Mb, ms[u * G + g]);
+            const float r = rescale_w(M, Mb);
+            L *= r;
+            Acc *= r;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (u < nb) {
+                    const float w = rescale_w(ms[u * G + g], Mb);
+                    L = fmaf(w, ls[u * G + g], L);
+                    Acc = fmaf(w, av[u], Acc);
+                }
+            }
+            M = Mb;
         }
-        for (; sp < nsplit; ++sp) {
-            const float w = wm[sp * G + g];
-            L += w * ls[sp * G + g];
-            Acc += w * __ldcg(src + (int64_t)sp * G * sg);
+        if (active) {
+            if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
+            out_rows[(int64_t)g * D + d] = f_to_bf16(L > 0.f ? Acc / L : 0.f);
         }
-        if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
-        out_rows[(int64_t)g * D + d] = f_to_bf16(L > 0.f ? Acc / L : 0.f);
     }
 }
 

@@ -1,0 +1,164 @@
+// Pieces shared by the single-launch decode-step kernels ("TokenButler: Token
+// Importance is Predictable": project the new key, score every cached token,
+// keep a fixed per-token budget, attend over only the kept rows).
+//
+//  - step_append_project: the CTA owning the new token writes K_new / V_new
+//    into the cache and projects K_new into its Kp row (fp32 sum, one RNE).
+//  - chunk_select_attend: exact top-k of a row split into contiguous chunks
+//    (topk_core.cuh), attending the kept tokens of this CTA's chunk and
+//    writing them, ascending, to idx and sel.
+//  - row_finish: this CTA's partial softmax state goes to the workspace; the
+//    row's last CTA merges the partials into the output rows and puts the
+//    row's control words back to zero.
+#pragma once
+
+#include "attn_core.cuh"
+#include "topk_core.cuh"
+
+namespace tb {
+
+// Scratch floats attn_block_combine needs for nthreads threads.
+__host__ __device__ inline int comb_floats_for(int nthreads, int G, int D) {
+    const int f = (nthreads / 32) * G * (2 + D);
+    return f > nthreads ? f : nthreads;
+}
+
+// Append the step's K/V row of (b,h) = row at position n and project the key.
+// knew [D] and kpn [dp] (shared, fp32) receive the new key and its projected
+// (bf16-rounded) row; comb is shared scratch of at least blockDim.x floats.
+// All threads of the CTA must call it.
+__device__ __forceinline__ void step_append_project(const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk,
+                                                    uint16_t *K, uint16_t *V, uint16_t *Kp, int64_t cap, int64_t n,
+                                                    int row, int h, int D, int dp, float *knew, float *kpn,
+                                                    float *comb) {
+    const uint16_t *kn = K_new + (int64_t)row * D;
+    const uint16_t *vn = V_new + (int64_t)row * D;
+    uint16_t *Kr = K + ((int64_t)row * cap + n) * D;
+    uint16_t *Vr = V + ((int64_t)row * cap + n) * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        const uint16_t kb = kn[d];
+        knew[d] = bf16_to_f(kb);
+        Kr[d] = kb;
+        Vr[d] = vn[d];
+    }
+    __syncthreads();
+    // threads (j, slice) accumulate output j over a slice of D, summed in comb
+    const uint16_t *W = Wk + (int64_t)h * D * dp;
+    const int jn = dp < (int)blockDim.x ? dp : (int)blockDim.x;
+    const int slices = blockDim.x / jn;
+    const int dlen = (D + slices - 1) / slices;
+    const int j = threadIdx.x % jn, sl = threadIdx.x / jn;
+    if (sl < slices) {
+        float acc = 0.f;
+        const int d0 = sl * dlen, d1 = min(D, d0 + dlen);
+        for (int d = d0; d < d1; ++d) acc = fmaf(knew[d], bf16_to_f(W[(int64_t)d * dp + j]), acc);
+        comb[sl * jn + j] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x < dp) {
+        float s = 0.f;
+        for (int x = 0; x < slices; ++x) s += comb[x * jn + threadIdx.x];
+        const uint16_t kb = f_to_bf16(s);
+        Kp[((int64_t)row * cap + n) * dp + threadIdx.x] = kb;
+        kpn[threadIdx.x] = bf16_to_f(kb);
+    }
+    __syncthreads();
+}
+
+// Exact selection over contiguous chunks plus attention over this CTA's kept
+// tokens. S.keys[0..Lc) hold the keys of tokens t0 .. t0+Lc-1 (chunk c of C,
+// chunk length L); list is shared scratch of L ints. irow / srow receive the
+// row's kept tokens in ascending order. bar_base: phases of rc->bar already
+// completed in this launch. Returns false when a group wait timed out.
+template <int GM>
+__device__ bool chunk_select_attend(AttnLane<GM> &A, RowCtl *rc, SelectSmem &S, int32_t *list, int Lc, int L, int c,
+                                    int C, int bar_base, uint32_t k, int64_t t0, const uint16_t *Kh,
+                                    const uint16_t *Vh, int64_t cap, int G, int D, int32_t *irow, int32_t *srow,
+                                    int32_t *dev_status) {
+    SelectBegin B = group_select_begin(rc, S, Lc, L, c, C, k, dev_status, bar_base);
+    if (!B.ok) return false;
+    // tokens above the threshold bin are kept whatever the exact threshold:
+    // attend them while the last selection barrier completes
+    uint32_t n_above = 0;
+    for (int e0 = 0; e0 < Lc; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        const uint32_t f = (e < Lc && above_bin(B, S.keys[e])) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t pos = block_exclusive_scan(f, S.scan, tot);
+        if (f) list[n_above + pos] = e;
+        n_above += tot;
+    }
+    __syncthreads();
+    attn_tokens(A, G, D, (int)n_above, [&](int j) -> int64_t { return t0 + list[j]; }, Kh, Vh, cap, dev_status);
+    __syncthreads();
+    // exact threshold; kept tokens out (ascending); attend the kept bin tokens
+    SelectResult R = group_select_end(rc, S, B, L, c, C, dev_status);
+    if (!R.ok) return false;
+    uint32_t base_kept = 0, base_tied = 0, n_bin = 0;
+    for (int e0 = 0; e0 < Lc; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        uint32_t key = 0, tied = 0;
+        if (e < Lc) {
+            key = S.keys[e];
+            tied = (R.mode == 1 && key == R.tkey) ? 1u : 0u;
+        }
+        uint32_t ttot;
+        const uint32_t tied_before = base_tied + block_exclusive_scan(tied, S.scan, ttot);
+        const bool kept = e < Lc && is_kept(R, key, (uint32_t)(t0 + e), tied_before);
+        const uint32_t kf = kept ? 1u : 0u;
+        const uint32_t bf = (kept && !above_bin(B, key)) ? 1u : 0u;
+        uint32_t ktot, btot;
+        const uint32_t pos = block_exclusive_scan(kf, S.scan, ktot);
+        const uint32_t bpos = block_exclusive_scan(bf, S.scan, btot);
+        if (kept) {
+            const uint32_t slot = R.offset + base_kept + pos;
+            irow[slot] = (int32_t)(t0 + e);
+            srow[slot] = (int32_t)(t0 + e);
+        }
+        if (bf) list[n_bin + bpos] = e;
+        base_kept += ktot;
+        base_tied += ttot;
+        n_bin += btot;
+    }
+    __syncthreads();
+    attn_tokens(A, G, D, (int)n_bin, [&](int j) -> int64_t { return t0 + list[j]; }, Kh, Vh, cap, dev_status);
+    return true;
+}
+
+// The row's last CTA to finish merges the C partial states (this CTA's is
+// already stored at prow + c * G * (2 + D)) into the G output rows and
+// resets the row's control block (the radix histograms and candidate count
+// only when reset_hist). msm: shared scratch of 2*C*G + G floats; flag: one
+// shared word. All threads of the CTA must call it.
+__device__ __forceinline__ void row_merge_tail(RowCtl *rc, const float *prow, int C, int G, int D,
+                                               uint16_t *out_rows, float *msm, uint32_t *flag, bool reset_hist,
+                                               int32_t *dev_status) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&rc->done, 1u);
+        *flag = (prev == (uint32_t)(C - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    attn_merge(prow, C, G, D, out_rows, dev_status, msm);
+    if (reset_hist)
+        for (int x = threadIdx.x; x < 3 * kRadixBins; x += blockDim.x) (&rc->hist[0][0])[x] = 0;
+    if (threadIdx.x == 0) {
+        rc->bar = 0;
+        rc->ncand = 0;
+        rc->done = 0;
+    }
+}
+
+// Partial state of this CTA -> workspace, then row_merge_tail.
+// comb: shared scratch of comb_floats_for(blockDim.x, G, D) floats.
+template <int GM>
+__device__ void row_finish(AttnLane<GM> &A, RowCtl *rc, float *prow, int c, int C, int G, int D, uint16_t *out_rows,
+                           float *comb, float *msm, uint32_t *flag, bool reset_hist, int32_t *dev_status) {
+    attn_block_combine(A, G, D, comb, prow + (int64_t)c * G * (2 + D));
+    row_merge_tail(rc, prow, C, G, D, out_rows, msm, flag, reset_hist, dev_status);
+}
+
+}  // namespace tb

@@ -1,0 +1,965 @@
+// One decode step with a fresh prediction (interval T = 1, no neighbours) as a
+// single cooperative launch with one exchange between the CTAs of a row
+// ("TokenButler: Token Importance is Predictable": score every cached token
+// with the importance query, keep a fixed per-token budget, attend over only
+// the kept full-precision rows).
+//
+// Grid = rows x C CTAs, one per SM. The tokens of a row are dealt to its C
+// CTAs in blocks of 32 (CTA c owns blocks c, c + C, c + 2C, ...), so every CTA
+// holds a sample of the whole row and its local score distribution follows
+// the row's.
+//
+//   1. The CTA owning token n appends K_new / V_new and projects K_new.
+//   2. Bulk copies bring the CTA's blocks of Kp into shared memory; the
+//      scores become order-preserving keys.
+//   3. Locally about t_c = k L_c / n of the CTA's L_c tokens are kept, with a
+//      binomial spread sigma = sqrt(t_c (1 - k/n)). From its histogram the
+//      CTA picks a window of 16-bit score prefixes [lo, hi] holding its local
+//      ranks t_c -+ (5 sigma + 4) and publishes: the count above the window,
+//      per-block counts above it, and every (key, token) inside it.
+//   4. It starts gathering the K/V rows of its tokens above and inside the
+//      window into shared memory (cp.async), then waits for the row's
+//      single exchange.
+//   5. All records of the row are read. If the windows intersect in [L, H]
+//      and the row's k-th largest element lies there, the exact threshold T
+//      (the composite of score key and token, lower token first) follows from
+//      the entries inside [L, H]: a fine histogram finds the 16-bit bin of
+//      the k-th element and a rank count inside that bin finds T. Per-block
+//      kept counts of the whole row then give every CTA the slots of its kept
+//      tokens in the ascending idx / sel rows.
+//      Otherwise (a window missed: rare unless the score layout is blocky)
+//      the CTAs re-split the row into contiguous chunks through the workspace
+//      and run the general distributed radix select (topk_core.cuh).
+//   6. Attention over the gathered rows runs on the tensor cores: per warp,
+//      chunks of 16 rows, S = Q K^T and O += P V as m16n8k16 bf16 MMAs with
+//      fp32 accumulation and an online softmax (exp2 domain, fp32); rows
+//      that are not kept are masked. The warps' states are combined and the
+//      row's last CTA merges the C partial states.
+#include <string.h>
+
+#include "async_copy.cuh"
+#include "fused_common.cuh"
+#include "kernels.cuh"
+
+namespace tb {
+
+constexpr int kFFThreads = 512;
+constexpr int kFFWarps = kFFThreads / 32;
+constexpr int kFFEntMax = kFastEntMax;
+constexpr int kFFEntPerThread = 8;  // entries of one record a thread reads
+constexpr int kFFStageMax = 512;    // K/V rows gathered into shared memory per round
+constexpr int kFFFine = 128;        // fine bins: 4 coarse bins x 32
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+
+struct FFHdr {
+    uint32_t above, lo, hi, n_ent, valid, pad0, pad1, pad2;
+};
+constexpr int kFFRecBytes = kFastRecBytes;
+static_assert(sizeof(FFHdr) == 32, "record header is 32 bytes");
+
+struct FFArgs {
+    const uint16_t *q, *q_imp, *K_new, *V_new, *Wk;
+    uint16_t *K, *V, *Kp;
+    int32_t *idx, *sel, *counts;
+    uint16_t *out;
+    RowCtl *ctl;
+    float *part;
+    uint8_t *rec;        // rows x C records of kFFRecBytes
+    uint8_t *blk_above;  // rows x blk_stride: per 32-token block, tokens above the owner's window
+    uint32_t *keys_g;    // rows x keys_stride: keys in token order (general path)
+    int32_t *dev_status;
+    int64_t cap, n, keys_stride;
+    int Hq, Hkv, D, k, agg, sel_stride;
+    float scale;
+    int C, NB, blk_stride, stage_cap;
+};
+
+// Shared-memory layout (byte offsets, each 16-byte aligned).
+struct FFLayout {
+    int X, qsm, keys, hist, fine, ckey, cidx, ccount, scan, misc, abort_, cnt, bcnt, stok, skey, kept, qs, kpn, knew,
+        bar, total;
+};
+
+__host__ __device__ inline int ff_a16(int x) { return (x + 15) & ~15; }
+__host__ __device__ inline int ff_slot_bytes(int D) { return 4 * D + 16; }   // K row, V row, 16-byte skew
+
+__host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int G, int D, int dp) {
+    FFLayout L;
+    int x = 0;
+    int xb = NB * 32 * dp * 2;                                   // Kp blocks
+    const int sb = stage_cap * ff_slot_bytes(D);                 // gathered K/V rows
+    const int wb = kFFWarps * G * (2 + D) * 4;                   // per-warp attention states
+    const int cb = comb_floats_for(kFFThreads, G, D) * 4;        // general path's combine scratch
+    if (sb > xb) xb = sb;
+    if (wb > xb) xb = wb;
+    if (cb > xb) xb = cb;
+    L.X = x; x += ff_a16(xb);
+    L.qsm = x; x += 16 * (2 * D + 16);
+    L.keys = x; x += ff_a16(NB * 32 * 4);
+    L.hist = x; x += kRadixBins * 4;
+    L.fine = x; x += kFFFine * 4;
+    L.ckey = x; x += kCandCap * 4;
+    L.cidx = x; x += kCandCap * 4;
+    L.ccount = x; x += kMaxChunks * 4;
+    L.scan = x; x += 36 * 4;
+    L.misc = x; x += 16 * 4;
+    L.abort_ = x; x += 16;
+    L.cnt = x; x += 32 * 4;
+    L.bcnt = x; x += ff_a16(NB * C * 4);
+    L.stok = x; x += ff_a16(NB * 32 * 4);
+    L.skey = x; x += ff_a16(NB * 32 * 4);
+    L.kept = x; x += ff_a16(NB * 32);
+    L.qs = x; x += ff_a16(G * dp * 4);
+    L.kpn = x; x += ff_a16(dp * 4);
+    L.knew = x; x += ff_a16(D * 4);
+    L.bar = x; x += 16;
+    L.total = x;
+    return L;
+}
+
+// counters in the cnt region
+enum {
+    CN_ABOVE = 0, CN_WIN, CN_CAND, CN_AE, CN_L, CN_H, CN_VALID, CN_ASUM, CN_RANGE, CN_BM, CN_FLAG
+};
+
+// Warp-aggregated slot allocation on a shared counter: lanes with `want`
+// get consecutive slots. All lanes of the warp must call it.
+__device__ __forceinline__ uint32_t warp_alloc(uint32_t *ctr, bool want) {
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, want);
+    const int lane = threadIdx.x & 31;
+    uint32_t base = 0;
+    if (m) {
+        const int leader = __ffs(m) - 1;
+        if (lane == leader) base = atomicAdd(ctr, (uint32_t)__popc(m));
+        base = __shfl_sync(0xFFFFFFFFu, base, leader);
+    }
+    return base + (uint32_t)__popc(m & ((1u << lane) - 1u));
+}
+
+// Bins of two targets (ranks from the top, 1-based; 0 = none) in a histogram
+// of nbins (a multiple of blockDim.x). out = {bin1, above1, bin2, above2},
+// kNone where a target is 0 or beyond the total. All threads call.
+__device__ __noinline__ void find_two_bins(const uint32_t *hist, int nbins, uint32_t need1, uint32_t need2,
+                                           uint32_t *scan, uint32_t *out) {
+    if (threadIdx.x == 0) out[0] = out[1] = out[2] = out[3] = kNone;
+    const int per = nbins / blockDim.x;
+    const int hi = nbins - 1 - threadIdx.x * per;
+    uint32_t local = 0;
+    for (int j = 0; j < per; ++j) local += hist[hi - j];
+    uint32_t total;
+    const uint32_t above = block_exclusive_scan(local, scan, total);
+    for (int t = 0; t < 2; ++t) {
+        const uint32_t need = t == 0 ? need1 : need2;
+        if (need >= 1 && above < need && need <= above + local) {
+            uint32_t a = above;
+            for (int j = 0; j < per; ++j) {
+                const uint32_t c = hist[hi - j];
+                if (need <= a + c) {
+                    out[2 * t] = (uint32_t)(hi - j);
+                    out[2 * t + 1] = a;
+                    break;
+                }
+                a += c;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// One warp: bins of up to two targets among kFFFine fine bins with `base`
+// elements above them. out[t] = bin (kNone if not inside), out[2 + t] =
+// elements above that bin, out[4 + t] = elements in it.
+__device__ __noinline__ void warp_find_fine(const uint32_t *fine, uint32_t base, uint32_t need1, uint32_t need2,
+                                            uint32_t *out) {
+    const int lane = threadIdx.x & 31;
+    const int hi = kFFFine - 1 - lane * 4;
+    uint32_t local = 0;
+    for (int j = 0; j < 4; ++j) local += fine[hi - j];
+    uint32_t x = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    const uint32_t above = base + x - local;
+    if (lane == 0) out[0] = out[1] = kNone;
+    __syncwarp();
+    for (int t = 0; t < 2; ++t) {
+        const uint32_t need = t == 0 ? need1 : need2;
+        if (need >= 1 && above < need && need <= above + local) {
+            uint32_t a = above;
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t c = fine[hi - j];
+                if (need <= a + c) {
+                    out[t] = (uint32_t)(hi - j);
+                    out[2 + t] = a;
+                    out[4 + t] = c;
+                    break;
+                }
+                a += c;
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// Exclusive prefix over n shared counters in place (all threads call).
+__device__ __noinline__ void block_scan_inplace(uint32_t *v, int n, uint32_t *scan) {
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int x0 = threadIdx.x * per;
+    uint32_t loc = 0;
+    for (int x = x0; x < x0 + per && x < n; ++x) loc += v[x];
+    uint32_t tot;
+    uint32_t run = block_exclusive_scan(loc, scan, tot);
+    for (int x = x0; x < x0 + per && x < n; ++x) {
+        const uint32_t t = v[x];
+        v[x] = run;
+        run += t;
+    }
+    __syncthreads();
+}
+
+// Per-warp attention state on the tensor cores: rows g = lane/4 and g + 8 of
+// the 16-row tiles (query heads; rows >= G are zero padding), O over NT
+// n-tiles of 8 dims.
+template <int NT>
+struct MmaAttn {
+    float m0, m1, l0, l1;
+    float o[NT][4];
+};
+
+// Attend slots [0, n) of the gathered rows (K row at X + s*SB, V row at
+// +2D) for the slots whose kept flag is set; chunks of 16 slots per warp.
+template <int DT>
+__device__ __forceinline__ void mma_attend(MmaAttn<DT / 8> &A, const uint8_t *X, int SB, int n, const uint8_t *kept,
+                                           int kept_off, const uint8_t *qsm, float qscale) {
+    constexpr int NT = DT / 8, KS = DT / 16, QS = 2 * DT + 16;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t xs = smem_addr(X), qa = smem_addr(qsm);
+    const int nch = (n + 15) >> 4;
+    for (int ch = warp; ch < nch; ch += kFFWarps) {
+        const int s0 = ch * 16;
+        // S = Q K^T for slots s0 .. s0+15 (two n-tiles of 8)
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int kt = s0 + 8 * (lane >> 4) + (lane & 7);        // K row this lane addresses
+        const uint32_t krow = xs + (uint32_t)kt * SB + 16 * ((lane >> 3) & 1);
+        const uint32_t qrow = qa + (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)) * QS + 16 * (lane >> 4);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(qrow + kk * 32, a0, a1, a2, a3);
+            ldsm_x4(krow + kk * 32, b0, b1, b2, b3);
+            mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
+        }
+        // online softmax (exp2 domain); columns of this lane: s0 + 8j + 2(lane%4) + {0,1}
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int s = s0 + 8 * j + 2 * (lane & 3) + u;
+                const bool on = s < n && kept[kept_off + s];
+                sc[j][u] = on ? sc[j][u] * qscale : -INFINITY;
+                sc[j][2 + u] = on ? sc[j][2 + u] * qscale : -INFINITY;
+                mx0 = fmaxf(mx0, sc[j][u]);
+                mx1 = fmaxf(mx1, sc[j][2 + u]);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+        const float n0 = fmaxf(A.m0, mx0), n1 = fmaxf(A.m1, mx1);
+        const float c0 = n0 == -INFINITY ? 1.f : exp2f(A.m0 - n0);
+        const float c1 = n1 == -INFINITY ? 1.f : exp2f(A.m1 - n1);
+        float p[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                p[j][u] = n0 == -INFINITY ? 0.f : exp2f(sc[j][u] - n0);
+                p[j][2 + u] = n1 == -INFINITY ? 0.f : exp2f(sc[j][2 + u] - n1);
+            }
+        }
+        A.l0 = A.l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        A.l1 = A.l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        A.m0 = n0;
+        A.m1 = n1;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            A.o[t][0] *= c0;
+            A.o[t][1] *= c0;
+            A.o[t][2] *= c1;
+            A.o[t][3] *= c1;
+        }
+        // O += P V: A operand from p (row, 16 slots), B from V rows (transposed loads)
+        const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
+        const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
+        const int vt = s0 + 8 * ((lane >> 3) & 1) + (lane & 7);   // V row this lane addresses
+        const uint32_t vrow = xs + (uint32_t)vt * SB + 2 * DT + 16 * (lane >> 4);
+#pragma unroll
+        for (int jp = 0; jp < NT / 2; ++jp) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(vrow + jp * 32, b0, b1, b2, b3);
+            mma_bf16_16816(A.o[2 * jp], pa0, pa1, pa2, pa3, b0, b1);
+            mma_bf16_16816(A.o[2 * jp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+    }
+}
+
+// The general path (rare): keys to the workspace in token order, re-split
+// into contiguous chunks, general distributed select with CUDA-core
+// attention, this CTA's partial state to the workspace.
+template <int GM>
+__device__ __noinline__ bool ff_general_path(const FFArgs &a, SelectSmem &S, int32_t *list, float *comb, int row, int c,
+                                             int nb, int64_t n_t, const uint16_t *Kh, const uint16_t *Vh,
+                                             const uint16_t *qrow, float *prow) {
+    const int C = a.C, G = a.Hq / a.Hkv, D = a.D;
+    RowCtl *rc = a.ctl + row;
+    uint32_t *kg = a.keys_g + (int64_t)row * a.keys_stride;
+    for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+        const int64_t t = ((int64_t)(c + (e >> 5) * C) << 5) + (e & 31);
+        if (t < n_t) kg[t] = S.keys[e];
+    }
+    if (threadIdx.x == 0 && c == 0) atomicAdd(&rc->general_steps, 1u);
+    if (!group_barrier(&rc->bar, (uint32_t)(2 * C), S.abort_flag, a.dev_status)) return false;
+    const int Ls = (int)((((n_t + C - 1) / C) + 31) / 32 * 32);
+    const int64_t t0 = (int64_t)c * Ls;
+    const int Lcs = (int)(n_t - t0 < Ls ? (n_t - t0 > 0 ? n_t - t0 : 0) : Ls);
+    for (int e = threadIdx.x; e < Lcs; e += blockDim.x) S.keys[e] = __ldcg(kg + t0 + e);
+    __syncthreads();
+    AttnLane<GM> A;
+    attn_init(A, qrow, G, D, (threadIdx.x & 31) % (D / 8), a.scale);
+    if (!chunk_select_attend(A, rc, S, list, Lcs, Ls, c, C, 2, (uint32_t)a.k, t0, Kh, Vh, a.cap, G, D,
+                             a.idx + (int64_t)row * a.k, a.sel + (int64_t)row * a.sel_stride, a.dev_status))
+        return false;
+    attn_block_combine(A, G, D, comb, prow + (int64_t)c * G * (2 + D));
+    return true;
+}
+
+template <int CPT, int DT, int GM>
+__global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs a) {
+    extern __shared__ __align__(128) uint8_t smb[];
+    constexpr int DP = CPT * 8;
+    constexpr int NT = DT / 8;
+    const int G = a.Hq / a.Hkv;
+    const int C = a.C, NB = a.NB;
+    const int row = blockIdx.x / C, c = blockIdx.x % C;
+    const int b = row / a.Hkv, h = row % a.Hkv;
+    const int64_t n_t = a.n + 1;
+    const int nblk = (int)((n_t + 31) >> 5);
+    const int nb = c < nblk ? (nblk - 1 - c) / C + 1 : 0;   // blocks this CTA owns
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int SB = ff_slot_bytes(DT);
+
+    const FFLayout Y = ff_layout(NB, C, a.stage_cap, G, DT, DP);
+    uint8_t *X = smb + Y.X;
+    uint8_t *qsm = smb + Y.qsm;
+    SelectSmem S;
+    S.keys = reinterpret_cast<uint32_t *>(smb + Y.keys);
+    S.hist = reinterpret_cast<uint32_t *>(smb + Y.hist);
+    S.ckey = reinterpret_cast<uint32_t *>(smb + Y.ckey);
+    S.cidx = reinterpret_cast<uint32_t *>(smb + Y.cidx);
+    S.ccount = reinterpret_cast<uint32_t *>(smb + Y.ccount);
+    S.scan = reinterpret_cast<uint32_t *>(smb + Y.scan);
+    S.misc = reinterpret_cast<uint32_t *>(smb + Y.misc);
+    S.abort_flag = reinterpret_cast<int *>(smb + Y.abort_);
+    uint32_t *fine = reinterpret_cast<uint32_t *>(smb + Y.fine);
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(smb + Y.cnt);
+    uint32_t *bcnt = reinterpret_cast<uint32_t *>(smb + Y.bcnt);
+    int32_t *stok = reinterpret_cast<int32_t *>(smb + Y.stok);
+    uint32_t *skey = reinterpret_cast<uint32_t *>(smb + Y.skey);
+    uint8_t *kept = smb + Y.kept;
+    float *qs = reinterpret_cast<float *>(smb + Y.qs);
+    float *kpn = reinterpret_cast<float *>(smb + Y.kpn);
+    float *knew = reinterpret_cast<float *>(smb + Y.knew);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smb + Y.bar);
+    const int LIST = NB * 32;   // capacity of stok / skey / kept
+
+    auto tok_of = [&](int e) -> int64_t { return ((int64_t)(c + (e >> 5) * C) << 5) + (e & 31); };
+
+    // ---- 0. counters and the copy barrier
+    if (threadIdx.x < 32) cnt[threadIdx.x] = threadIdx.x == CN_H ? 0xFFFFu : threadIdx.x == CN_VALID ? 1u : 0u;
+    if (threadIdx.x == 0) {
+        *S.abort_flag = 0;
+        mbarrier_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // ---- 1. Kp blocks -> shared memory (bulk copies issued first by one warp)
+    const int blk_n = (int)(a.n >> 5);
+    const bool owner = (blk_n % C) == c;
+    int Lv = nb * 32;   // owned tokens (only the row's last block may be partial): local e < Lv
+    if (nb > 0 && ((nblk - 1) % C) == c) Lv -= (int)((int64_t)nblk * 32 - n_t);
+    if (warp == 0) {
+        if (lane == 0) mbarrier_arrive_expect_tx(bar, (uint32_t)Lv * DP * 2);
+        __syncwarp();
+        const uint16_t *Kpr = a.Kp + (int64_t)row * a.cap * DP;
+        for (int j = lane; j < nb; j += 32) {
+            const int64_t blk = (int64_t)c + (int64_t)j * C;
+            const int64_t rows = n_t - blk * 32 < 32 ? n_t - blk * 32 : 32;
+            bulk_g2s(X + (size_t)j * 32 * DP * 2, Kpr + blk * 32 * DP, (uint32_t)(rows * DP * 2), bar);
+        }
+    }
+    // ---- 1a. while the copies fly: importance query, attention query tile, append
+    const uint16_t *qi = a.q_imp + ((int64_t)b * a.Hq + (int64_t)h * G) * DP;
+    if (a.agg == TB_AGG_MEAN) {
+        const float inv = 1.0f / (float)G;
+        for (int i = threadIdx.x; i < DP; i += blockDim.x) {
+            float s = 0.f;
+            for (int g = 0; g < G; ++g) s += bf16_to_f(qi[g * DP + i]);
+            qs[i] = s * inv;
+        }
+    } else {
+        for (int i = threadIdx.x; i < G * DP; i += blockDim.x) qs[i] = bf16_to_f(qi[i]);
+    }
+    const uint16_t *qrow = a.q + ((int64_t)b * a.Hq + (int64_t)h * G) * DT;
+    for (int x = threadIdx.x; x < 16 * (DT / 8); x += blockDim.x) {
+        const int g = x / (DT / 8), cc = x % (DT / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (g < G) v = *reinterpret_cast<const uint4 *>(qrow + g * DT + cc * 8);
+        *reinterpret_cast<uint4 *>(qsm + g * (2 * DT + 16) + cc * 16) = v;
+    }
+    for (int x = threadIdx.x; x < kRadixBins; x += blockDim.x) S.hist[x] = 0;
+    for (int x = threadIdx.x; x < kFFFine; x += blockDim.x) fine[x] = 0;
+    // importance rows as MMA B fragments: lane (g, q) holds head g (+8) at the
+    // dims q*DP/4 .. (q+1)*DP/4 (the token rows use the same dim order)
+    constexpr int KSP = DP / 16;         // k-steps of 16 dims
+    constexpr int WPL = DP / 8;          // 32-bit words of a row per lane
+    constexpr int NHG = GM > 8 ? 2 : 1;  // groups of 8 heads
+    uint32_t qb[NHG][WPL];
+    {
+        const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+        for (int hg = 0; hg < NHG; ++hg) {
+            const int head = hg * 8 + g;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(qi + head * DP + q * (DP / 4));
+#pragma unroll
+            for (int w = 0; w < WPL; ++w) qb[hg][w] = head < G ? src[w] : 0u;
+        }
+    }
+    const uint16_t *Kh = a.K + (int64_t)row * a.cap * DT;
+    const uint16_t *Vh = a.V + (int64_t)row * a.cap * DT;
+    if (owner)
+        step_append_project(a.K_new, a.V_new, a.Wk, a.K, a.V, a.Kp, a.cap, a.n, row, h, DT, DP, knew, kpn,
+                            reinterpret_cast<float *>(S.ckey));
+    __syncthreads();
+    if (!mbarrier_wait_bounded(bar, 0, kWaitLimitNs)) {
+        set_status(a.dev_status, TB_ERR_TIMEOUT);
+        (void)mbarrier_wait_bounded(bar, 0, kWaitLimitNs);   // let copies in flight land before leaving
+        return;
+    }
+
+    // ---- 2. scores on the tensor cores: tiles of 16 tokens (A) x 8 heads (B),
+    // m16n8k16; per token the G dot products are averaged (or maxed), then the
+    // order-preserving key and its coarse bin
+    bool nan_seen = false;
+    {
+        const int g = lane >> 2, q = lane & 3;
+        const float invG = 1.0f / (float)G;
+        const int ntile = (nb * 32) >> 4;
+        for (int tt = warp; tt < ntile; tt += kFFWarps) {
+            const uint8_t *tb = X + (size_t)tt * 16 * DP * 2 + q * (DP / 2);
+            uint32_t w0[WPL], w1[WPL];
+            if (WPL == 4) {
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(tb + g * DP * 2);
+                const uint4 u1 = *reinterpret_cast<const uint4 *>(tb + (g + 8) * DP * 2);
+                w0[0] = u0.x; w0[1] = u0.y; w0[WPL > 2 ? 2 : 0] = u0.z; w0[WPL > 3 ? 3 : 0] = u0.w;
+                w1[0] = u1.x; w1[1] = u1.y; w1[WPL > 2 ? 2 : 0] = u1.z; w1[WPL > 3 ? 3 : 0] = u1.w;
+            } else {
+                const uint2 u0 = *reinterpret_cast<const uint2 *>(tb + g * DP * 2);
+                const uint2 u1 = *reinterpret_cast<const uint2 *>(tb + (g + 8) * DP * 2);
+                w0[0] = u0.x; w0[1] = u0.y;
+                w1[0] = u1.x; w1[1] = u1.y;
+            }
+            float ca[NHG][4];
+#pragma unroll
+            for (int hg = 0; hg < NHG; ++hg) {
+                ca[hg][0] = ca[hg][1] = ca[hg][2] = ca[hg][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KSP; ++ks)
+                    mma_bf16_16816(ca[hg], w0[2 * ks], w1[2 * ks], w0[2 * ks + 1], w1[2 * ks + 1], qb[hg][2 * ks],
+                                   qb[hg][2 * ks + 1]);
+            }
+            float v0, v1;
+            if (a.agg == TB_AGG_MEAN) {
+                v0 = 0.f;
+                v1 = 0.f;
+#pragma unroll
+                for (int hg = 0; hg < NHG; ++hg) {
+                    v0 += ca[hg][0] + ca[hg][1];
+                    v1 += ca[hg][2] + ca[hg][3];
+                }
+                v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+                v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+                v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 2);
+                v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 2);
+                v0 *= invG;
+                v1 *= invG;
+            } else {
+                v0 = -INFINITY;
+                v1 = -INFINITY;
+#pragma unroll
+                for (int hg = 0; hg < NHG; ++hg) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        if (hg * 8 + 2 * q + u < G) {
+                            v0 = fmaxf(v0, ca[hg][u]);
+                            v1 = fmaxf(v1, ca[hg][2 + u]);
+                        }
+                    }
+                }
+                v0 = fmaxf(v0, __shfl_xor_sync(0xFFFFFFFFu, v0, 1));
+                v1 = fmaxf(v1, __shfl_xor_sync(0xFFFFFFFFu, v1, 1));
+                v0 = fmaxf(v0, __shfl_xor_sync(0xFFFFFFFFu, v0, 2));
+                v1 = fmaxf(v1, __shfl_xor_sync(0xFFFFFFFFu, v1, 2));
+            }
+            if (q < 2) {
+                const int e = tt * 16 + g + 8 * q;
+                uint32_t key = 0;
+                if (e < Lv) {
+                    key = score_key(q ? v1 : v0, nan_seen);
+                    atomicAdd(&S.hist[key >> 21], 1u);
+                }
+                S.keys[e] = key;
+            }
+        }
+    }
+    __syncthreads();
+    if (owner && threadIdx.x == 0) {
+        // the appended token scores from its freshly projected row (its Kp
+        // row in shared memory may predate the append)
+        float s = -INFINITY;
+        const int ng = a.agg == TB_AGG_MEAN ? 1 : G;
+        for (int g = 0; g < ng; ++g) {
+            float p = 0.f;
+            for (int i = 0; i < DP; ++i) p = fmaf(qs[g * DP + i], kpn[i], p);
+            s = fmaxf(s, p);
+        }
+        const int en = (blk_n / C) * 32 + (int)(a.n & 31);
+        atomicSub(&S.hist[S.keys[en] >> 21], 1u);
+        const uint32_t key = score_key(s, nan_seen);
+        atomicAdd(&S.hist[key >> 21], 1u);
+        S.keys[en] = key;
+    }
+    if (nan_seen) set_status(a.dev_status, TB_ERR_NONFINITE);
+    __syncthreads();
+
+    // ---- 3. local window around the row's threshold
+    uint32_t need_hi = 0, need_lo = 0;   // ranks from the top; 0 = no bound on that side
+    {
+        const int t_c = (int)(((int64_t)a.k * Lv + n_t / 2) / n_t);
+        const float p = (float)a.k / (float)n_t;
+        const int R = (int)ceilf(5.0f * sqrtf((float)t_c * (1.0f - p))) + 4;
+        if (t_c - R >= 0 && Lv > 0) need_hi = (uint32_t)(t_c - R + 1);
+        if (t_c + R <= Lv) need_lo = (uint32_t)(t_c + R);
+    }
+    uint32_t *bins = S.misc;   // {Bhi, Ahi, Blo, Alo}
+    find_two_bins(S.hist, kRadixBins, need_hi, need_lo, S.scan, bins);
+    const uint32_t Bhi = bins[0], Blo = bins[2];
+    uint32_t F0 = 0;
+    if (Bhi != kNone) F0 = Bhi >= 3 ? Bhi - 3 : 0;
+    else if (Blo != kNone) F0 = Blo >= 3 ? Blo - 3 : 0;
+    for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+        const bool valid = e < Lv;
+        const uint32_t key = S.keys[e];
+        const uint32_t cb = key >> 21;
+        if (valid && cb >= F0 && cb <= F0 + 3) atomicAdd(&fine[(key >> 16) - (F0 << 5)], 1u);
+        const uint32_t ob = __ballot_sync(0xFFFFFFFFu, valid && cb > F0 + 3);
+        if (lane == 0 && ob) atomicAdd(&cnt[CN_RANGE], (uint32_t)__popc(ob));
+    }
+    __syncthreads();
+    if (warp == 0) warp_find_fine(fine, cnt[CN_RANGE], need_hi, need_lo, S.misc + 4);
+    __syncthreads();
+    uint32_t hi16 = 0xFFFFu, lo16 = 0u;
+    if (Bhi != kNone) hi16 = S.misc[4] != kNone ? (F0 << 5) + S.misc[4] : ((Bhi << 5) | 31u);
+    if (Blo != kNone) lo16 = S.misc[5] != kNone ? (F0 << 5) + S.misc[5] : (Blo << 5);
+    if (need_hi == 0) hi16 = 0xFFFFu;
+    if (need_lo == 0) lo16 = 0u;
+
+    // ---- 4. publish the record; tokens above the window at the front of
+    // stok, tokens inside it at the back
+    RowCtl *rc = a.ctl + row;
+    uint8_t *myrec = a.rec + ((int64_t)row * C + c) * kFFRecBytes;
+    uint2 *myent = reinterpret_cast<uint2 *>(myrec + sizeof(FFHdr));
+    uint8_t *blkab = a.blk_above + (int64_t)row * a.blk_stride;
+    for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+        const int64_t t = tok_of(e);
+        const uint32_t key = S.keys[e];
+        const uint32_t pf = key >> 16;
+        const bool valid = e < Lv;
+        const bool above = valid && pf > hi16;
+        const bool inwin = valid && !above && pf >= lo16;
+        const uint32_t ab = __ballot_sync(0xFFFFFFFFu, above);
+        if (lane == 0) blkab[c + (e >> 5) * C] = (uint8_t)__popc(ab);
+        const uint32_t as = warp_alloc(&cnt[CN_ABOVE], above);
+        if (above) {
+            stok[as] = (int32_t)t;
+            skey[as] = key;
+        }
+        const uint32_t ws = warp_alloc(&cnt[CN_WIN], inwin);
+        if (inwin) {
+            stok[LIST - 1 - ws] = (int32_t)t;
+            skey[LIST - 1 - ws] = key;
+            if (ws < (uint32_t)kFFEntMax) myent[ws] = make_uint2(key, (uint32_t)t);
+        }
+    }
+    __syncthreads();
+    const int n_above = (int)cnt[CN_ABOVE], n_win = (int)cnt[CN_WIN];
+    const int n_att = n_above + n_win;
+    if (threadIdx.x == 0) {
+        FFHdr hd;
+        hd.above = (uint32_t)n_above;
+        hd.lo = lo16;
+        hd.hi = hi16;
+        hd.n_ent = (uint32_t)n_win;
+        hd.valid = n_win <= kFFEntMax ? 1u : 0u;
+        hd.pad0 = hd.pad1 = hd.pad2 = 0;
+        *reinterpret_cast<FFHdr *>(myrec) = hd;
+    }
+    group_arrive(&rc->bar);
+
+    // ---- 4b. gather the first round of K/V rows (above, then window)
+    auto att_tok = [&](int i) -> int64_t { return i < n_above ? stok[i] : stok[LIST - 1 - (i - n_above)]; };
+    auto att_key = [&](int i) -> uint32_t { return i < n_above ? skey[i] : skey[LIST - 1 - (i - n_above)]; };
+    constexpr int CPR = DT / 8;   // 16-byte chunks per row
+    auto gather_round = [&](int r0, int nr) {
+        for (int x = threadIdx.x; x < nr * 2 * CPR; x += blockDim.x) {
+            const int s = x / (2 * CPR), ci = x % (2 * CPR);
+            const bool isv = ci >= CPR;
+            const int cc = isv ? ci - CPR : ci;
+            const int64_t t = att_tok(r0 + s);
+            cp_async16(X + (size_t)s * SB + (isv ? 2 * DT : 0) + cc * 16, (isv ? Vh : Kh) + t * DT + cc * 8);
+        }
+        cp_async_commit();
+    };
+    const int n_r1 = n_att < a.stage_cap ? n_att : a.stage_cap;
+    gather_round(0, n_r1);
+
+    // ---- 5. the row's exchange; read every record of the row
+    if (!group_wait(&rc->bar, (uint32_t)C, S.abort_flag, a.dev_status)) {
+        cp_async_wait_all();
+        return;
+    }
+    const int P = blockDim.x / C;   // threads per record
+    const int rr = threadIdx.x / P, rsub = threadIdx.x % P;
+    uint4 hd4 = make_uint4(0, 0, 0, 0);
+    uint32_t hvalid = 1;
+    uint2 ent[kFFEntPerThread];
+    const uint8_t *rrec = a.rec + ((int64_t)row * C + (rr < C ? rr : 0)) * kFFRecBytes;
+    if (rr < C) {
+        hd4 = __ldcg(reinterpret_cast<const uint4 *>(rrec));
+        hvalid = __ldcg(reinterpret_cast<const uint32_t *>(rrec) + 4);
+    }
+#pragma unroll
+    for (int i = 0; i < kFFEntPerThread; ++i) {
+        const int e = rsub + P * i;
+        ent[i] = (rr < C && e < kFFEntMax) ? __ldcg(reinterpret_cast<const uint2 *>(rrec + sizeof(FFHdr)) + e)
+                                           : make_uint2(0, 0);
+    }
+    for (int x = threadIdx.x; x < nblk; x += blockDim.x) bcnt[x] = __ldcg(blkab + x);
+    if (rr < C && rsub == 0) {
+        atomicMax(&cnt[CN_L], hd4.y);
+        atomicMin(&cnt[CN_H], hd4.z);
+        atomicAdd(&cnt[CN_ASUM], hd4.x);
+        if (!hvalid || hd4.w > (uint32_t)(P * kFFEntPerThread)) cnt[CN_VALID] = 0;
+    }
+    __syncthreads();
+    const uint32_t Lw = cnt[CN_L], Hw = cnt[CN_H];
+    bool fast = cnt[CN_VALID] != 0 && Lw <= Hw;
+    uint32_t is_cand = 0;
+    if (fast) {
+#pragma unroll
+        for (int i = 0; i < kFFEntPerThread; ++i) {
+            const bool have = rr < C && (uint32_t)(rsub + P * i) < hd4.w;
+            const uint32_t pf = ent[i].x >> 16;
+            const bool hi_side = have && pf > Hw;
+            const bool cand = have && !hi_side && pf >= Lw;
+            if (hi_side) atomicAdd(&bcnt[ent[i].y >> 5], 1u);
+            const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hi_side);
+            if (lane == 0 && hb) atomicAdd(&cnt[CN_AE], (uint32_t)__popc(hb));
+            const uint32_t cs = warp_alloc(&cnt[CN_CAND], cand);
+            if (cand && cs < (uint32_t)kCandCap) {
+                S.ckey[cs] = ent[i].x;
+                S.cidx[cs] = ent[i].y;
+            }
+            if (cand) is_cand |= 1u << i;
+        }
+    }
+    __syncthreads();
+    const uint32_t m = cnt[CN_CAND];
+    const int64_t need = (int64_t)a.k - (int64_t)cnt[CN_ASUM] - (int64_t)cnt[CN_AE];
+    fast = fast && m <= (uint32_t)kCandCap && need >= 1 && need <= (int64_t)m;
+
+    // ---- 5b. the exact threshold T among the candidates
+    uint64_t T = 0;
+    uint64_t *Tsm = reinterpret_cast<uint64_t *>(S.misc + 8);
+    if (fast) {
+        bool done = false;
+        if (Hw - Lw < (uint32_t)kFFFine) {
+            for (int x = threadIdx.x; x < kFFFine; x += blockDim.x) fine[x] = 0;
+            __syncthreads();
+            for (uint32_t e = threadIdx.x; e < m; e += blockDim.x) atomicAdd(&fine[(S.ckey[e] >> 16) - Lw], 1u);
+            __syncthreads();
+            if (warp == 0) warp_find_fine(fine, 0, (uint32_t)need, 0, S.misc);
+            __syncthreads();
+            const uint32_t bstar = S.misc[0], babove = S.misc[2], bc = S.misc[4];
+            if (bstar != kNone && bc <= (uint32_t)kFFThreads) {
+                // rank count inside the bin (composites are distinct)
+                uint64_t *comp = reinterpret_cast<uint64_t *>(S.hist);
+                for (uint32_t e0 = 0; e0 < m; e0 += blockDim.x) {
+                    const uint32_t e = e0 + threadIdx.x;
+                    const bool in = e < m && ((S.ckey[e] >> 16) - Lw) == bstar;
+                    const uint32_t sl = warp_alloc(&cnt[CN_BM], in);
+                    if (in) comp[sl] = composite(S.ckey[e], S.cidx[e]);
+                }
+                __syncthreads();
+                const uint32_t need2 = (uint32_t)need - babove;
+                if (threadIdx.x < bc) {
+                    const uint64_t v = comp[threadIdx.x];
+                    uint32_t rank = 0;
+                    for (uint32_t j = 0; j < bc; ++j) rank += comp[j] > v ? 1u : 0u;
+                    if (rank == need2 - 1) *Tsm = v;
+                }
+                __syncthreads();
+                T = *Tsm;
+                done = true;
+            }
+        }
+        if (!done) T = local_select(S.ckey, S.cidx, m, (uint32_t)need, 32, S);
+    }
+
+    float *prow = a.part + (int64_t)row * C * G * (2 + DT);
+    bool reset_hist = false;
+    if (fast) {
+        // ---- 5c. per-block kept counts of the row -> ascending idx / sel slots
+#pragma unroll
+        for (int i = 0; i < kFFEntPerThread; ++i)
+            if (((is_cand >> i) & 1u) && composite(ent[i].x, ent[i].y) >= T) atomicAdd(&bcnt[ent[i].y >> 5], 1u);
+        for (int i = threadIdx.x; i < n_att; i += blockDim.x)
+            kept[i] = composite(att_key(i), (uint32_t)att_tok(i)) >= T ? 1 : 0;
+        __syncthreads();
+        block_scan_inplace(bcnt, nblk, S.scan);
+        int32_t *irow = a.idx + (int64_t)row * a.k;
+        int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
+        for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+            const int64_t t = tok_of(e);
+            const bool kp = e < Lv && composite(S.keys[e], (uint32_t)t) >= T;
+            const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
+            if (kp) {
+                const uint32_t slot = bcnt[t >> 5] + (uint32_t)__popc(km & ((1u << lane) - 1u));
+                if (slot < (uint32_t)a.k) {
+                    irow[slot] = (int32_t)t;
+                    srow[slot] = (int32_t)t;
+                } else {
+                    set_status(a.dev_status, TB_ERR_INVALID_ARG);
+                }
+            }
+        }
+        // ---- 6. attention over the gathered rows, round by round
+        MmaAttn<NT> A;
+        A.m0 = A.m1 = -INFINITY;
+        A.l0 = A.l1 = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) A.o[t][0] = A.o[t][1] = A.o[t][2] = A.o[t][3] = 0.f;
+        const float qscale = a.scale * kLog2e;
+        for (int r0 = 0; r0 < n_att; r0 += a.stage_cap) {
+            const int nr = n_att - r0 < a.stage_cap ? n_att - r0 : a.stage_cap;
+            if (r0 > 0) {
+                __syncthreads();   // the previous round's rows are consumed
+                gather_round(r0, nr);
+            }
+            cp_async_wait_all();
+            __syncthreads();
+            // rows that take no part (not kept, or padding to 16) hold zeros in V
+            const int npad = (nr + 15) & ~15;
+            for (int x = threadIdx.x; x < npad * CPR; x += blockDim.x) {
+                const int s = x / CPR, cc = x % CPR;
+                if (s >= nr || !kept[r0 + s])
+                    *reinterpret_cast<uint4 *>(X + (size_t)s * SB + 2 * DT + cc * 16) = make_uint4(0, 0, 0, 0);
+            }
+            __syncthreads();
+            mma_attend<DT>(A, X, SB, nr, kept, r0, qsm, qscale);
+        }
+        // ---- 6b. combine the warps' states into this CTA's partial
+        A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 1);
+        A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 2);
+        A.l1 += __shfl_xor_sync(0xFFFFFFFFu, A.l1, 1);
+        A.l1 += __shfl_xor_sync(0xFFFFFFFFu, A.l1, 2);
+        __syncthreads();   // X is free: warp states go there
+        float *ws = reinterpret_cast<float *>(X);
+        const int sg = 2 + DT;
+        {
+            const int g0 = lane >> 2, d0 = 2 * (lane & 3);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int g = g0 + 8 * half;
+                if (g < G) {
+                    float *w = ws + ((int64_t)warp * G + g) * sg;
+                    if ((lane & 3) == 0) {
+                        w[0] = half ? A.m1 : A.m0;
+                        w[1] = half ? A.l1 : A.l0;
+                    }
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        w[2 + 8 * t + d0] = A.o[t][2 * half];
+                        w[2 + 8 * t + d0 + 1] = A.o[t][2 * half + 1];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        for (int x = threadIdx.x; x < G * DT; x += blockDim.x) {
+            const int g = x / DT, d = x % DT;
+            float M = -INFINITY;
+            for (int w = 0; w < kFFWarps; ++w) M = fmaxf(M, ws[((int64_t)w * G + g) * sg]);
+            float L = 0.f, Acc = 0.f;
+            for (int w = 0; w < kFFWarps; ++w) {
+                const float *sw = ws + ((int64_t)w * G + g) * sg;
+                const float wt = rescale_w(sw[0], M);
+                L += wt * sw[1];
+                Acc += wt * sw[2 + d];
+            }
+            float *o = prow + ((int64_t)c * G + g) * sg;
+            if (d == 0) {
+                o[0] = M;
+                o[1] = L;
+            }
+            o[2 + d] = Acc;
+        }
+    } else {
+        cp_async_wait_all();
+        if (!ff_general_path<GM>(a, S, stok, reinterpret_cast<float *>(X), row, c, nb, n_t, Kh, Vh, qrow, prow))
+            return;
+        reset_hist = true;
+    }
+    if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
+
+    // ---- 7. the row's last CTA merges the partial states
+    row_merge_tail(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT,
+                   reinterpret_cast<float *>(S.ckey), &cnt[CN_FLAG], reset_hist, a.dev_status);
+}
+
+// ------------------------------------------------------------------ host side
+
+struct FFPlan {
+    int C = 0, NB = 0, stage_cap = 0, cpt = 0, gm = 0;
+    size_t smem = 0;
+};
+
+static int ff_gm(int G) { return G <= 1 ? 1 : G <= 4 ? 4 : 16; }
+
+template <int CPT, int DT, int GM>
+static int ff_occupancy(size_t smem) {
+    if (cudaFuncSetAttribute(fused_fast_kernel<CPT, DT, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 0;
+    int per = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fused_fast_kernel<CPT, DT, GM>, kFFThreads, smem) !=
+        cudaSuccess)
+        return 0;
+    return per;
+}
+
+#define TB_FF_CASES(X) X(2, 64, 1) X(2, 64, 4) X(2, 64, 16) X(2, 128, 1) X(2, 128, 4) X(2, 128, 16) \
+    X(4, 64, 1) X(4, 64, 4) X(4, 64, 16) X(4, 128, 1) X(4, 128, 4) X(4, 128, 16)
+
+static bool ff_plan_uncached(const tb_shape &sh, int64_t n_t, FFPlan &P) {
+    const DevInfo &di = dev_info();
+    if (di.sms <= 0) return false;
+    const int cpt = sh.dp / 8;
+    if (sh.dp % 8 != 0 || (cpt != 2 && cpt != 4)) return false;
+    if (sh.D != 64 && sh.D != 128) return false;
+    const int G = sh.Hq / sh.Hkv;
+    if (G > 16) return false;
+    const int rows = sh.B * sh.Hkv;
+    const int64_t nblk = (n_t + 31) / 32;
+    int64_t C = di.sms / rows;
+    if (C > nblk) C = nblk;
+    if (C > kMaxChunks) C = kMaxChunks;
+    if (C < 1) return false;
+    const int64_t NB = (nblk + C - 1) / C;
+    if (NB * 32 > 16384) return false;                 // keys and lists must fit shared memory
+    if (2 * C * G + G > 2 * kCandCap) return false;     // merge scratch
+    int lo = 16, hi = kFFStageMax;                       // largest round of gathered rows that fits
+    if (ff_layout((int)NB, (int)C, lo, G, sh.D, sh.dp).total > di.max_smem_optin) return false;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (ff_layout((int)NB, (int)C, mid, G, sh.D, sh.dp).total <= di.max_smem_optin) lo = mid;
+        else hi = mid - 1;
+    }
+    P.C = (int)C;
+    P.NB = (int)NB;
+    P.stage_cap = lo & ~15;
+    P.cpt = cpt;
+    P.gm = ff_gm(G);
+    P.smem = (size_t)ff_layout(P.NB, P.C, P.stage_cap, G, sh.D, sh.dp).total;
+    int occ = 0;
+#define TB_FF_OCC(CP, DTT, GMC) \
+    if (P.cpt == CP && sh.D == DTT && P.gm == GMC) occ = ff_occupancy<CP, DTT, GMC>(P.smem);
+    TB_FF_CASES(TB_FF_OCC)
+#undef TB_FF_OCC
+    return occ >= 1 && (int64_t)rows * C <= (int64_t)occ * di.sms;
+}
+
+static bool ff_plan(const tb_shape &sh, int64_t n_t, FFPlan &P) {
+    struct Key {
+        int dev, B, Hq, Hkv, D, dp;
+        int64_t n;
+    };
+    static thread_local Key last = {-2, 0, 0, 0, 0, 0, 0};
+    static thread_local bool last_ok = false;
+    static thread_local FFPlan last_plan;
+    Key k = {dev_info().device, sh.B, sh.Hq, sh.Hkv, sh.D, sh.dp, n_t};
+    if (memcmp(&k, &last, sizeof k) != 0) {
+        last_plan = FFPlan();
+        last_ok = ff_plan_uncached(sh, n_t, last_plan);
+        last = k;
+    }
+    P = last_plan;
+    return last_ok;
+}
+
+bool fused_fast_supported(const tb_shape &sh, int64_t n_tokens, int32_t k) {
+    if (k < 1 || k > n_tokens) return false;
+    FFPlan P;
+    if (!ff_plan(sh, n_tokens, P)) return false;
+    return P.C <= fused_chunks(sh, n_tokens);
+}
+
+cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64_t n, const uint16_t *q,
+                              const uint16_t *q_imp, const uint16_t *K_new, const uint16_t *V_new,
+                              const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx_state,
+                              int32_t *sel, int32_t *counts, uint16_t *out, const FastWs &w, int32_t sel_stride,
+                              int32_t *dev_status, cudaStream_t st) {
+    FFPlan P;
+    if (!ff_plan(sh, n + 1, P)) return cudaErrorNotSupported;
+    FFArgs a;
+    a.q = q; a.q_imp = q_imp; a.K_new = K_new; a.V_new = V_new; a.Wk = Wk;
+    a.K = K; a.V = V; a.Kp = Kp;
+    a.idx = idx_state; a.sel = sel; a.counts = counts; a.out = out;
+    a.ctl = w.ctl; a.part = w.part; a.rec = w.rec; a.blk_above = w.blk_above; a.keys_g = w.keys_g;
+    a.dev_status = dev_status;
+    a.cap = sh.cap; a.n = n; a.keys_stride = w.keys_stride;
+    a.Hq = sh.Hq; a.Hkv = sh.Hkv; a.D = sh.D; a.k = p.k; a.agg = p.agg; a.sel_stride = sel_stride;
+    a.scale = p.scale;
+    a.C = P.C; a.NB = P.NB; a.blk_stride = (int)w.blk_stride; a.stage_cap = P.stage_cap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(P.C * sh.B * sh.Hkv));
+    cfg.blockDim = dim3(kFFThreads);
+    cfg.dynamicSmemBytes = P.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#define TB_FF_LAUNCH(CP, DTT, GMC) \
+    if (P.cpt == CP && sh.D == DTT && P.gm == GMC) return cudaLaunchKernelEx(&cfg, fused_fast_kernel<CP, DTT, GMC>, a);
+    TB_FF_CASES(TB_FF_LAUNCH)
+#undef TB_FF_LAUNCH
+    return cudaErrorNotSupported;
+}
+
+}  // namespace tb

@@ -20,9 +20,8 @@
 // algorithmic bytes is the histogram/candidate exchange and the partials.
 #include <string.h>
 
-#include "attn_core.cuh"
+#include "fused_common.cuh"
 #include "kernels.cuh"
-#include "topk_core.cuh"
 
 namespace tb {
 
@@ -45,10 +44,7 @@ struct FusedArgs {
     int C, L;
 };
 
-__host__ __device__ inline int comb_floats(int G, int D) {
-    const int f = (kFusedThreads / 32) * G * (2 + D);
-    return f > kFusedThreads ? f : kFusedThreads;
-}
+__host__ __device__ inline int comb_floats(int G, int D) { return comb_floats_for(kFusedThreads, G, D); }
 
 __host__ __device__ inline size_t fused_smem_bytes(int L, int G, int D, int dp) {
     size_t b = (size_t)L * 4                       // keys
@@ -114,39 +110,7 @@ fused_step_kernel(const FusedArgs a) {
     const bool owner = a.n >= t0 && a.n < t0 + Lc;
     const uint16_t *Kh = a.K + (int64_t)row * a.cap * D;
     const uint16_t *Vh = a.V + (int64_t)row * a.cap * D;
-    if (owner) {
-        const uint16_t *kn = a.K_new + (int64_t)row * D;
-        const uint16_t *vn = a.V_new + (int64_t)row * D;
-        uint16_t *Kr = a.K + ((int64_t)row * a.cap + a.n) * D;
-        uint16_t *Vr = a.V + ((int64_t)row * a.cap + a.n) * D;
-        for (int d = threadIdx.x; d < D; d += blockDim.x) {
-            const uint16_t kb = kn[d];
-            knew[d] = bf16_to_f(kb);
-            Kr[d] = kb;
-            Vr[d] = vn[d];
-        }
-        __syncthreads();
-        // Kp row: threads (j, slice) accumulate over a slice of D, summed in comb
-        const uint16_t *W = a.Wk + (int64_t)h * D * dp;
-        const int jn = dp < (int)blockDim.x ? dp : (int)blockDim.x;
-        const int slices = blockDim.x / jn;
-        const int dlen = (D + slices - 1) / slices;
-        const int j = threadIdx.x % jn, sl = threadIdx.x / jn;
-        float acc = 0.f;
-        if (sl < slices) {
-            const int d0 = sl * dlen, d1 = min(D, d0 + dlen);
-            for (int d = d0; d < d1; ++d) acc = fmaf(knew[d], bf16_to_f(W[(int64_t)d * dp + j]), acc);
-            comb[sl * jn + j] = acc;
-        }
-        __syncthreads();
-        if (threadIdx.x < dp) {
-            float s = 0.f;
-            for (int x = 0; x < slices; ++x) s += comb[x * jn + threadIdx.x];
-            const uint16_t kb = f_to_bf16(s);
-            a.Kp[((int64_t)row * a.cap + a.n) * dp + threadIdx.x] = kb;
-            kpn[threadIdx.x] = bf16_to_f(kb);
-        }
-    }
+    if (owner) step_append_project(a.K_new, a.V_new, a.Wk, a.K, a.V, a.Kp, a.cap, a.n, row, h, D, dp, knew, kpn, comb);
     __syncthreads();
 
     // ---- 2. scores of this chunk -> keys in shared memory
@@ -219,82 +183,21 @@ fused_step_kernel(const FusedArgs a) {
     if (nan_seen) set_status(a.dev_status, TB_ERR_NONFINITE);
     __syncthreads();
 
-    // ---- 3. selection, first half; then attend the tokens above the bin
+    // ---- 3-4. exact selection; attention over this chunk's kept tokens
     RowCtl *rc = a.ctl + row;
-    SelectBegin B = group_select_begin(rc, S, Lc, L, c, C, (uint32_t)a.k, a.dev_status);
-    if (!B.ok) return;
-    uint32_t n_above = 0;
-    for (int e0 = 0; e0 < Lc; e0 += blockDim.x) {
-        const int e = e0 + threadIdx.x;
-        const uint32_t f = (e < Lc && above_bin(B, S.keys[e])) ? 1u : 0u;
-        uint32_t tot;
-        const uint32_t pos = block_exclusive_scan(f, S.scan, tot);
-        if (f) list[n_above + pos] = e;
-        n_above += tot;
-    }
-    __syncthreads();
     const int TPG = D / 8;
     const int gl = (threadIdx.x & 31) % TPG;
     AttnLane<GM> A;
     attn_init(A, a.q + ((int64_t)b * a.Hq + (int64_t)h * G) * D, G, D, gl, a.scale);
-    attn_tokens(A, G, D, (int)n_above, [&](int j) -> int64_t { return t0 + list[j]; }, Kh, Vh, a.cap,
-                a.dev_status);
-    __syncthreads();
-
-    // ---- 4. exact threshold; kept tokens out (ascending); attend the kept bin tokens
-    SelectResult R = group_select_end(rc, S, B, L, c, C, a.dev_status);
-    if (!R.ok) return;
-    int32_t *irow = a.idx + (int64_t)row * a.k;
-    int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
-    uint32_t base_kept = 0, base_tied = 0, n_bin = 0;
-    for (int e0 = 0; e0 < Lc; e0 += blockDim.x) {
-        const int e = e0 + threadIdx.x;
-        uint32_t key = 0, tied = 0;
-        if (e < Lc) {
-            key = S.keys[e];
-            tied = (R.mode == 1 && key == R.tkey) ? 1u : 0u;
-        }
-        uint32_t ttot;
-        const uint32_t tied_before = base_tied + block_exclusive_scan(tied, S.scan, ttot);
-        const bool kept = e < Lc && is_kept(R, key, (uint32_t)(t0 + e), tied_before);
-        const uint32_t kf = kept ? 1u : 0u;
-        const uint32_t bf = (kept && !above_bin(B, key)) ? 1u : 0u;
-        uint32_t ktot, btot;
-        const uint32_t pos = block_exclusive_scan(kf, S.scan, ktot);
-        const uint32_t bpos = block_exclusive_scan(bf, S.scan, btot);
-        if (kept) {
-            const uint32_t slot = R.offset + base_kept + pos;
-            irow[slot] = (int32_t)(t0 + e);
-            srow[slot] = (int32_t)(t0 + e);
-        }
-        if (bf) list[n_bin + bpos] = e;
-        base_kept += ktot;
-        base_tied += ttot;
-        n_bin += btot;
-    }
-    __syncthreads();
-    attn_tokens(A, G, D, (int)n_bin, [&](int j) -> int64_t { return t0 + list[j]; }, Kh, Vh, a.cap, a.dev_status);
+    if (!chunk_select_attend(A, rc, S, list, Lc, L, c, C, 0, (uint32_t)a.k, t0, Kh, Vh, a.cap, G, D,
+                             a.idx + (int64_t)row * a.k, a.sel + (int64_t)row * a.sel_stride, a.dev_status))
+        return;
     if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
 
     // ---- 5. partial state; the row's last CTA merges and resets the row
-    float *prow = a.part + (int64_t)row * C * G * (2 + D);
-    attn_block_combine(A, G, D, comb, prow + (int64_t)c * G * (2 + D));
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(&rc->done, 1u);
-        S.misc[6] = (prev == (uint32_t)(C - 1)) ? 1u : 0u;
-    }
-    __syncthreads();
-    if (!S.misc[6]) return;
-    __threadfence();
-    attn_merge(prow, C, G, D, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * D, a.dev_status,
-               reinterpret_cast<float *>(S.ckey));
-    for (int x = threadIdx.x; x < 3 * kRadixBins; x += blockDim.x) (&rc->hist[0][0])[x] = 0;
-    if (threadIdx.x == 0) {
-        rc->bar = 0;
-        rc->ncand = 0;
-        rc->done = 0;
-    }
+    row_finish(A, rc, a.part + (int64_t)row * C * G * (2 + D), c, C, G, D,
+               a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * D, comb, reinterpret_cast<float *>(S.ckey), &S.misc[6],
+               true, a.dev_status);
 }
 
 // ------------------------------------------------------------------ host side

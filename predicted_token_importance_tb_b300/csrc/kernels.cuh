@@ -44,4 +44,22 @@ cudaError_t launch_fused_step(const tb_shape &sh, const tb_step_params &p, int64
                               int32_t *sel, int32_t *counts, uint16_t *out, RowCtl *ctl, uint32_t *attn_ctl,
                               float *partials, int32_t sel_stride, int32_t *dev_status, cudaStream_t st);
 
+// The decode step (T == 1, r == 0) as one cooperative kernel with a single
+// exchange between the CTAs of a row (fused_fast.cu).
+struct FastWs {
+    RowCtl *ctl;
+    float *part;
+    uint8_t *rec;
+    uint8_t *blk_above;
+    int64_t blk_stride;
+    uint32_t *keys_g;
+    int64_t keys_stride;
+};
+bool fused_fast_supported(const tb_shape &sh, int64_t n_tokens, int32_t k);
+cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64_t n, const uint16_t *q,
+                              const uint16_t *q_imp, const uint16_t *K_new, const uint16_t *V_new,
+                              const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx_state,
+                              int32_t *sel, int32_t *counts, uint16_t *out, const FastWs &w, int32_t sel_stride,
+                              int32_t *dev_status, cudaStream_t st);
+
 }  // namespace tb

@@ -188,9 +188,10 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     if (body > np) body = np;
     if ((int64_t)sel_stride < body + (n_t - np)) return TB_ERR_INVALID_ARG;
     const int rows = shape->B * shape->Hkv;
-    const bool fused = predict && p->T == 1 && p->r == 0 && !(p->flags & TB_STEP_UNFUSED) &&
-                       fused_step_supported(*shape, n_t, p->k);
-    const WsLayout L = layout_for(*shape, n_t, sel_stride, fused ? fused_chunks(*shape, n_t) : 0);
+    const bool one_launch = predict && p->T == 1 && p->r == 0 && !(p->flags & TB_STEP_UNFUSED);
+    const bool fast = one_launch && fused_fast_supported(*shape, n_t, p->k);
+    const bool fused = one_launch && !fast && fused_step_supported(*shape, n_t, p->k);
+    const WsLayout L = layout_for(*shape, n_t, sel_stride, (fused || fast) ? fused_chunks(*shape, n_t) : 0);
     if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
     uint8_t *w = static_cast<uint8_t *>(ws);
     RowCtl *ctl = reinterpret_cast<RowCtl *>(w + L.rowctl_off);
@@ -198,6 +199,21 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     float *part = reinterpret_cast<float *>(w + L.part_off);
     float *scores = reinterpret_cast<float *>(w + L.scores_off);
     cudaError_t e;
+    if (fast) {
+        FastWs fw;
+        fw.ctl = ctl;
+        fw.part = part;
+        fw.rec = w + L.rec_off;
+        fw.blk_above = w + L.blk_off;
+        fw.blk_stride = L.blk_stride;
+        fw.keys_g = reinterpret_cast<uint32_t *>(scores);
+        fw.keys_stride = n_t;
+        e = launch_fused_fast(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, sel, counts, out, fw,
+                              sel_stride, dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        *n_pred = n_t;
+        return TB_OK;
+    }
     if (fused) {
         e = launch_fused_step(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, sel, counts, out, ctl,
                               actl, part, sel_stride, dev_status, stream);

@@ -124,14 +124,15 @@ struct SelectBegin {
 // the final barrier without waiting, so it can work on tokens that are kept
 // whatever the exact threshold (those above the bin) in the meantime.
 // Keys of this CTA's chunk are in S.keys[0..Lc). Chunk c of C covers tokens
-// c*L .. c*L+Lc-1; budget k with 1 <= k <= n.
+// c*L .. c*L+Lc-1; budget k with 1 <= k <= n. bar_base: phases of ctl->bar
+// the group has already completed in this launch.
 __device__ __forceinline__ SelectBegin group_select_begin(RowCtl *ctl, SelectSmem &S, int Lc, int L, int c, int C,
-                                                          uint32_t k, int32_t *dev_status) {
+                                                          uint32_t k, int32_t *dev_status, int bar_base = 0) {
     SelectBegin B;
     B.ok = true;
     uint32_t prefix = 0, need = k, bincount = 0;
     int shift = 32;
-    int nbar = 0;
+    int nbar = bar_base;
     for (int pass = 0; pass < 3; ++pass) {
         const int bits = pass < 2 ? kRadixBits : 32 - 2 * kRadixBits;
         const int upper = shift;   // bits above this pass's digit are fixed to `prefix`
@@ -264,8 +265,8 @@ __device__ __forceinline__ SelectResult group_select_end(RowCtl *ctl, SelectSmem
 
 // The whole threshold search (both halves back to back).
 __device__ __forceinline__ SelectResult group_select(RowCtl *ctl, SelectSmem &S, int Lc, int L, int c, int C,
-                                                     uint32_t k, int32_t *dev_status) {
-    SelectBegin B = group_select_begin(ctl, S, Lc, L, c, C, k, dev_status);
+                                                     uint32_t k, int32_t *dev_status, int bar_base = 0) {
+    SelectBegin B = group_select_begin(ctl, S, Lc, L, c, C, k, dev_status, bar_base);
     if (!B.ok) {
         SelectResult R;
         R.ok = false;

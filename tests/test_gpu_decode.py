@@ -21,7 +21,8 @@ def _lib():
     tb.load_library()
 
 
-def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=None, fused=True, agg=0):
+def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=None, fused=True, agg=0,
+                      layer_hook=None):
     """Drive `steps` decode steps per layer on the GPU and check every step against the oracle.
 
     The oracle starts from the GPU-projected prefix of Kp (identical inputs),
@@ -33,8 +34,11 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
     k = w.k if k is None else k
     cap = n0 + steps
     shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, cap)
+    dec = None
     for layer in layers:
         L = synth.make_layer(w, layer=layer, cap=cap, n=n0)
+        if layer_hook is not None:
+            layer_hook(L)
         K, V, Wk = L["K"].cuda(), L["V"].cuda(), L["Wk"].cuda()
         Kp = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
         tb.tb_project_append(shape, K, cap, Wk, Kp, 0, n0)
@@ -80,6 +84,22 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
             # and the end-to-end output where the predictions agree
             if np.array_equal(gidx, st.idx):
                 assert np.abs(got - ref_out).max() <= OUT_ATOL
+    return dec
+
+
+def general_select_steps(dec) -> list:
+    """Per (batch, KV head) row: decode steps whose single-exchange selection fell back to the general one.
+
+    The count sits in the row's control block at the start of the workspace
+    (fourth 32-bit word of each block)."""
+    rows = dec.shape.B * dec.shape.Hkv
+    ws = dec.ws.cpu().numpy()
+    stride = ROWCTL_BYTES
+    return [int(ws[r * stride + 12:r * stride + 16].view(np.uint32)[0]) for r in range(rows)]
+
+
+# bytes of one row control block: 4 words, 3 x 2048 histogram words, 2 x 512 chunk words, 4096 (key, token) pairs
+ROWCTL_BYTES = 4 * 4 + 3 * 2048 * 4 + 2 * 512 * 4 + 4096 * 8
 
 
 @pytest.mark.parametrize("fused", [True, False])
@@ -123,6 +143,31 @@ def test_decode_fused_equals_unfused_bitwise_selection():
     assert np.array_equal(res[0][1][..., :w.k], res[1][1][..., :w.k])
     assert np.array_equal(res[0][4], res[1][4])
     assert np.abs(res[0][3] - res[1][3]).max() <= 2e-3
+
+
+def test_decode_fast_step_takes_the_single_exchange_on_smooth_scores():
+    w = synth.WORKLOADS[1]
+    dec = run_decode_parity(w, n0=w.N - 1, steps=2)
+    assert sum(general_select_steps(dec)) == 0
+
+
+def test_decode_blocky_scores_fall_back_to_the_general_select():
+    # 10% of the 32-token blocks hold keys scaled by 8: the CTAs of a row own
+    # very different shares of them, so their local threshold estimates miss
+    # and the step must take the general distributed select, with the same
+    # exact result.
+    w = synth.WORKLOADS[1]
+
+    def hot_blocks(L):
+        g = torch.Generator().manual_seed(77)
+        nblk = L["K"].shape[2] // 32
+        hot = torch.randperm(nblk, generator=g)[: nblk // 10]
+        rows = (hot[:, None] * 32 + torch.arange(32)[None, :]).reshape(-1)
+        rows = rows[rows < L["K"].shape[2]]
+        L["K"][:, :, rows] = L["K"][:, :, rows] * 8
+
+    dec = run_decode_parity(w, n0=w.N - 1, steps=2, layer_hook=hot_blocks)
+    assert sum(general_select_steps(dec)) > 0
 
 
 def test_decode_small_interval_with_neighbours():
