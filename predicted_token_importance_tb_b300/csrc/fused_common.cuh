@@ -23,46 +23,83 @@ __host__ __device__ inline int comb_floats_for(int nthreads, int G, int D) {
     return f > nthreads ? f : nthreads;
 }
 
-// Append the step's K/V row of (b,h) = row at position n and project the key.
-// knew [D] and kpn [dp] (shared, fp32) receive the new key and its projected
-// (bf16-rounded) row; comb is shared scratch of at least blockDim.x floats.
-// All threads of the CTA must call it.
-__device__ __forceinline__ void step_append_project(const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk,
-                                                    uint16_t *K, uint16_t *V, uint16_t *Kp, int64_t cap, int64_t n,
-                                                    int row, int h, int D, int dp, float *knew, float *kpn,
-                                                    float *comb) {
-    const uint16_t *kn = K_new + (int64_t)row * D;
-    const uint16_t *vn = V_new + (int64_t)row * D;
-    uint16_t *Kr = K + ((int64_t)row * cap + n) * D;
-    uint16_t *Vr = V + ((int64_t)row * cap + n) * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        const uint16_t kb = kn[d];
-        knew[d] = bf16_to_f(kb);
-        Kr[d] = kb;
-        Vr[d] = vn[d];
-    }
-    __syncthreads();
-    // threads (j, slice) accumulate output j over a slice of D, summed in comb
+// The step's append, split in two so the loads can fly while other work runs:
+// append_issue loads this thread's slice of Wk and its element of K_new and
+// V_new into registers; append_finish writes the K/V row into the cache and
+// projects the key into its Kp row: thread (j, slice) accumulates output j
+// over a slice of D in fp32, the slices are summed in comb and the sum is
+// rounded once to bf16. knew [D] and kpn [dp] (shared fp32) receive the new
+// key and its projected row; comb is shared scratch of blockDim.x floats.
+constexpr int kAppendW = 8;   // Wk values a thread keeps in registers
+
+struct AppendRegs {
+    uint16_t wv[kAppendW];
+    uint16_t kb, vb;
+};
+
+__device__ __forceinline__ AppendRegs append_issue(const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk,
+                                                   int row, int h, int D, int dp) {
+    AppendRegs r;
     const uint16_t *W = Wk + (int64_t)h * D * dp;
     const int jn = dp < (int)blockDim.x ? dp : (int)blockDim.x;
     const int slices = blockDim.x / jn;
     const int dlen = (D + slices - 1) / slices;
     const int j = threadIdx.x % jn, sl = threadIdx.x / jn;
+    const int d0 = sl * dlen, d1 = min(D, d0 + dlen);
+#pragma unroll
+    for (int u = 0; u < kAppendW; ++u) r.wv[u] = (sl < slices && d0 + u < d1) ? W[(int64_t)(d0 + u) * dp + j] : (uint16_t)0;
+    r.kb = (int)threadIdx.x < D ? K_new[(int64_t)row * D + threadIdx.x] : (uint16_t)0;
+    r.vb = (int)threadIdx.x < D ? V_new[(int64_t)row * D + threadIdx.x] : (uint16_t)0;
+    return r;
+}
+
+// All threads of the CTA must call it.
+__device__ __forceinline__ void append_finish(const AppendRegs &r, const uint16_t *K_new, const uint16_t *V_new,
+                                              const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp,
+                                              int64_t cap, int64_t n, int row, int h, int D, int dp, float *knew,
+                                              float *kpn, float *comb) {
+    uint16_t *Kr = K + ((int64_t)row * cap + n) * D;
+    uint16_t *Vr = V + ((int64_t)row * cap + n) * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        const uint16_t k2 = d == (int)threadIdx.x ? r.kb : K_new[(int64_t)row * D + d];
+        const uint16_t v2 = d == (int)threadIdx.x ? r.vb : V_new[(int64_t)row * D + d];
+        knew[d] = bf16_to_f(k2);
+        Kr[d] = k2;
+        Vr[d] = v2;
+    }
+    __syncthreads();
+    const uint16_t *W = Wk + (int64_t)h * D * dp;
+    const int jn = dp < (int)blockDim.x ? dp : (int)blockDim.x;
+    const int slices = blockDim.x / jn;
+    const int dlen = (D + slices - 1) / slices;
+    const int j = threadIdx.x % jn, sl = threadIdx.x / jn;
+    const int d0 = sl * dlen, d1 = min(D, d0 + dlen);
     if (sl < slices) {
         float acc = 0.f;
-        const int d0 = sl * dlen, d1 = min(D, d0 + dlen);
-        for (int d = d0; d < d1; ++d) acc = fmaf(knew[d], bf16_to_f(W[(int64_t)d * dp + j]), acc);
+#pragma unroll
+        for (int u = 0; u < kAppendW; ++u)
+            if (d0 + u < d1) acc = fmaf(knew[d0 + u], bf16_to_f(r.wv[u]), acc);
+        for (int d = d0 + kAppendW; d < d1; ++d) acc = fmaf(knew[d], bf16_to_f(W[(int64_t)d * dp + j]), acc);
         comb[sl * jn + j] = acc;
     }
     __syncthreads();
     if (threadIdx.x < dp) {
         float s = 0.f;
         for (int x = 0; x < slices; ++x) s += comb[x * jn + threadIdx.x];
-        const uint16_t kb = f_to_bf16(s);
-        Kp[((int64_t)row * cap + n) * dp + threadIdx.x] = kb;
-        kpn[threadIdx.x] = bf16_to_f(kb);
+        const uint16_t pb = f_to_bf16(s);
+        Kp[((int64_t)row * cap + n) * dp + threadIdx.x] = pb;
+        kpn[threadIdx.x] = bf16_to_f(pb);
     }
     __syncthreads();
+}
+
+// Both halves back to back. All threads of the CTA must call it.
+__device__ __forceinline__ void step_append_project(const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk,
+                                                    uint16_t *K, uint16_t *V, uint16_t *Kp, int64_t cap, int64_t n,
+                                                    int row, int h, int D, int dp, float *knew, float *kpn,
+                                                    float *comb) {
+    const AppendRegs r = append_issue(K_new, V_new, Wk, row, h, D, dp);
+    append_finish(r, K_new, V_new, Wk, K, V, Kp, cap, n, row, h, D, dp, knew, kpn, comb);
 }
 
 // Exact selection over contiguous chunks plus attention over this CTA's kept
@@ -149,6 +186,67 @@ __device__ __forceinline__ void row_merge_tail(RowCtl *rc, const float *prow, in
         rc->bar = 0;
         rc->ncand = 0;
         rc->done = 0;
+    }
+}
+
+// Merge of a row's C partial states spread over its C CTAs: after every CTA
+// stored its partial at prow + c * G * (2 + D) and arrived on rc->done,
+// CTA c merges outputs [c*per, (c+1)*per) of the G*D, loading a batch of up
+// to 32 partials per output in one round trip. The last CTA to finish puts
+// the row's control words back to zero (and the radix histograms when
+// reset_hist). flag: one shared word. All threads of the CTA must call it.
+static __device__ __forceinline__ void row_merge_spread(RowCtl *rc, const float *prow, int c, int C, int G, int D,
+                                              uint16_t *out_rows, uint32_t *flag, int *abort_flag, bool reset_hist,
+                                              int32_t *dev_status) {
+    constexpr int kBatch = 32;
+    if (!group_wait(&rc->done, (uint32_t)C, abort_flag, dev_status)) return;
+    const int sg = 2 + D, total = G * D;
+    const int per = (total + C - 1) / C;
+    const int x_end = min(total, (c + 1) * per);
+    for (int x = c * per + threadIdx.x; x < x_end; x += blockDim.x) {
+        const int g = x / D, d = x % D;
+        float M = -INFINITY, L = 0.f, Acc = 0.f;
+        for (int sp0 = 0; sp0 < C; sp0 += kBatch) {
+            float mv[kBatch], lv[kBatch], av[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const bool in = sp0 + u < C;
+                const float *pp = prow + ((int64_t)(in ? sp0 + u : 0) * G + g) * sg;
+                mv[u] = in ? __ldcg(pp) : -INFINITY;
+                lv[u] = in ? __ldcg(pp + 1) : 0.f;
+                av[u] = in ? __ldcg(pp + 2 + d) : 0.f;
+            }
+            float Mb = M;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) Mb = fmaxf(Mb, mv[u]);
+            const float rsc = rescale_w(M, Mb);
+            L *= rsc;
+            Acc *= rsc;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const float w = rescale_w(mv[u], Mb);
+                L = fmaf(w, lv[u], L);
+                Acc = fmaf(w, av[u], Acc);
+            }
+            M = Mb;
+        }
+        if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
+        out_rows[(int64_t)g * D + d] = f_to_bf16(L > 0.f ? Acc / L : 0.f);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(&rc->ncand, 1u);
+        *flag = (prev == (uint32_t)(C - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    if (reset_hist)
+        for (int x = threadIdx.x; x < 3 * kRadixBins; x += blockDim.x) (&rc->hist[0][0])[x] = 0;
+    if (threadIdx.x == 0) {
+        rc->bar = 0;
+        rc->done = 0;
+        rc->ncand = 0;
     }
 }
 

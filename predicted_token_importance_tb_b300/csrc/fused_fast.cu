@@ -122,6 +122,14 @@ enum {
     CN_ABOVE = 0, CN_WIN, CN_CAND, CN_AE, CN_L, CN_H, CN_VALID, CN_ASUM, CN_RANGE, CN_BM, CN_FLAG
 };
 
+// 16 zero bytes to shared memory where cond holds (a predicated store, no branch).
+__device__ __forceinline__ void st_shared_zero16_if(void *p, bool cond) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q st.shared.v4.u32 [%0], {%2, %2, %2, %2};\n\t}" ::"r"(
+                     smem_addr(p)),
+                 "r"((uint32_t)cond), "r"(0u)
+                 : "memory");
+}
+
 // Warp-aggregated slot allocation on a shared counter: lanes with `want`
 // get consecutive slots. All lanes of the warp must call it.
 __device__ __forceinline__ uint32_t warp_alloc(uint32_t *ctr, bool want) {
@@ -139,7 +147,7 @@ __device__ __forceinline__ uint32_t warp_alloc(uint32_t *ctr, bool want) {
 // Bins of two targets (ranks from the top, 1-based; 0 = none) in a histogram
 // of nbins (a multiple of blockDim.x). out = {bin1, above1, bin2, above2},
 // kNone where a target is 0 or beyond the total. All threads call.
-__device__ __noinline__ void find_two_bins(const uint32_t *hist, int nbins, uint32_t need1, uint32_t need2,
+__device__ __forceinline__ void find_two_bins(const uint32_t *hist, int nbins, uint32_t need1, uint32_t need2,
                                            uint32_t *scan, uint32_t *out) {
     if (threadIdx.x == 0) out[0] = out[1] = out[2] = out[3] = kNone;
     const int per = nbins / blockDim.x;
@@ -169,7 +177,7 @@ __device__ __noinline__ void find_two_bins(const uint32_t *hist, int nbins, uint
 // One warp: bins of up to two targets among kFFFine fine bins with `base`
 // elements above them. out[t] = bin (kNone if not inside), out[2 + t] =
 // elements above that bin, out[4 + t] = elements in it.
-__device__ __noinline__ void warp_find_fine(const uint32_t *fine, uint32_t base, uint32_t need1, uint32_t need2,
+__device__ __forceinline__ void warp_find_fine(const uint32_t *fine, uint32_t base, uint32_t need1, uint32_t need2,
                                             uint32_t *out) {
     const int lane = threadIdx.x & 31;
     const int hi = kFFFine - 1 - lane * 4;
@@ -203,7 +211,7 @@ __device__ __noinline__ void warp_find_fine(const uint32_t *fine, uint32_t base,
 }
 
 // Exclusive prefix over n shared counters in place (all threads call).
-__device__ __noinline__ void block_scan_inplace(uint32_t *v, int n, uint32_t *scan) {
+__device__ __forceinline__ void block_scan_inplace(uint32_t *v, int n, uint32_t *scan) {
     const int per = (n + blockDim.x - 1) / blockDim.x;
     const int x0 = threadIdx.x * per;
     uint32_t loc = 0;
@@ -239,17 +247,28 @@ __device__ __forceinline__ void mma_attend(MmaAttn<DT / 8> &A, const uint8_t *X,
     for (int ch = warp; ch < nch; ch += kFFWarps) {
         const int s0 = ch * 16;
         // S = Q K^T for slots s0 .. s0+15 (two n-tiles of 8)
+        // kept flags of this lane's columns s0 + 8j + 2(lane%4) + {0,1}
+        // (the flags are zero past the gathered rows)
+        const uint32_t f0 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 2 * (lane & 3));
+        const uint32_t f1 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 8 + 2 * (lane & 3));
+        // S = Q K^T, two independent accumulator chains per n-tile (even / odd k-steps)
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int kt = s0 + 8 * (lane >> 4) + (lane & 7);        // K row this lane addresses
         const uint32_t krow = xs + (uint32_t)kt * SB + 16 * ((lane >> 3) & 1);
         const uint32_t qrow = qa + (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)) * QS + 16 * (lane >> 4);
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
+        for (int kk = 0; kk < KS; kk += 2) {
             uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            uint32_t e0, e1, e2, e3, g0, g1, g2, g3;
             ldsm_x4(qrow + kk * 32, a0, a1, a2, a3);
             ldsm_x4(krow + kk * 32, b0, b1, b2, b3);
+            ldsm_x4(qrow + kk * 32 + 32, e0, e1, e2, e3);
+            ldsm_x4(krow + kk * 32 + 32, g0, g1, g2, g3);
             mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
             mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
+            mma_bf16_16816(sd[0], e0, e1, e2, e3, g0, g1);
+            mma_bf16_16816(sd[1], e0, e1, e2, e3, g2, g3);
         }
         // online softmax (exp2 domain); columns of this lane: s0 + 8j + 2(lane%4) + {0,1}
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -257,10 +276,10 @@ __device__ __forceinline__ void mma_attend(MmaAttn<DT / 8> &A, const uint8_t *X,
         for (int j = 0; j < 2; ++j) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int s = s0 + 8 * j + 2 * (lane & 3) + u;
-                const bool on = s < n && kept[kept_off + s];
-                sc[j][u] = on ? sc[j][u] * qscale : -INFINITY;
-                sc[j][2 + u] = on ? sc[j][2 + u] * qscale : -INFINITY;
+                const bool on = (((j ? f1 : f0) >> (8 * u)) & 0xFFu) != 0u;
+                const float z0 = (sc[j][u] + sd[j][u]) * qscale, z1 = (sc[j][2 + u] + sd[j][2 + u]) * qscale;
+                sc[j][u] = on ? z0 : -INFINITY;
+                sc[j][2 + u] = on ? z1 : -INFINITY;
                 mx0 = fmaxf(mx0, sc[j][u]);
                 mx1 = fmaxf(mx1, sc[j][2 + u]);
             }
@@ -307,33 +326,42 @@ __device__ __forceinline__ void mma_attend(MmaAttn<DT / 8> &A, const uint8_t *X,
     }
 }
 
+// Arguments of the general path, passed by value (the kernel parameters stay
+// in the parameter space).
+struct FFGeneral {
+    RowCtl *rc;
+    uint32_t *kg;            // this row's keys in token order
+    int32_t *irow, *srow;    // this row's idx / sel
+    int32_t *dev_status;
+    const uint16_t *Kh, *Vh, *qrow;
+    float *prow;
+    int64_t cap, n_t;
+    int C, c, nb, G, D, k;
+    float scale;
+};
+
 // The general path (rare): keys to the workspace in token order, re-split
 // into contiguous chunks, general distributed select with CUDA-core
 // attention, this CTA's partial state to the workspace.
 template <int GM>
-__device__ __noinline__ bool ff_general_path(const FFArgs &a, SelectSmem &S, int32_t *list, float *comb, int row, int c,
-                                             int nb, int64_t n_t, const uint16_t *Kh, const uint16_t *Vh,
-                                             const uint16_t *qrow, float *prow) {
-    const int C = a.C, G = a.Hq / a.Hkv, D = a.D;
-    RowCtl *rc = a.ctl + row;
-    uint32_t *kg = a.keys_g + (int64_t)row * a.keys_stride;
-    for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
-        const int64_t t = ((int64_t)(c + (e >> 5) * C) << 5) + (e & 31);
-        if (t < n_t) kg[t] = S.keys[e];
+__device__ __noinline__ bool ff_general_path(const FFGeneral g, SelectSmem S, int32_t *list, float *comb) {
+    for (int e = threadIdx.x; e < g.nb * 32; e += blockDim.x) {
+        const int64_t t = ((int64_t)(g.c + (e >> 5) * g.C) << 5) + (e & 31);
+        if (t < g.n_t) g.kg[t] = S.keys[e];
     }
-    if (threadIdx.x == 0 && c == 0) atomicAdd(&rc->general_steps, 1u);
-    if (!group_barrier(&rc->bar, (uint32_t)(2 * C), S.abort_flag, a.dev_status)) return false;
-    const int Ls = (int)((((n_t + C - 1) / C) + 31) / 32 * 32);
-    const int64_t t0 = (int64_t)c * Ls;
-    const int Lcs = (int)(n_t - t0 < Ls ? (n_t - t0 > 0 ? n_t - t0 : 0) : Ls);
-    for (int e = threadIdx.x; e < Lcs; e += blockDim.x) S.keys[e] = __ldcg(kg + t0 + e);
+    if (threadIdx.x == 0 && g.c == 0) atomicAdd(&g.rc->general_steps, 1u);
+    if (!group_barrier(&g.rc->bar, (uint32_t)(2 * g.C), S.abort_flag, g.dev_status)) return false;
+    const int Ls = (int)((((g.n_t + g.C - 1) / g.C) + 31) / 32 * 32);
+    const int64_t t0 = (int64_t)g.c * Ls;
+    const int Lcs = (int)(g.n_t - t0 < Ls ? (g.n_t - t0 > 0 ? g.n_t - t0 : 0) : Ls);
+    for (int e = threadIdx.x; e < Lcs; e += blockDim.x) S.keys[e] = __ldcg(g.kg + t0 + e);
     __syncthreads();
     AttnLane<GM> A;
-    attn_init(A, qrow, G, D, (threadIdx.x & 31) % (D / 8), a.scale);
-    if (!chunk_select_attend(A, rc, S, list, Lcs, Ls, c, C, 2, (uint32_t)a.k, t0, Kh, Vh, a.cap, G, D,
-                             a.idx + (int64_t)row * a.k, a.sel + (int64_t)row * a.sel_stride, a.dev_status))
+    attn_init(A, g.qrow, g.G, g.D, (threadIdx.x & 31) % (g.D / 8), g.scale);
+    if (!chunk_select_attend(A, g.rc, S, list, Lcs, Ls, g.c, g.C, 2, (uint32_t)g.k, t0, g.Kh, g.Vh, g.cap, g.G, g.D,
+                             g.irow, g.srow, g.dev_status))
         return false;
-    attn_block_combine(A, G, D, comb, prow + (int64_t)c * G * (2 + D));
+    attn_block_combine(A, g.G, g.D, comb, g.prow + (int64_t)g.c * g.G * (2 + g.D));
     return true;
 }
 
@@ -402,7 +430,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             bulk_g2s(X + (size_t)j * 32 * DP * 2, Kpr + blk * 32 * DP, (uint32_t)(rows * DP * 2), bar);
         }
     }
-    // ---- 1a. while the copies fly: importance query, attention query tile, append
+    // ---- 1a. while the copies fly: the append's loads, importance query, attention query tile
+    AppendRegs ar;
+    if (owner) ar = append_issue(a.K_new, a.V_new, a.Wk, row, h, DT, DP);
     const uint16_t *qi = a.q_imp + ((int64_t)b * a.Hq + (int64_t)h * G) * DP;
     if (a.agg == TB_AGG_MEAN) {
         const float inv = 1.0f / (float)G;
@@ -441,9 +471,6 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     }
     const uint16_t *Kh = a.K + (int64_t)row * a.cap * DT;
     const uint16_t *Vh = a.V + (int64_t)row * a.cap * DT;
-    if (owner)
-        step_append_project(a.K_new, a.V_new, a.Wk, a.K, a.V, a.Kp, a.cap, a.n, row, h, DT, DP, knew, kpn,
-                            reinterpret_cast<float *>(S.ckey));
     __syncthreads();
     if (!mbarrier_wait_bounded(bar, 0, kWaitLimitNs)) {
         set_status(a.dev_status, TB_ERR_TIMEOUT);
@@ -527,6 +554,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         }
     }
     __syncthreads();
+    if (owner)
+        append_finish(ar, a.K_new, a.V_new, a.Wk, a.K, a.V, a.Kp, a.cap, a.n, row, h, DT, DP, knew, kpn,
+                      reinterpret_cast<float *>(S.ckey));
     if (owner && threadIdx.x == 0) {
         // the appended token scores from its freshly projected row (its Kp
         // row in shared memory may predate the append)
@@ -624,13 +654,15 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     auto att_tok = [&](int i) -> int64_t { return i < n_above ? stok[i] : stok[LIST - 1 - (i - n_above)]; };
     auto att_key = [&](int i) -> uint32_t { return i < n_above ? skey[i] : skey[LIST - 1 - (i - n_above)]; };
     constexpr int CPR = DT / 8;   // 16-byte chunks per row
+    // a group of 2*CPR lanes copies one row's K and V (one 16-byte chunk each)
+    constexpr int RPW = 32 / (2 * CPR);   // rows per warp per pass
+    const int rl = lane % (2 * CPR);
+    const bool rl_v = rl >= CPR;
+    const int rl_c = rl_v ? rl - CPR : rl;
     auto gather_round = [&](int r0, int nr) {
-        for (int x = threadIdx.x; x < nr * 2 * CPR; x += blockDim.x) {
-            const int s = x / (2 * CPR), ci = x % (2 * CPR);
-            const bool isv = ci >= CPR;
-            const int cc = isv ? ci - CPR : ci;
+        for (int s = warp * RPW + lane / (2 * CPR); s < nr; s += kFFWarps * RPW) {
             const int64_t t = att_tok(r0 + s);
-            cp_async16(X + (size_t)s * SB + (isv ? 2 * DT : 0) + cc * 16, (isv ? Vh : Kh) + t * DT + cc * 8);
+            cp_async16(X + (size_t)s * SB + (rl_v ? 2 * DT : 0) + rl_c * 16, (rl_v ? Vh : Kh) + t * DT + rl_c * 8);
         }
         cp_async_commit();
     };
@@ -733,30 +765,12 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     float *prow = a.part + (int64_t)row * C * G * (2 + DT);
     bool reset_hist = false;
     if (fast) {
-        // ---- 5c. per-block kept counts of the row -> ascending idx / sel slots
+        // ---- 5c. kept flags of the gathered rows; per-block kept counts of the row
 #pragma unroll
         for (int i = 0; i < kFFEntPerThread; ++i)
             if (((is_cand >> i) & 1u) && composite(ent[i].x, ent[i].y) >= T) atomicAdd(&bcnt[ent[i].y >> 5], 1u);
-        for (int i = threadIdx.x; i < n_att; i += blockDim.x)
-            kept[i] = composite(att_key(i), (uint32_t)att_tok(i)) >= T ? 1 : 0;
-        __syncthreads();
-        block_scan_inplace(bcnt, nblk, S.scan);
-        int32_t *irow = a.idx + (int64_t)row * a.k;
-        int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
-        for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
-            const int64_t t = tok_of(e);
-            const bool kp = e < Lv && composite(S.keys[e], (uint32_t)t) >= T;
-            const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
-            if (kp) {
-                const uint32_t slot = bcnt[t >> 5] + (uint32_t)__popc(km & ((1u << lane) - 1u));
-                if (slot < (uint32_t)a.k) {
-                    irow[slot] = (int32_t)t;
-                    srow[slot] = (int32_t)t;
-                } else {
-                    set_status(a.dev_status, TB_ERR_INVALID_ARG);
-                }
-            }
-        }
+        for (int i = threadIdx.x; i < LIST; i += blockDim.x)
+            kept[i] = (i < n_att && composite(att_key(i), (uint32_t)att_tok(i)) >= T) ? 1 : 0;
         // ---- 6. attention over the gathered rows, round by round
         MmaAttn<NT> A;
         A.m0 = A.m1 = -INFINITY;
@@ -774,11 +788,8 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             __syncthreads();
             // rows that take no part (not kept, or padding to 16) hold zeros in V
             const int npad = (nr + 15) & ~15;
-            for (int x = threadIdx.x; x < npad * CPR; x += blockDim.x) {
-                const int s = x / CPR, cc = x % CPR;
-                if (s >= nr || !kept[r0 + s])
-                    *reinterpret_cast<uint4 *>(X + (size_t)s * SB + 2 * DT + cc * 16) = make_uint4(0, 0, 0, 0);
-            }
+            for (int s = warp * RPW + lane / (2 * CPR); s < npad; s += kFFWarps * RPW)
+                st_shared_zero16_if(X + (size_t)s * SB + 2 * DT + rl_c * 16, rl_v && !kept[r0 + s]);
             __syncthreads();
             mma_attend<DT>(A, X, SB, nr, kept, r0, qsm, qscale);
         }
@@ -802,10 +813,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                         w[1] = half ? A.l1 : A.l0;
                     }
 #pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        w[2 + 8 * t + d0] = A.o[t][2 * half];
-                        w[2 + 8 * t + d0 + 1] = A.o[t][2 * half + 1];
-                    }
+                    for (int t = 0; t < NT; ++t)
+                        *reinterpret_cast<float2 *>(w + 2 + 8 * t + d0) =
+                            make_float2(A.o[t][2 * half], A.o[t][2 * half + 1]);
                 }
             }
         }
@@ -813,13 +823,15 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         for (int x = threadIdx.x; x < G * DT; x += blockDim.x) {
             const int g = x / DT, d = x % DT;
             float M = -INFINITY;
+#pragma unroll
             for (int w = 0; w < kFFWarps; ++w) M = fmaxf(M, ws[((int64_t)w * G + g) * sg]);
             float L = 0.f, Acc = 0.f;
+#pragma unroll
             for (int w = 0; w < kFFWarps; ++w) {
                 const float *sw = ws + ((int64_t)w * G + g) * sg;
                 const float wt = rescale_w(sw[0], M);
-                L += wt * sw[1];
-                Acc += wt * sw[2 + d];
+                L = fmaf(wt, sw[1], L);
+                Acc = fmaf(wt, sw[2 + d], Acc);
             }
             float *o = prow + ((int64_t)c * G + g) * sg;
             if (d == 0) {
@@ -828,17 +840,53 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             }
             o[2 + d] = Acc;
         }
+        group_arrive(&rc->done);
+        // ---- 6c. idx / sel in the shadow of the merge barrier: slots from
+        // the row's per-block kept counts
+        block_scan_inplace(bcnt, nblk, S.scan);
+        int32_t *irow = a.idx + (int64_t)row * a.k;
+        int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
+        for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+            const int64_t t = tok_of(e);
+            const bool kp = e < Lv && composite(S.keys[e], (uint32_t)t) >= T;
+            const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
+            const uint32_t slot = bcnt[t >> 5] + (uint32_t)__popc(km & ((1u << lane) - 1u));
+            if (kp && slot < (uint32_t)a.k) {
+                irow[slot] = (int32_t)t;
+                srow[slot] = (int32_t)t;
+            }
+            if (kp && slot >= (uint32_t)a.k) set_status(a.dev_status, TB_ERR_INVALID_ARG);
+        }
     } else {
         cp_async_wait_all();
-        if (!ff_general_path<GM>(a, S, stok, reinterpret_cast<float *>(X), row, c, nb, n_t, Kh, Vh, qrow, prow))
-            return;
+        FFGeneral gp;
+        gp.rc = rc;
+        gp.kg = a.keys_g + (int64_t)row * a.keys_stride;
+        gp.irow = a.idx + (int64_t)row * a.k;
+        gp.srow = a.sel + (int64_t)row * a.sel_stride;
+        gp.dev_status = a.dev_status;
+        gp.Kh = Kh;
+        gp.Vh = Vh;
+        gp.qrow = qrow;
+        gp.prow = prow;
+        gp.cap = a.cap;
+        gp.n_t = n_t;
+        gp.C = C;
+        gp.c = c;
+        gp.nb = nb;
+        gp.G = G;
+        gp.D = DT;
+        gp.k = a.k;
+        gp.scale = a.scale;
+        if (!ff_general_path<GM>(gp, S, stok, reinterpret_cast<float *>(X))) return;
         reset_hist = true;
+        group_arrive(&rc->done);
     }
     if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
 
-    // ---- 7. the row's last CTA merges the partial states
-    row_merge_tail(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT,
-                   reinterpret_cast<float *>(S.ckey), &cnt[CN_FLAG], reset_hist, a.dev_status);
+    // ---- 7. every CTA merges its share of the row's partial states
+    row_merge_spread(rc, prow, c, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT, &cnt[CN_FLAG],
+                     S.abort_flag, reset_hist, a.dev_status);
 }
 
 // ------------------------------------------------------------------ host side
