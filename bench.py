@@ -60,6 +60,22 @@ def _workload(name):
     raise SystemExit(f"unknown workload {name}")
 
 
+def _traffic(workload: str):
+    """DRAM bytes per launch of the step kernel from the committed ncu capture,
+    or None when the capture was taken on another workload or another build
+    of the library (the record carries the library's source hash)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "fused_fast_traffic.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, "predicted_token_importance_tb_b300", "libtb.so.buildhash")) as f:
+            build = f.read().strip()
+    except (OSError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("library_build_hash") != build:
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -348,7 +364,7 @@ def run_ours(args, w):
             "hbm_gbs": achieved * world,
             "bytes_per_step": step_bytes_real,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None,
+                         "frac": achieved / hbm_peak, "traffic": _traffic(w.name),
                          "kernel": "tb decode step, %s kernel(s) per step" % kernels_per_step,
                          "peak_source": peak_kind},
             "cpu_baseline": cpu,

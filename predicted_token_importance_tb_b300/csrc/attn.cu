@@ -69,6 +69,8 @@ cudaError_t launch_attn(const tb_shape &sh, const uint16_t *q, const uint16_t *K
     const int rows = sh.B * sh.Hkv;
     const int G = sh.Hq / sh.Hkv;
     if (rows <= 0) return cudaSuccess;
+    if (attn_mma_supported(sh))
+        return launch_attn_mma(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials, dev_status, st);
     const int64_t nsplit = attn_splits(sel_stride);
     const int split_tok = (int)attn_split_tokens(sel_stride);
     dim3 grid((unsigned)nsplit, (unsigned)rows);

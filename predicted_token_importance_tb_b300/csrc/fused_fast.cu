@@ -38,6 +38,7 @@
 #include <string.h>
 
 #include "async_copy.cuh"
+#include "attn_mma.cuh"
 #include "fused_common.cuh"
 #include "kernels.cuh"
 
@@ -49,6 +50,7 @@ constexpr int kFFEntMax = kFastEntMax;
 constexpr int kFFEntPerThread = 8;  // entries of one record a thread reads
 constexpr int kFFStageMax = 512;    // K/V rows gathered into shared memory per round
 constexpr int kFFFine = 128;        // fine bins: 4 coarse bins x 32
+constexpr int kFFKpGroups = 4;      // Kp blocks arrive in groups, each on its own barrier
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 
 struct FFHdr {
@@ -56,6 +58,7 @@ struct FFHdr {
 };
 constexpr int kFFRecBytes = kFastRecBytes;
 static_assert(sizeof(FFHdr) == 32, "record header is 32 bytes");
+static_assert(kFFKpGroups == 4, "cp_async_wait_pending covers four groups");
 
 struct FFArgs {
     const uint16_t *q, *q_imp, *K_new, *V_new, *Wk;
@@ -81,7 +84,7 @@ struct FFLayout {
 };
 
 __host__ __device__ inline int ff_a16(int x) { return (x + 15) & ~15; }
-__host__ __device__ inline int ff_slot_bytes(int D) { return 4 * D + 16; }   // K row, V row, 16-byte skew
+__host__ __device__ inline int ff_slot_bytes(int D) { return mma_slot_bytes(D); }
 
 __host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int G, int D, int dp) {
     FFLayout L;
@@ -112,7 +115,7 @@ __host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int 
     L.qs = x; x += ff_a16(G * dp * 4);
     L.kpn = x; x += ff_a16(dp * 4);
     L.knew = x; x += ff_a16(D * 4);
-    L.bar = x; x += 16;
+    L.bar = x; x += 8 * kFFKpGroups;
     L.total = x;
     return L;
 }
@@ -122,12 +125,14 @@ enum {
     CN_ABOVE = 0, CN_WIN, CN_CAND, CN_AE, CN_L, CN_H, CN_VALID, CN_ASUM, CN_RANGE, CN_BM, CN_FLAG
 };
 
-// 16 zero bytes to shared memory where cond holds (a predicated store, no branch).
-__device__ __forceinline__ void st_shared_zero16_if(void *p, bool cond) {
-    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q st.shared.v4.u32 [%0], {%2, %2, %2, %2};\n\t}" ::"r"(
-                     smem_addr(p)),
-                 "r"((uint32_t)cond), "r"(0u)
-                 : "memory");
+// Wait until at most n (0..3) of this thread's cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    }
 }
 
 // Warp-aggregated slot allocation on a shared counter: lanes with `want`
@@ -226,102 +231,62 @@ __device__ __forceinline__ void block_scan_inplace(uint32_t *v, int n, uint32_t 
     __syncthreads();
 }
 
-// Per-warp attention state on the tensor cores: rows g = lane/4 and g + 8 of
-// the 16-row tiles (query heads; rows >= G are zero padding), O over NT
-// n-tiles of 8 dims.
-template <int NT>
-struct MmaAttn {
-    float m0, m1, l0, l1;
-    float o[NT][4];
+// The owner CTA's append, one warp per pair of projected outputs (16 warps x
+// 2 = 32 outputs at most): lane l holds dims l, l + 32, ... of K_new and the
+// matching Wk entries of its warp's outputs; the fp32 dot products are summed
+// across the warp and rounded once to bf16. The loads are issued first
+// (append_warp_issue), the arithmetic and the stores later.
+template <int DT, int DP>
+struct WarpAppend {
+    static constexpr int DPL = DT / 32;            // dims per lane
+    static constexpr int OPW = (DP + 15) / 16;     // outputs per warp
+    uint16_t kv[DPL];                              // raw bf16: converted when used, so that the
+    uint16_t w[OPW][DPL];                          // loads do not stall the thread that issued them
+    uint16_t kb, vb;                               // this thread's element of K_new / V_new (t < D)
 };
 
-// Attend slots [0, n) of the gathered rows (K row at X + s*SB, V row at
-// +2D) for the slots whose kept flag is set; chunks of 16 slots per warp.
-template <int DT>
-__device__ __forceinline__ void mma_attend(MmaAttn<DT / 8> &A, const uint8_t *X, int SB, int n, const uint8_t *kept,
-                                           int kept_off, const uint8_t *qsm, float qscale) {
-    constexpr int NT = DT / 8, KS = DT / 16, QS = 2 * DT + 16;
+template <int DT, int DP>
+__device__ __forceinline__ void append_warp_issue(WarpAppend<DT, DP> &r, const uint16_t *K_new, const uint16_t *V_new,
+                                                  const uint16_t *Wk, int row, int h) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t xs = smem_addr(X), qa = smem_addr(qsm);
-    const int nch = (n + 15) >> 4;
-    for (int ch = warp; ch < nch; ch += kFFWarps) {
-        const int s0 = ch * 16;
-        // S = Q K^T for slots s0 .. s0+15 (two n-tiles of 8)
-        // kept flags of this lane's columns s0 + 8j + 2(lane%4) + {0,1}
-        // (the flags are zero past the gathered rows)
-        const uint32_t f0 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 2 * (lane & 3));
-        const uint32_t f1 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 8 + 2 * (lane & 3));
-        // S = Q K^T, two independent accumulator chains per n-tile (even / odd k-steps)
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int kt = s0 + 8 * (lane >> 4) + (lane & 7);        // K row this lane addresses
-        const uint32_t krow = xs + (uint32_t)kt * SB + 16 * ((lane >> 3) & 1);
-        const uint32_t qrow = qa + (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)) * QS + 16 * (lane >> 4);
+    const uint16_t *kn = K_new + (int64_t)row * DT;
+    const uint16_t *W = Wk + (int64_t)h * DT * DP;
 #pragma unroll
-        for (int kk = 0; kk < KS; kk += 2) {
-            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-            uint32_t e0, e1, e2, e3, g0, g1, g2, g3;
-            ldsm_x4(qrow + kk * 32, a0, a1, a2, a3);
-            ldsm_x4(krow + kk * 32, b0, b1, b2, b3);
-            ldsm_x4(qrow + kk * 32 + 32, e0, e1, e2, e3);
-            ldsm_x4(krow + kk * 32 + 32, g0, g1, g2, g3);
-            mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
-            mma_bf16_16816(sd[0], e0, e1, e2, e3, g0, g1);
-            mma_bf16_16816(sd[1], e0, e1, e2, e3, g2, g3);
+    for (int i = 0; i < WarpAppend<DT, DP>::DPL; ++i) {
+        const int d = lane + 32 * i;
+        r.kv[i] = kn[d];
+#pragma unroll
+        for (int o = 0; o < WarpAppend<DT, DP>::OPW; ++o) {
+            const int j = warp * WarpAppend<DT, DP>::OPW + o;
+            r.w[o][i] = j < DP ? W[(int64_t)d * DP + j] : (uint16_t)0;
         }
-        // online softmax (exp2 domain); columns of this lane: s0 + 8j + 2(lane%4) + {0,1}
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+    }
+    r.kb = (int)threadIdx.x < DT ? kn[threadIdx.x] : (uint16_t)0;
+    r.vb = (int)threadIdx.x < DT ? V_new[(int64_t)row * DT + threadIdx.x] : (uint16_t)0;
+}
+
+// Writes the K/V row and the Kp row; kpn [DP] (shared fp32) receives the
+// projected row. The caller synchronises before reading kpn.
+template <int DT, int DP>
+__device__ __forceinline__ void append_warp_finish(const WarpAppend<DT, DP> &r, uint16_t *K, uint16_t *V, uint16_t *Kp,
+                                                   int64_t cap, int64_t n, int row, float *kpn) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if ((int)threadIdx.x < DT) {
+        K[((int64_t)row * cap + n) * DT + threadIdx.x] = r.kb;
+        V[((int64_t)row * cap + n) * DT + threadIdx.x] = r.vb;
+    }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+    for (int o = 0; o < WarpAppend<DT, DP>::OPW; ++o) {
+        float acc = 0.f;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const bool on = (((j ? f1 : f0) >> (8 * u)) & 0xFFu) != 0u;
-                const float z0 = (sc[j][u] + sd[j][u]) * qscale, z1 = (sc[j][2 + u] + sd[j][2 + u]) * qscale;
-                sc[j][u] = on ? z0 : -INFINITY;
-                sc[j][2 + u] = on ? z1 : -INFINITY;
-                mx0 = fmaxf(mx0, sc[j][u]);
-                mx1 = fmaxf(mx1, sc[j][2 + u]);
-            }
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-        const float n0 = fmaxf(A.m0, mx0), n1 = fmaxf(A.m1, mx1);
-        const float c0 = n0 == -INFINITY ? 1.f : exp2f(A.m0 - n0);
-        const float c1 = n1 == -INFINITY ? 1.f : exp2f(A.m1 - n1);
-        float p[2][4];
+        for (int i = 0; i < WarpAppend<DT, DP>::DPL; ++i) acc = fmaf(bf16_to_f(r.kv[i]), bf16_to_f(r.w[o][i]), acc);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                p[j][u] = n0 == -INFINITY ? 0.f : exp2f(sc[j][u] - n0);
-                p[j][2 + u] = n1 == -INFINITY ? 0.f : exp2f(sc[j][2 + u] - n1);
-            }
-        }
-        A.l0 = A.l0 * c0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        A.l1 = A.l1 * c1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-        A.m0 = n0;
-        A.m1 = n1;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            A.o[t][0] *= c0;
-            A.o[t][1] *= c0;
-            A.o[t][2] *= c1;
-            A.o[t][3] *= c1;
-        }
-        // O += P V: A operand from p (row, 16 slots), B from V rows (transposed loads)
-        const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
-        const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
-        const int vt = s0 + 8 * ((lane >> 3) & 1) + (lane & 7);   // V row this lane addresses
-        const uint32_t vrow = xs + (uint32_t)vt * SB + 2 * DT + 16 * (lane >> 4);
-#pragma unroll
-        for (int jp = 0; jp < NT / 2; ++jp) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(vrow + jp * 32, b0, b1, b2, b3);
-            mma_bf16_16816(A.o[2 * jp], pa0, pa1, pa2, pa3, b0, b1);
-            mma_bf16_16816(A.o[2 * jp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, x);
+        const int j = warp * WarpAppend<DT, DP>::OPW + o;
+        if (lane == 0 && j < DP) {
+            const uint16_t pb = f_to_bf16(acc);
+            Kp[((int64_t)row * cap + n) * DP + j] = pb;
+            kpn[j] = bf16_to_f(pb);
         }
     }
 }
@@ -400,59 +365,24 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     uint8_t *kept = smb + Y.kept;
     float *qs = reinterpret_cast<float *>(smb + Y.qs);
     float *kpn = reinterpret_cast<float *>(smb + Y.kpn);
-    float *knew = reinterpret_cast<float *>(smb + Y.knew);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smb + Y.bar);
     const int LIST = NB * 32;   // capacity of stok / skey / kept
 
     auto tok_of = [&](int e) -> int64_t { return ((int64_t)(c + (e >> 5) * C) << 5) + (e & 31); };
 
     // ---- 0. counters and the copy barrier
     if (threadIdx.x < 32) cnt[threadIdx.x] = threadIdx.x == CN_H ? 0xFFFFu : threadIdx.x == CN_VALID ? 1u : 0u;
-    if (threadIdx.x == 0) {
-        *S.abort_flag = 0;
-        mbarrier_init(bar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    if (threadIdx.x == 0) *S.abort_flag = 0;
     __syncthreads();
 
-    // ---- 1. Kp blocks -> shared memory (bulk copies issued first by one warp)
+    // ---- 1. the step's small inputs first, so that their loads do not queue
+    // behind the Kp stream: importance rows (as MMA B fragments and as fp32
+    // rows), the attention query tile, and the owner's append operands
     const int blk_n = (int)(a.n >> 5);
     const bool owner = (blk_n % C) == c;
     int Lv = nb * 32;   // owned tokens (only the row's last block may be partial): local e < Lv
     if (nb > 0 && ((nblk - 1) % C) == c) Lv -= (int)((int64_t)nblk * 32 - n_t);
-    if (warp == 0) {
-        if (lane == 0) mbarrier_arrive_expect_tx(bar, (uint32_t)Lv * DP * 2);
-        __syncwarp();
-        const uint16_t *Kpr = a.Kp + (int64_t)row * a.cap * DP;
-        for (int j = lane; j < nb; j += 32) {
-            const int64_t blk = (int64_t)c + (int64_t)j * C;
-            const int64_t rows = n_t - blk * 32 < 32 ? n_t - blk * 32 : 32;
-            bulk_g2s(X + (size_t)j * 32 * DP * 2, Kpr + blk * 32 * DP, (uint32_t)(rows * DP * 2), bar);
-        }
-    }
-    // ---- 1a. while the copies fly: the append's loads, importance query, attention query tile
-    AppendRegs ar;
-    if (owner) ar = append_issue(a.K_new, a.V_new, a.Wk, row, h, DT, DP);
     const uint16_t *qi = a.q_imp + ((int64_t)b * a.Hq + (int64_t)h * G) * DP;
-    if (a.agg == TB_AGG_MEAN) {
-        const float inv = 1.0f / (float)G;
-        for (int i = threadIdx.x; i < DP; i += blockDim.x) {
-            float s = 0.f;
-            for (int g = 0; g < G; ++g) s += bf16_to_f(qi[g * DP + i]);
-            qs[i] = s * inv;
-        }
-    } else {
-        for (int i = threadIdx.x; i < G * DP; i += blockDim.x) qs[i] = bf16_to_f(qi[i]);
-    }
     const uint16_t *qrow = a.q + ((int64_t)b * a.Hq + (int64_t)h * G) * DT;
-    for (int x = threadIdx.x; x < 16 * (DT / 8); x += blockDim.x) {
-        const int g = x / (DT / 8), cc = x % (DT / 8);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (g < G) v = *reinterpret_cast<const uint4 *>(qrow + g * DT + cc * 8);
-        *reinterpret_cast<uint4 *>(qsm + g * (2 * DT + 16) + cc * 16) = v;
-    }
-    for (int x = threadIdx.x; x < kRadixBins; x += blockDim.x) S.hist[x] = 0;
-    for (int x = threadIdx.x; x < kFFFine; x += blockDim.x) fine[x] = 0;
     // importance rows as MMA B fragments: lane (g, q) holds head g (+8) at the
     // dims q*DP/4 .. (q+1)*DP/4 (the token rows use the same dim order)
     constexpr int KSP = DP / 16;         // k-steps of 16 dims
@@ -469,14 +399,40 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             for (int w = 0; w < WPL; ++w) qb[hg][w] = head < G ? src[w] : 0u;
         }
     }
+    const int qg = threadIdx.x / (DT / 8), qc = threadIdx.x % (DT / 8);   // Q tile chunk of this thread
+    uint4 qv = make_uint4(0, 0, 0, 0);
+    if (qg < G) qv = *reinterpret_cast<const uint4 *>(qrow + qg * DT + qc * 8);
+    const uint16_t qsr = (int)threadIdx.x < G * DP ? qi[threadIdx.x] : (uint16_t)0;   // converted after the Kp issue
+    WarpAppend<DT, DP> ar;
+    if (owner) append_warp_issue<DT, DP>(ar, a.K_new, a.V_new, a.Wk, row, h);
+
+    // ---- 1a. Kp blocks -> shared memory: 16-byte cp.async by every thread,
+    // consecutive threads on consecutive chunks; owned block j belongs to
+    // commit group j / gsz, so scoring can start on the first groups
+    const int gsz = (nb + kFFKpGroups - 1) / kFFKpGroups > 0 ? (nb + kFFKpGroups - 1) / kFFKpGroups : 1;
+    {
+        constexpr int CPB = 32 * DP * 2 / 16;   // 16-byte chunks per block
+        const uint16_t *Kpr = a.Kp + (int64_t)row * a.cap * DP;
+        for (int g = 0; g < kFFKpGroups; ++g) {
+            const int j0 = g * gsz, j1 = min(nb, j0 + gsz);
+            for (int x = threadIdx.x; x < (j1 - j0) * CPB; x += blockDim.x) {
+                const int j = j0 + x / CPB, ch = x % CPB;
+                const int64_t blk = (int64_t)c + (int64_t)j * C;
+                if (blk * 32 + (ch * 16) / (DP * 2) < n_t)
+                    cp_async16(X + (size_t)j * 32 * DP * 2 + ch * 16,
+                               reinterpret_cast<const uint8_t *>(Kpr + blk * 32 * DP) + ch * 16);
+            }
+            cp_async_commit();
+        }
+    }
+    // ---- 1b. the small inputs to shared memory; histograms cleared
+    if (qg < 16) *reinterpret_cast<uint4 *>(qsm + qg * (2 * DT + 16) + qc * 16) = qv;
+    if ((int)threadIdx.x < G * DP) qs[threadIdx.x] = bf16_to_f(qsr);
+    for (int x = threadIdx.x; x < kRadixBins; x += blockDim.x) S.hist[x] = 0;
+    for (int x = threadIdx.x; x < kFFFine; x += blockDim.x) fine[x] = 0;
     const uint16_t *Kh = a.K + (int64_t)row * a.cap * DT;
     const uint16_t *Vh = a.V + (int64_t)row * a.cap * DT;
     __syncthreads();
-    if (!mbarrier_wait_bounded(bar, 0, kWaitLimitNs)) {
-        set_status(a.dev_status, TB_ERR_TIMEOUT);
-        (void)mbarrier_wait_bounded(bar, 0, kWaitLimitNs);   // let copies in flight land before leaving
-        return;
-    }
 
     // ---- 2. scores on the tensor cores: tiles of 16 tokens (A) x 8 heads (B),
     // m16n8k16; per token the G dot products are averaged (or maxed), then the
@@ -486,8 +442,19 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         const int g = lane >> 2, q = lane & 3;
         const float invG = 1.0f / (float)G;
         const int ntile = (nb * 32) >> 4;
-        for (int tt = warp; tt < ntile; tt += kFFWarps) {
-            const uint8_t *tb = X + (size_t)tt * 16 * DP * 2 + q * (DP / 2);
+        int grp = -1;
+        for (int tt = 0; tt < ntile; tt += kFFWarps) {
+            // every thread waits for its own copies of the group, then the CTA
+            // barrier makes all threads' copies of it visible
+            const int gt = min((tt + kFFWarps - 1) >> 1, nb - 1) / gsz;   // last group any warp needs now
+            while (grp < gt) {
+                ++grp;
+                cp_async_wait_pending(kFFKpGroups - 1 - grp);
+                __syncthreads();
+            }
+            if (tt + warp >= ntile) continue;
+            const int tw = tt + warp;
+            const uint8_t *tb = X + (size_t)tw * 16 * DP * 2 + q * (DP / 2);
             uint32_t w0[WPL], w1[WPL];
             if (WPL == 4) {
                 const uint4 u0 = *reinterpret_cast<const uint4 *>(tb + g * DP * 2);
@@ -543,7 +510,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 v1 = fmaxf(v1, __shfl_xor_sync(0xFFFFFFFFu, v1, 2));
             }
             if (q < 2) {
-                const int e = tt * 16 + g + 8 * q;
+                const int e = tw * 16 + g + 8 * q;
                 uint32_t key = 0;
                 if (e < Lv) {
                     key = score_key(q ? v1 : v0, nan_seen);
@@ -553,20 +520,22 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             }
         }
     }
+    cp_async_wait_all();   // (the groups are complete; nothing may reuse X while a copy could land)
     __syncthreads();
-    if (owner)
-        append_finish(ar, a.K_new, a.V_new, a.Wk, a.K, a.V, a.Kp, a.cap, a.n, row, h, DT, DP, knew, kpn,
-                      reinterpret_cast<float *>(S.ckey));
+    if (owner) {
+        append_warp_finish<DT, DP>(ar, a.K, a.V, a.Kp, a.cap, a.n, row, kpn);
+        __syncthreads();
+    }
     if (owner && threadIdx.x == 0) {
         // the appended token scores from its freshly projected row (its Kp
         // row in shared memory may predate the append)
-        float s = -INFINITY;
-        const int ng = a.agg == TB_AGG_MEAN ? 1 : G;
-        for (int g = 0; g < ng; ++g) {
+        float s = a.agg == TB_AGG_MEAN ? 0.f : -INFINITY;
+        for (int g = 0; g < G; ++g) {
             float p = 0.f;
             for (int i = 0; i < DP; ++i) p = fmaf(qs[g * DP + i], kpn[i], p);
-            s = fmaxf(s, p);
+            s = a.agg == TB_AGG_MEAN ? s + p : fmaxf(s, p);
         }
+        if (a.agg == TB_AGG_MEAN) s *= 1.0f / (float)G;
         const int en = (blk_n / C) * 32 + (int)(a.n & 31);
         atomicSub(&S.hist[S.keys[en] >> 21], 1u);
         const uint32_t key = score_key(s, nan_seen);
@@ -791,7 +760,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             for (int s = warp * RPW + lane / (2 * CPR); s < npad; s += kFFWarps * RPW)
                 st_shared_zero16_if(X + (size_t)s * SB + 2 * DT + rl_c * 16, rl_v && !kept[r0 + s]);
             __syncthreads();
-            mma_attend<DT>(A, X, SB, nr, kept, r0, qsm, qscale);
+            mma_attend<DT, kFFWarps>(A, X, SB, nr, kept, r0, qsm, qscale);
         }
         // ---- 6b. combine the warps' states into this CTA's partial
         A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 1);

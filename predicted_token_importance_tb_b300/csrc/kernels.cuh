@@ -12,9 +12,11 @@ namespace tb {
 cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16_t *Kp, int64_t n, int agg,
                          float *s, int64_t lds, cudaStream_t st);
 
-// rows x n scores (row stride lds) -> rows x k ascending indices.
+// rows x n scores (row stride lds) -> rows x k ascending indices; when sel
+// is given the indices also go to sel (row stride sel_stride) and k to counts.
 cudaError_t launch_topk(int rows, const float *s, int64_t lds, int64_t n, int32_t k, int32_t *idx, RowCtl *ctl,
-                        int32_t *dev_status, cudaStream_t st);
+                        int32_t *dev_status, cudaStream_t st, int32_t *sel = nullptr, int32_t sel_stride = 0,
+                        int32_t *counts = nullptr);
 
 cudaError_t launch_expand(int rows, const int32_t *idx, int32_t k, int32_t r, int64_t n_pred, int64_t n_t,
                           int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status, cudaStream_t st);
@@ -22,6 +24,12 @@ cudaError_t launch_expand(int rows, const int32_t *idx, int32_t k, int32_t r, in
 cudaError_t launch_attn(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
                         const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale, uint16_t *out,
                         uint32_t *attn_ctl, float *partials, int32_t *dev_status, cudaStream_t st);
+
+// The same on the tensor cores (D = 64 or 128, G <= 16).
+bool attn_mma_supported(const tb_shape &sh);
+cudaError_t launch_attn_mma(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                            const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale, uint16_t *out,
+                            uint32_t *attn_ctl, float *partials, int32_t *dev_status, cudaStream_t st);
 
 // One new row per (b, h): cache writes, its projection and (optionally) the
 // tail entry of the selection.

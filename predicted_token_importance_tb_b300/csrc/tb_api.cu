@@ -229,10 +229,16 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
         // 2. score the n+1 tokens, select, widen
         e = launch_score(*shape, q_imp, Kp, n_t, p->agg, scores, n_t, stream);
         if (e != cudaSuccess) return from_cuda(e);
-        e = launch_topk(rows, scores, n_t, n_t, p->k, idx_state, ctl, dev_status, stream);
-        if (e != cudaSuccess) return from_cuda(e);
-        e = launch_expand(rows, idx_state, p->k, p->r, n_t, n_t, sel, sel_stride, counts, dev_status, stream);
-        if (e != cudaSuccess) return from_cuda(e);
+        if (p->r == 0 && p->T == 1) {
+            // no neighbours and no tail: the selection is the prediction itself
+            e = launch_topk(rows, scores, n_t, n_t, p->k, idx_state, ctl, dev_status, stream, sel, sel_stride, counts);
+            if (e != cudaSuccess) return from_cuda(e);
+        } else {
+            e = launch_topk(rows, scores, n_t, n_t, p->k, idx_state, ctl, dev_status, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            e = launch_expand(rows, idx_state, p->k, p->r, n_t, n_t, sel, sel_stride, counts, dev_status, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
         *n_pred = n_t;
     }
     // 3. attention over the selection

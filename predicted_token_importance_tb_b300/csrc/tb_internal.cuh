@@ -59,26 +59,28 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // arrives once per phase; a CTA waits until the counter reaches `target`
 // (phase count x group size). The wait is bounded: after kWaitLimitNs it
 // gives up, sets *abort_flag (shared) and records TB_ERR_TIMEOUT.
+// Arrival: the CTA's barrier orders its threads' writes before thread 0's
+// release add, which makes them visible at GPU scope before the count moves.
 __device__ __forceinline__ void group_arrive(uint32_t *ctr) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(ctr, 1u);
-    }
+    if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 
+// Wait: thread 0 polls with acquire loads, then the CTA barrier passes the
+// acquired view on to every thread of the CTA.
 __device__ __forceinline__ bool group_wait(uint32_t *ctr, uint32_t target, int *abort_flag, int32_t *dev_status) {
     if (threadIdx.x == 0) {
-        uint64_t t0 = global_ns();
-        while (ld_acquire(ctr) < target) {
-            if (global_ns() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                set_status(dev_status, TB_ERR_TIMEOUT);
-                break;
+        if (ld_acquire(ctr) < target) {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire(ctr) < target) {
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    set_status(dev_status, TB_ERR_TIMEOUT);
+                    break;
+                }
             }
-            __nanosleep(32);
         }
-        __threadfence();
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
     }
     __syncthreads();
     return *abort_flag == 0;

@@ -36,7 +36,8 @@ __device__ __forceinline__ SelectSmem carve_select_smem(uint8_t *base, int L) {
 
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float *__restrict__ s, int64_t lds, int64_t n, uint32_t k, int32_t *__restrict__ idx,
-            RowCtl *__restrict__ ctl, int row0, int C, int L, int32_t *dev_status) {
+            RowCtl *__restrict__ ctl, int row0, int C, int L, int32_t *dev_status, int32_t *sel, int32_t sel_stride,
+            int32_t *counts) {
     extern __shared__ __align__(16) uint8_t smem[];
     SelectSmem S = carve_select_smem(smem, L);
     const int row = row0 + blockIdx.x / C;
@@ -52,7 +53,8 @@ topk_kernel(const float *__restrict__ s, int64_t lds, int64_t n, uint32_t k, int
     RowCtl *rc = ctl + row;
     SelectResult R = group_select(rc, S, Lc, L, c, C, k, dev_status);
     if (!R.ok) return;
-    write_kept(R, S, Lc, (uint32_t)t0, idx + (int64_t)row * k);
+    write_kept(R, S, Lc, (uint32_t)t0, idx + (int64_t)row * k, sel ? sel + (int64_t)row * sel_stride : nullptr);
+    if (sel && c == 0 && threadIdx.x == 0) counts[row] = (int32_t)k;
     group_release(rc, C, S);
 }
 
@@ -102,7 +104,7 @@ static TopkPlan plan_topk(int rows, int64_t n) {
 }
 
 cudaError_t launch_topk(int rows, const float *s, int64_t lds, int64_t n, int32_t k, int32_t *idx, RowCtl *ctl,
-                        int32_t *dev_status, cudaStream_t st) {
+                        int32_t *dev_status, cudaStream_t st, int32_t *sel, int32_t sel_stride, int32_t *counts) {
     if (rows <= 0 || k <= 0 || n <= 0) return cudaSuccess;
     if (n > (int64_t)kTopkLMax * kMaxChunks) return cudaErrorInvalidValue;
     TopkPlan P = plan_topk(rows, n);
@@ -120,7 +122,7 @@ cudaError_t launch_topk(int rows, const float *s, int64_t lds, int64_t n, int32_
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, s, lds, n, (uint32_t)k, idx, ctl, r0, P.C, P.L,
-                                           dev_status);
+                                           dev_status, sel, sel_stride, counts);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -283,10 +283,11 @@ __device__ __forceinline__ bool is_kept(const SelectResult &R, uint32_t key, uin
     return key == R.tkey && tied_before < R.take;
 }
 
-// Write the kept tokens of this chunk, ascending, to out[R.offset ...]. The
-// chunk's keys are in S.keys; token of element e is tok0 + e.
+// Write the kept tokens of this chunk, ascending, to out[R.offset ...] (and
+// to out2 when given). The chunk's keys are in S.keys; token of element e is
+// tok0 + e.
 __device__ __forceinline__ void write_kept(const SelectResult &R, SelectSmem &S, int Lc, uint32_t tok0,
-                                          int32_t *out) {
+                                          int32_t *out, int32_t *out2 = nullptr) {
     uint32_t base_kept = 0, base_tied = 0;
     for (int t0 = 0; t0 < Lc; t0 += blockDim.x) {
         const int e = t0 + threadIdx.x;
@@ -301,7 +302,10 @@ __device__ __forceinline__ void write_kept(const SelectResult &R, SelectSmem &S,
         const uint32_t kept = (e < Lc && is_kept(R, key, tok0 + (uint32_t)e, tied_before)) ? 1u : 0u;
         uint32_t ktot;
         const uint32_t pos = block_exclusive_scan(kept, S.scan, ktot);
-        if (kept) out[R.offset + base_kept + pos] = (int32_t)(tok0 + (uint32_t)e);
+        if (kept) {
+            out[R.offset + base_kept + pos] = (int32_t)(tok0 + (uint32_t)e);
+            if (out2) out2[R.offset + base_kept + pos] = (int32_t)(tok0 + (uint32_t)e);
+        }
         base_kept += ktot;
         base_tied += ttot;
     }
