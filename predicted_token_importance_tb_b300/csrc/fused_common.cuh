@@ -189,21 +189,27 @@ __device__ __forceinline__ void row_merge_tail(RowCtl *rc, const float *prow, in
     }
 }
 
-// Merge of a row's C partial states spread over its C CTAs: after every CTA
-// stored its partial at prow + c * G * (2 + D) and arrived on rc->done,
-// CTA c merges outputs [c*per, (c+1)*per) of the G*D, loading a batch of up
-// to 32 partials per output in one round trip. The last CTA to finish puts
-// the row's control words back to zero (and the radix histograms when
-// reset_hist). flag: one shared word. All threads of the CTA must call it.
-static __device__ __forceinline__ void row_merge_spread(RowCtl *rc, const float *prow, int c, int C, int G, int D,
-                                              uint16_t *out_rows, uint32_t *flag, int *abort_flag, bool reset_hist,
-                                              int32_t *dev_status) {
+// The row's last CTA to arrive merges the C partial states (each CTA stored
+// its partial at prow + c * G * (2 + D) before arriving). A thread per output
+// issues the loads of all partials of a batch of up to 32 splits before using
+// any, so a batch costs one L2 round trip. Returns true in the CTA that
+// merged; that CTA also resets the row's control words (and the radix
+// histograms when reset_hist). flag: one shared word. All threads call it.
+__device__ __forceinline__ bool row_merge_last(RowCtl *rc, const float *prow, int C, int G, int D,
+                                               uint16_t *out_rows, uint32_t *flag, bool reset_hist,
+                                               int32_t *dev_status) {
     constexpr int kBatch = 32;
-    if (!group_wait(&rc->done, (uint32_t)C, abort_flag, dev_status)) return;
-    const int sg = 2 + D, total = G * D;
-    const int per = (total + C - 1) / C;
-    const int x_end = min(total, (c + 1) * per);
-    for (int x = c * per + threadIdx.x; x < x_end; x += blockDim.x) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&rc->done, 1u);
+        *flag = (prev == (uint32_t)(C - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!*flag) return false;
+    __threadfence();
+    const int sg = 2 + D;
+    for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
         const int g = x / D, d = x % D;
         float M = -INFINITY, L = 0.f, Acc = 0.f;
         for (int sp0 = 0; sp0 < C; sp0 += kBatch) {
@@ -233,21 +239,14 @@ static __device__ __forceinline__ void row_merge_spread(RowCtl *rc, const float 
         if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
         out_rows[(int64_t)g * D + d] = f_to_bf16(L > 0.f ? Acc / L : 0.f);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t prev = atomicAdd(&rc->ncand, 1u);
-        *flag = (prev == (uint32_t)(C - 1)) ? 1u : 0u;
-    }
-    __syncthreads();
-    if (!*flag) return;
-    __threadfence();
     if (reset_hist)
         for (int x = threadIdx.x; x < 3 * kRadixBins; x += blockDim.x) (&rc->hist[0][0])[x] = 0;
     if (threadIdx.x == 0) {
         rc->bar = 0;
-        rc->done = 0;
         rc->ncand = 0;
+        rc->done = 0;
     }
+    return true;
 }
 
 // Partial state of this CTA -> workspace, then row_merge_tail.

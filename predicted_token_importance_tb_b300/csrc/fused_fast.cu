@@ -732,7 +732,6 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     }
 
     float *prow = a.part + (int64_t)row * C * G * (2 + DT);
-    bool reset_hist = false;
     if (fast) {
         // ---- 5c. kept flags of the gathered rows; per-block kept counts of the row
 #pragma unroll
@@ -809,9 +808,11 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             }
             o[2 + d] = Acc;
         }
-        group_arrive(&rc->done);
-        // ---- 6c. idx / sel in the shadow of the merge barrier: slots from
-        // the row's per-block kept counts
+        // ---- 6c. the row's last CTA merges; the others write idx / sel meanwhile
+        const bool merged = row_merge_last(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT,
+                                           &cnt[CN_FLAG], false, a.dev_status);
+        (void)merged;
+        // idx / sel: slots from the row's per-block kept counts
         block_scan_inplace(bcnt, nblk, S.scan);
         int32_t *irow = a.idx + (int64_t)row * a.k;
         int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
@@ -826,6 +827,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             }
             if (kp && slot >= (uint32_t)a.k) set_status(a.dev_status, TB_ERR_INVALID_ARG);
         }
+        if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
     } else {
         cp_async_wait_all();
         FFGeneral gp;
@@ -848,14 +850,11 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         gp.k = a.k;
         gp.scale = a.scale;
         if (!ff_general_path<GM>(gp, S, stok, reinterpret_cast<float *>(X))) return;
-        reset_hist = true;
-        group_arrive(&rc->done);
+        if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
+        // ---- 7. the row's last CTA merges
+        (void)row_merge_last(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT, &cnt[CN_FLAG],
+                             true, a.dev_status);
     }
-    if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
-
-    // ---- 7. every CTA merges its share of the row's partial states
-    row_merge_spread(rc, prow, c, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT, &cnt[CN_FLAG],
-                     S.abort_flag, reset_hist, a.dev_status);
 }
 
 // ------------------------------------------------------------------ host side
