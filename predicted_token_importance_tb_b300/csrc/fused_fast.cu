@@ -79,8 +79,8 @@ struct FFArgs {
 
 // Shared-memory layout (byte offsets, each 16-byte aligned).
 struct FFLayout {
-    int X, qsm, keys, hist, fine, ckey, cidx, ccount, scan, misc, abort_, cnt, bcnt, stok, skey, kept, qs, kpn, knew,
-        bar, total;
+    int X, qsm, keys, hist, fine, ckey, cidx, ccount, scan, misc, abort_, cnt, bcnt, stok, skey, kept, kpn, knew, bar,
+        total;
 };
 
 __host__ __device__ inline int ff_a16(int x) { return (x + 15) & ~15; }
@@ -112,9 +112,8 @@ __host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int 
     L.stok = x; x += ff_a16(NB * 32 * 4);
     L.skey = x; x += ff_a16(NB * 32 * 4);
     L.kept = x; x += ff_a16(NB * 32);
-    L.qs = x; x += ff_a16(G * dp * 4);
-    L.kpn = x; x += ff_a16(dp * 4);
-    L.knew = x; x += ff_a16(D * 4);
+    L.kpn = x; x += ff_a16(dp * 2);
+    L.knew = x; x += ff_a16(D * 4);   // K_new and V_new rows (bf16)
     L.bar = x; x += 8 * kFFKpGroups;
     L.total = x;
     return L;
@@ -122,7 +121,7 @@ __host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int 
 
 // counters in the cnt region
 enum {
-    CN_ABOVE = 0, CN_WIN, CN_CAND, CN_AE, CN_L, CN_H, CN_VALID, CN_ASUM, CN_RANGE, CN_BM, CN_FLAG
+    CN_ABOVE = 0, CN_WIN, CN_CAND, CN_AE, CN_L, CN_H, CN_VALID, CN_ASUM, CN_RANGE, CN_BM, CN_FLAG, CN_WK
 };
 
 // Wait until at most n (0..3) of this thread's cp.async groups are pending.
@@ -231,63 +230,58 @@ __device__ __forceinline__ void block_scan_inplace(uint32_t *v, int n, uint32_t 
     __syncthreads();
 }
 
-// The owner CTA's append, one warp per pair of projected outputs (16 warps x
-// 2 = 32 outputs at most): lane l holds dims l, l + 32, ... of K_new and the
-// matching Wk entries of its warp's outputs; the fp32 dot products are summed
-// across the warp and rounded once to bf16. The loads are issued first
-// (append_warp_issue), the arithmetic and the stores later.
+// The owner CTA's append. Wk of head h ([DT][DP] bf16), K_new and V_new
+// rows come into shared memory by cp.async with the first Kp group, so that
+// the owner issues no register loads and no global stores while the Kp
+// stream is in flight. Projection: one warp per pair of outputs (16 warps x
+// 2 = 32 outputs at most), lane l takes dims l, l + 32, ...; the fp32 dot
+// products are summed across the warp and rounded once to bf16. The K / V /
+// Kp rows of token n go to global memory once the stream has landed.
 template <int DT, int DP>
-struct WarpAppend {
-    static constexpr int DPL = DT / 32;            // dims per lane
-    static constexpr int OPW = (DP + 15) / 16;     // outputs per warp
-    uint16_t kv[DPL];                              // raw bf16: converted when used, so that the
-    uint16_t w[OPW][DPL];                          // loads do not stall the thread that issued them
-    uint16_t kb, vb;                               // this thread's element of K_new / V_new (t < D)
-};
-
-template <int DT, int DP>
-__device__ __forceinline__ void append_warp_issue(WarpAppend<DT, DP> &r, const uint16_t *K_new, const uint16_t *V_new,
-                                                  const uint16_t *Wk, int row, int h) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint16_t *kn = K_new + (int64_t)row * DT;
-    const uint16_t *W = Wk + (int64_t)h * DT * DP;
-#pragma unroll
-    for (int i = 0; i < WarpAppend<DT, DP>::DPL; ++i) {
-        const int d = lane + 32 * i;
-        r.kv[i] = kn[d];
-#pragma unroll
-        for (int o = 0; o < WarpAppend<DT, DP>::OPW; ++o) {
-            const int j = warp * WarpAppend<DT, DP>::OPW + o;
-            r.w[o][i] = j < DP ? W[(int64_t)d * DP + j] : (uint16_t)0;
-        }
+__device__ __forceinline__ void append_issue(const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk, int row,
+                                             int h, uint8_t *wsm, uint8_t *kvn) {
+    const uint8_t *W = reinterpret_cast<const uint8_t *>(Wk + (int64_t)h * DT * DP);
+    for (int x = threadIdx.x; x < DT * DP * 2 / 16; x += blockDim.x) cp_async16(wsm + 16 * x, W + 16 * x);
+    constexpr int CR = DT * 2 / 16;   // 16-byte chunks of a K / V row
+    if ((int)threadIdx.x < 2 * CR) {
+        const int v = (int)threadIdx.x / CR, ch = (int)threadIdx.x % CR;
+        cp_async16(kvn + v * DT * 2 + 16 * ch,
+                   reinterpret_cast<const uint8_t *>((v ? V_new : K_new) + (int64_t)row * DT) + 16 * ch);
     }
-    r.kb = (int)threadIdx.x < DT ? kn[threadIdx.x] : (uint16_t)0;
-    r.vb = (int)threadIdx.x < DT ? V_new[(int64_t)row * DT + threadIdx.x] : (uint16_t)0;
 }
 
-// Writes the K/V row and the Kp row; kpn [DP] (shared fp32) receives the
-// projected row. The caller synchronises before reading kpn.
+// kpn [DP] (shared bf16) <- the projected row; wsm and kvn landed and visible.
+// The caller synchronises before reading kpn.
 template <int DT, int DP>
-__device__ __forceinline__ void append_warp_finish(const WarpAppend<DT, DP> &r, uint16_t *K, uint16_t *V, uint16_t *Kp,
-                                                   int64_t cap, int64_t n, int row, float *kpn) {
+__device__ __forceinline__ void append_project(const uint16_t *wsm, const uint16_t *kn, uint16_t *kpn) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if ((int)threadIdx.x < DT) {
-        K[((int64_t)row * cap + n) * DT + threadIdx.x] = r.kb;
-        V[((int64_t)row * cap + n) * DT + threadIdx.x] = r.vb;
-    }
+    constexpr int DPL = DT / 32, OPW = (DP + 15) / 16;
 #pragma unroll
-    for (int o = 0; o < WarpAppend<DT, DP>::OPW; ++o) {
+    for (int o = 0; o < OPW; ++o) {
+        const int j = warp * OPW + o;
+        if (j >= DP) break;   // (warp-uniform)
         float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < WarpAppend<DT, DP>::DPL; ++i) acc = fmaf(bf16_to_f(r.kv[i]), bf16_to_f(r.w[o][i]), acc);
+        for (int i = 0; i < DPL; ++i) acc = fmaf(bf16_to_f(kn[lane + 32 * i]), bf16_to_f(wsm[(lane + 32 * i) * DP + j]), acc);
 #pragma unroll
         for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, x);
-        const int j = warp * WarpAppend<DT, DP>::OPW + o;
-        if (lane == 0 && j < DP) {
-            const uint16_t pb = f_to_bf16(acc);
-            Kp[((int64_t)row * cap + n) * DP + j] = pb;
-            kpn[j] = bf16_to_f(pb);
-        }
+        if (lane == 0) kpn[j] = f_to_bf16(acc);
+    }
+}
+
+// K / V / Kp rows of token n from shared memory to the caches (16-byte stores).
+template <int DT, int DP>
+__device__ __forceinline__ void append_store(const uint8_t *kvn, const uint16_t *kpn, uint16_t *K, uint16_t *V,
+                                             uint16_t *Kp, int64_t cap, int64_t n, int row) {
+    constexpr int CR = DT * 2 / 16, CP = DP * 2 / 16;
+    const int x = threadIdx.x;
+    if (x < 2 * CR) {
+        const int v = x / CR, ch = x % CR;
+        reinterpret_cast<uint4 *>((v ? V : K) + ((int64_t)row * cap + n) * DT)[ch] =
+            reinterpret_cast<const uint4 *>(kvn + v * DT * 2)[ch];
+    } else if (x < 2 * CR + CP) {
+        reinterpret_cast<uint4 *>(Kp + ((int64_t)row * cap + n) * DP)[x - 2 * CR] =
+            reinterpret_cast<const uint4 *>(kpn)[x - 2 * CR];
     }
 }
 
@@ -363,8 +357,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     int32_t *stok = reinterpret_cast<int32_t *>(smb + Y.stok);
     uint32_t *skey = reinterpret_cast<uint32_t *>(smb + Y.skey);
     uint8_t *kept = smb + Y.kept;
-    float *qs = reinterpret_cast<float *>(smb + Y.qs);
-    float *kpn = reinterpret_cast<float *>(smb + Y.kpn);
+    uint16_t *kpn = reinterpret_cast<uint16_t *>(smb + Y.kpn);
     const int LIST = NB * 32;   // capacity of stok / skey / kept
 
     auto tok_of = [&](int e) -> int64_t { return ((int64_t)(c + (e >> 5) * C) << 5) + (e & 31); };
@@ -402,9 +395,11 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     const int qg = threadIdx.x / (DT / 8), qc = threadIdx.x % (DT / 8);   // Q tile chunk of this thread
     uint4 qv = make_uint4(0, 0, 0, 0);
     if (qg < G) qv = *reinterpret_cast<const uint4 *>(qrow + qg * DT + qc * 8);
-    const uint16_t qsr = (int)threadIdx.x < G * DP ? qi[threadIdx.x] : (uint16_t)0;   // converted after the Kp issue
-    WarpAppend<DT, DP> ar;
-    if (owner) append_warp_issue<DT, DP>(ar, a.K_new, a.V_new, a.Wk, row, h);
+    // the owner's Wk rows are staged where the candidate lists go later
+    static_assert(DT * DP * 2 <= 2 * kCandCap * 4, "Wk of one head fits the candidate lists");
+    uint8_t *wsm = smb + Y.ckey;
+    uint8_t *kvn = smb + Y.knew;
+    if (owner) append_issue<DT, DP>(a.K_new, a.V_new, a.Wk, row, h, wsm, kvn);   // (in commit group 0)
 
     // ---- 1a. Kp blocks -> shared memory: 16-byte cp.async by every thread,
     // consecutive threads on consecutive chunks; owned block j belongs to
@@ -427,7 +422,6 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     }
     // ---- 1b. the small inputs to shared memory; histograms cleared
     if (qg < 16) *reinterpret_cast<uint4 *>(qsm + qg * (2 * DT + 16) + qc * 16) = qv;
-    if ((int)threadIdx.x < G * DP) qs[threadIdx.x] = bf16_to_f(qsr);
     for (int x = threadIdx.x; x < kRadixBins; x += blockDim.x) S.hist[x] = 0;
     for (int x = threadIdx.x; x < kFFFine; x += blockDim.x) fine[x] = 0;
     const uint16_t *Kh = a.K + (int64_t)row * a.cap * DT;
@@ -443,6 +437,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         const float invG = 1.0f / (float)G;
         const int ntile = (nb * 32) >> 4;
         int grp = -1;
+        // the owner's appended token: local row and the group of its block
+        const int en = (blk_n / C) * 32 + (int)(a.n & 31);
+        const int g_n = owner ? (blk_n / C) / gsz : -1;
         for (int tt = 0; tt < ntile; tt += kFFWarps) {
             // every thread waits for its own copies of the group, then the CTA
             // barrier makes all threads' copies of it visible
@@ -451,6 +448,17 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 ++grp;
                 cp_async_wait_pending(kFFKpGroups - 1 - grp);
                 __syncthreads();
+                if (owner && grp == 0) {   // Wk, K_new and V_new arrived with group 0
+                    append_project<DT, DP>(reinterpret_cast<const uint16_t *>(wsm),
+                                           reinterpret_cast<const uint16_t *>(kvn), kpn);
+                    __syncthreads();
+                }
+                if (grp == g_n) {   // the fresh Kp row replaces the copied one before it is scored
+                    if ((int)threadIdx.x < DP / 8)
+                        *reinterpret_cast<uint4 *>(X + (size_t)en * DP * 2 + 16 * threadIdx.x) =
+                            reinterpret_cast<const uint4 *>(kpn)[threadIdx.x];
+                    __syncthreads();
+                }
             }
             if (tt + warp >= ntile) continue;
             const int tw = tt + warp;
@@ -521,27 +529,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         }
     }
     cp_async_wait_all();   // (the groups are complete; nothing may reuse X while a copy could land)
-    __syncthreads();
-    if (owner) {
-        append_warp_finish<DT, DP>(ar, a.K, a.V, a.Kp, a.cap, a.n, row, kpn);
-        __syncthreads();
-    }
-    if (owner && threadIdx.x == 0) {
-        // the appended token scores from its freshly projected row (its Kp
-        // row in shared memory may predate the append)
-        float s = a.agg == TB_AGG_MEAN ? 0.f : -INFINITY;
-        for (int g = 0; g < G; ++g) {
-            float p = 0.f;
-            for (int i = 0; i < DP; ++i) p = fmaf(qs[g * DP + i], kpn[i], p);
-            s = a.agg == TB_AGG_MEAN ? s + p : fmaxf(s, p);
-        }
-        if (a.agg == TB_AGG_MEAN) s *= 1.0f / (float)G;
-        const int en = (blk_n / C) * 32 + (int)(a.n & 31);
-        atomicSub(&S.hist[S.keys[en] >> 21], 1u);
-        const uint32_t key = score_key(s, nan_seen);
-        atomicAdd(&S.hist[key >> 21], 1u);
-        S.keys[en] = key;
-    }
+    if (owner) append_store<DT, DP>(kvn, kpn, a.K, a.V, a.Kp, a.cap, a.n, row);
     if (nan_seen) set_status(a.dev_status, TB_ERR_NONFINITE);
     __syncthreads();
 
@@ -560,13 +548,16 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     uint32_t F0 = 0;
     if (Bhi != kNone) F0 = Bhi >= 3 ? Bhi - 3 : 0;
     else if (Blo != kNone) F0 = Blo >= 3 ? Blo - 3 : 0;
-    for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
-        const bool valid = e < Lv;
-        const uint32_t key = S.keys[e];
-        const uint32_t cb = key >> 21;
-        if (valid && cb >= F0 && cb <= F0 + 3) atomicAdd(&fine[(key >> 16) - (F0 << 5)], 1u);
-        const uint32_t ob = __ballot_sync(0xFFFFFFFFu, valid && cb > F0 + 3);
-        if (lane == 0 && ob) atomicAdd(&cnt[CN_RANGE], (uint32_t)__popc(ob));
+    {
+        uint32_t n_up = 0;   // keys above the fine range
+        for (int e = threadIdx.x; e < Lv; e += blockDim.x) {
+            const uint32_t key = S.keys[e];
+            const uint32_t cb = key >> 21;
+            if (cb >= F0 && cb <= F0 + 3) atomicAdd(&fine[(key >> 16) - (F0 << 5)], 1u);
+            n_up += cb > F0 + 3 ? 1u : 0u;
+        }
+        n_up = __reduce_add_sync(0xFFFFFFFFu, n_up);
+        if (lane == 0 && n_up) atomicAdd(&cnt[CN_RANGE], n_up);
     }
     __syncthreads();
     if (warp == 0) warp_find_fine(fine, cnt[CN_RANGE], need_hi, need_lo, S.misc + 4);
@@ -583,30 +574,54 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     uint8_t *myrec = a.rec + ((int64_t)row * C + c) * kFFRecBytes;
     uint2 *myent = reinterpret_cast<uint2 *>(myrec + sizeof(FFHdr));
     uint8_t *blkab = a.blk_above + (int64_t)row * a.blk_stride;
-    for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
-        const int64_t t = tok_of(e);
-        const uint32_t key = S.keys[e];
-        const uint32_t pf = key >> 16;
-        const bool valid = e < Lv;
-        const bool above = valid && pf > hi16;
-        const bool inwin = valid && !above && pf >= lo16;
-        const uint32_t ab = __ballot_sync(0xFFFFFFFFu, above);
-        if (lane == 0) blkab[c + (e >> 5) * C] = (uint8_t)__popc(ab);
-        const uint32_t as = warp_alloc(&cnt[CN_ABOVE], above);
-        if (above) {
-            stok[as] = (int32_t)t;
-            skey[as] = key;
+    // a warp takes whole blocks; its slots are reserved with one atomic per
+    // list (first pass: counts), then filled in order (second pass)
+    {
+        const uint32_t lt = (1u << lane) - 1u;
+        uint32_t na = 0, nw = 0;
+        for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+            const uint32_t pf = S.keys[e] >> 16;
+            const bool valid = e < Lv;
+            const bool above = valid && pf > hi16;
+            const uint32_t ab = __ballot_sync(0xFFFFFFFFu, above);
+            const uint32_t wb = __ballot_sync(0xFFFFFFFFu, valid && !above && pf >= lo16);
+            if (lane == 0) blkab[c + (e >> 5) * C] = (uint8_t)__popc(ab);
+            na += (uint32_t)__popc(ab);
+            nw += (uint32_t)__popc(wb);
         }
-        const uint32_t ws = warp_alloc(&cnt[CN_WIN], inwin);
-        if (inwin) {
-            stok[LIST - 1 - ws] = (int32_t)t;
-            skey[LIST - 1 - ws] = key;
-            if (ws < (uint32_t)kFFEntMax) myent[ws] = make_uint2(key, (uint32_t)t);
+        uint32_t as = 0, ws = 0;
+        if (lane == 0) {
+            if (na) as = atomicAdd(&cnt[CN_ABOVE], na);
+            if (nw) ws = atomicAdd(&cnt[CN_WIN], nw);
+        }
+        as = __shfl_sync(0xFFFFFFFFu, as, 0);
+        ws = __shfl_sync(0xFFFFFFFFu, ws, 0);
+        for (int e = threadIdx.x; e < nb * 32 && (na | nw); e += blockDim.x) {
+            const int64_t t = tok_of(e);
+            const uint32_t key = S.keys[e];
+            const uint32_t pf = key >> 16;
+            const bool valid = e < Lv;
+            const bool above = valid && pf > hi16;
+            const bool inwin = valid && !above && pf >= lo16;
+            const uint32_t ab = __ballot_sync(0xFFFFFFFFu, above);
+            const uint32_t wb = __ballot_sync(0xFFFFFFFFu, inwin);
+            if (above) {
+                const uint32_t sl = as + (uint32_t)__popc(ab & lt);
+                stok[sl] = (int32_t)t;
+                skey[sl] = key;
+            }
+            if (inwin) {
+                const uint32_t sl = ws + (uint32_t)__popc(wb & lt);
+                stok[LIST - 1 - sl] = (int32_t)t;
+                skey[LIST - 1 - sl] = key;
+                if (sl < (uint32_t)kFFEntMax) myent[sl] = make_uint2(key, (uint32_t)t);
+            }
+            as += (uint32_t)__popc(ab);
+            ws += (uint32_t)__popc(wb);
         }
     }
     __syncthreads();
     const int n_above = (int)cnt[CN_ABOVE], n_win = (int)cnt[CN_WIN];
-    const int n_att = n_above + n_win;
     if (threadIdx.x == 0) {
         FFHdr hd;
         hd.above = (uint32_t)n_above;
@@ -619,24 +634,27 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     }
     group_arrive(&rc->bar);
 
-    // ---- 4b. gather the first round of K/V rows (above, then window)
-    auto att_tok = [&](int i) -> int64_t { return i < n_above ? stok[i] : stok[LIST - 1 - (i - n_above)]; };
-    auto att_key = [&](int i) -> uint32_t { return i < n_above ? skey[i] : skey[LIST - 1 - (i - n_above)]; };
+    // ---- 4b. gather the K/V rows of the tokens above the window: every one
+    // of them is kept. The attention list is these, then the window's kept
+    // tokens (wk, known after the exchange).
+    int32_t *wk = reinterpret_cast<int32_t *>(S.hist);
+    auto att_tok = [&](int i) -> int64_t { return i < n_above ? stok[i] : wk[i - n_above]; };
     constexpr int CPR = DT / 8;   // 16-byte chunks per row
     // a group of 2*CPR lanes copies one row's K and V (one 16-byte chunk each)
     constexpr int RPW = 32 / (2 * CPR);   // rows per warp per pass
     const int rl = lane % (2 * CPR);
     const bool rl_v = rl >= CPR;
     const int rl_c = rl_v ? rl - CPR : rl;
-    auto gather_round = [&](int r0, int nr) {
-        for (int s = warp * RPW + lane / (2 * CPR); s < nr; s += kFFWarps * RPW) {
+    // list entries r0 + s -> slots s, for s in [s0, s1)
+    auto gather_rows = [&](int r0, int s0, int s1) {
+        for (int s = s0 + warp * RPW + lane / (2 * CPR); s < s1; s += kFFWarps * RPW) {
             const int64_t t = att_tok(r0 + s);
             cp_async16(X + (size_t)s * SB + (rl_v ? 2 * DT : 0) + rl_c * 16, (rl_v ? Vh : Kh) + t * DT + rl_c * 8);
         }
         cp_async_commit();
     };
-    const int n_r1 = n_att < a.stage_cap ? n_att : a.stage_cap;
-    gather_round(0, n_r1);
+    const int n_r1 = n_above < a.stage_cap ? n_above : a.stage_cap;
+    gather_rows(0, 0, n_r1);
 
     // ---- 5. the row's exchange; read every record of the row
     if (!group_wait(&rc->bar, (uint32_t)C, S.abort_flag, a.dev_status)) {
@@ -671,6 +689,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     bool fast = cnt[CN_VALID] != 0 && Lw <= Hw;
     uint32_t is_cand = 0;
     if (fast) {
+        // per thread: entries above the intersection (counted per block) and
+        // candidates inside it; one atomic per warp and counter
+        uint32_t n_hi = 0, n_c = 0;
 #pragma unroll
         for (int i = 0; i < kFFEntPerThread; ++i) {
             const bool have = rr < C && (uint32_t)(rsub + P * i) < hd4.w;
@@ -678,14 +699,32 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             const bool hi_side = have && pf > Hw;
             const bool cand = have && !hi_side && pf >= Lw;
             if (hi_side) atomicAdd(&bcnt[ent[i].y >> 5], 1u);
-            const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hi_side);
-            if (lane == 0 && hb) atomicAdd(&cnt[CN_AE], (uint32_t)__popc(hb));
-            const uint32_t cs = warp_alloc(&cnt[CN_CAND], cand);
-            if (cand && cs < (uint32_t)kCandCap) {
-                S.ckey[cs] = ent[i].x;
-                S.cidx[cs] = ent[i].y;
-            }
+            n_hi += hi_side ? 1u : 0u;
+            n_c += cand ? 1u : 0u;
             if (cand) is_cand |= 1u << i;
+        }
+        uint32_t x = n_c;   // inclusive scan of the candidate counts over the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        const uint32_t hw_tot = __reduce_add_sync(0xFFFFFFFFu, n_hi);
+        uint32_t base = 0;
+        if (lane == 31) {
+            if (hw_tot) atomicAdd(&cnt[CN_AE], hw_tot);
+            if (x) base = atomicAdd(&cnt[CN_CAND], x);
+        }
+        uint32_t cs = __shfl_sync(0xFFFFFFFFu, base, 31) + x - n_c;
+#pragma unroll
+        for (int i = 0; i < kFFEntPerThread; ++i) {
+            if ((is_cand >> i) & 1u) {
+                if (cs < (uint32_t)kCandCap) {
+                    S.ckey[cs] = ent[i].x;
+                    S.cidx[cs] = ent[i].y;
+                }
+                ++cs;
+            }
         }
     }
     __syncthreads();
@@ -733,12 +772,21 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
 
     float *prow = a.part + (int64_t)row * C * G * (2 + DT);
     if (fast) {
-        // ---- 5c. kept flags of the gathered rows; per-block kept counts of the row
+        // ---- 5c. per-block kept counts of the row; the window's kept tokens
+        // -> wk; flags of the attention list (zero past its end)
 #pragma unroll
         for (int i = 0; i < kFFEntPerThread; ++i)
             if (((is_cand >> i) & 1u) && composite(ent[i].x, ent[i].y) >= T) atomicAdd(&bcnt[ent[i].y >> 5], 1u);
-        for (int i = threadIdx.x; i < LIST; i += blockDim.x)
-            kept[i] = (i < n_att && composite(att_key(i), (uint32_t)att_tok(i)) >= T) ? 1 : 0;
+        __syncthreads();   // (the selection's scratch in S.hist is dead)
+        for (int i0 = 0; i0 < n_win; i0 += blockDim.x) {
+            const int i = i0 + (int)threadIdx.x;
+            const bool kp = i < n_win && composite(skey[LIST - 1 - i], (uint32_t)stok[LIST - 1 - i]) >= T;
+            const uint32_t sl = warp_alloc(&cnt[CN_WK], kp);
+            if (kp) wk[sl] = stok[LIST - 1 - i];
+        }
+        __syncthreads();
+        const int n_att = n_above + (int)cnt[CN_WK];
+        for (int i = threadIdx.x; i < LIST; i += blockDim.x) kept[i] = i < n_att ? 1 : 0;
         // ---- 6. attention over the gathered rows, round by round
         MmaAttn<NT> A;
         A.m0 = A.m1 = -INFINITY;
@@ -748,16 +796,13 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         const float qscale = a.scale * kLog2e;
         for (int r0 = 0; r0 < n_att; r0 += a.stage_cap) {
             const int nr = n_att - r0 < a.stage_cap ? n_att - r0 : a.stage_cap;
-            if (r0 > 0) {
-                __syncthreads();   // the previous round's rows are consumed
-                gather_round(r0, nr);
-            }
-            cp_async_wait_all();
-            __syncthreads();
-            // rows that take no part (not kept, or padding to 16) hold zeros in V
+            if (r0 > 0) __syncthreads();   // the previous round's rows are consumed
+            gather_rows(r0, r0 > 0 ? 0 : n_r1, nr);
+            // the padding rows up to a multiple of 16 hold zeros in V
             const int npad = (nr + 15) & ~15;
-            for (int s = warp * RPW + lane / (2 * CPR); s < npad; s += kFFWarps * RPW)
-                st_shared_zero16_if(X + (size_t)s * SB + 2 * DT + rl_c * 16, rl_v && !kept[r0 + s]);
+            for (int s = nr + warp * RPW + lane / (2 * CPR); s < npad; s += kFFWarps * RPW)
+                if (rl_v) st_shared_zero16_if(X + (size_t)s * SB + 2 * DT + rl_c * 16, true);
+            cp_async_wait_all();
             __syncthreads();
             mma_attend<DT, kFFWarps>(A, X, SB, nr, kept, r0, qsm, qscale);
         }
