@@ -189,52 +189,73 @@ __device__ __forceinline__ void row_merge_tail(RowCtl *rc, const float *prow, in
     }
 }
 
-// The row's last CTA to arrive merges the C partial states (each CTA stored
-// its partial at prow + c * G * (2 + D) before arriving). A thread per output
-// issues the loads of all partials of a batch of up to 32 splits before using
-// any, so a batch costs one L2 round trip. Returns true in the CTA that
+// The row's last-arriving CTA merges the C partial states (m, l, acc[D]) per
+// head into out_rows ([G][D] bf16) and resets the row's control words; the
+// others return false at once. Arrival is one acq_rel atomic by thread 0
+// (release of the CTA's partial, acquire of the others' for the merger),
+// ordered with the CTA's other threads by the barriers around it. The merger
+// requests its first accumulators before the weights are known (one round
+// trip for up to 32 chunks), then weights exp2(m_c - M) and w l per (chunk,
+// head) go to
+// `scratch` (4 C G floats of shared memory). Returns true in the CTA that
 // merged; that CTA also resets the row's control words (and the radix
 // histograms when reset_hist). flag: one shared word. All threads call it.
 __device__ __forceinline__ bool row_merge_last(RowCtl *rc, const float *prow, int C, int G, int D,
                                                uint16_t *out_rows, uint32_t *flag, bool reset_hist,
-                                               int32_t *dev_status) {
-    constexpr int kBatch = 32;
+                                               int32_t *dev_status, float *scratch) {
+    constexpr int kBatch = 32;   // chunks per round trip
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(&rc->done, 1u);
+        uint32_t prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(&rc->done) : "memory");
         *flag = (prev == (uint32_t)(C - 1)) ? 1u : 0u;
     }
     __syncthreads();
     if (!*flag) return false;
-    __threadfence();
-    const int sg = 2 + D;
-    for (int x = threadIdx.x; x < G * D; x += blockDim.x) {
+    const int sg = 2 + D, CG = C * G;
+    float *ms = scratch, *ls = scratch + CG, *wt = scratch + 2 * CG, *wl = scratch + 3 * CG;
+    // a thread per output (g, d); its first batch of accumulators is
+    // requested before the weights are known
+    const int x0 = threadIdx.x;
+    const bool act0 = x0 < G * D;
+    const int g0 = act0 ? x0 / D : 0, d0 = act0 ? x0 % D : 0;
+    float av[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) av[u] = (act0 && u < C) ? __ldcg(prow + (u * G + g0) * sg + 2 + d0) : 0.f;
+    for (int y = threadIdx.x; y < CG; y += blockDim.x) {
+        ms[y] = __ldcg(prow + (int64_t)y * sg);
+        ls[y] = __ldcg(prow + (int64_t)y * sg + 1);
+    }
+    __syncthreads();
+    for (int y = threadIdx.x; y < CG; y += blockDim.x) {
+        const int g = y % G;
+        float M = -INFINITY;
+        for (int u0 = 0; u0 < C; u0 += kBatch) {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (u0 + u < C) M = fmaxf(M, ms[(u0 + u) * G + g]);
+        }
+        const float w = rescale_w(ms[y], M);
+        wt[y] = w;
+        wl[y] = w * ls[y];
+    }
+    __syncthreads();
+    for (int x = x0; x < G * D; x += blockDim.x) {
         const int g = x / D, d = x % D;
-        float M = -INFINITY, L = 0.f, Acc = 0.f;
-        for (int sp0 = 0; sp0 < C; sp0 += kBatch) {
-            float mv[kBatch], lv[kBatch], av[kBatch];
+        float L = 0.f, Acc = 0.f;
+        for (int u0 = 0; u0 < C; u0 += kBatch) {
+            if (x != x0 || u0 != 0) {
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+                    av[u] = u0 + u < C ? __ldcg(prow + ((int64_t)(u0 + u) * G + g) * sg + 2 + d) : 0.f;
+            }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
-                const bool in = sp0 + u < C;
-                const float *pp = prow + ((int64_t)(in ? sp0 + u : 0) * G + g) * sg;
-                mv[u] = in ? __ldcg(pp) : -INFINITY;
-                lv[u] = in ? __ldcg(pp + 1) : 0.f;
-                av[u] = in ? __ldcg(pp + 2 + d) : 0.f;
+                if (u0 + u < C) {
+                    L += wl[(u0 + u) * G + g];
+                    Acc = fmaf(wt[(u0 + u) * G + g], av[u], Acc);
+                }
             }
-            float Mb = M;
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) Mb = fmaxf(Mb, mv[u]);
-            const float rsc = rescale_w(M, Mb);
-            L *= rsc;
-            Acc *= rsc;
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const float w = rescale_w(mv[u], Mb);
-                L = fmaf(w, lv[u], L);
-                Acc = fmaf(w, av[u], Acc);
-            }
-            M = Mb;
         }
         if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
         out_rows[(int64_t)g * D + d] = f_to_bf16(L > 0.f ? Acc / L : 0.f);

@@ -91,10 +91,12 @@ __host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int 
     int x = 0;
     int xb = NB * 32 * dp * 2;                                   // Kp blocks
     const int sb = stage_cap * ff_slot_bytes(D);                 // gathered K/V rows
-    const int wb = kFFWarps * G * (2 + D) * 4;                   // per-warp attention states
+    const int wb = (kFFWarps * G * (2 + D) + kFFWarps * G + G) * 4;   // per-warp attention states, weights
+    const int mb = 4 * C * G * 4 > 3 * (G * D + C) * 4 ? 4 * C * G * 4 : 3 * (G * D + C) * 4;   // merge scratch
     const int cb = comb_floats_for(kFFThreads, G, D) * 4;        // general path's combine scratch
     if (sb > xb) xb = sb;
     if (wb > xb) xb = wb;
+    if (mb > xb) xb = mb;
     if (cb > xb) xb = cb;
     L.X = x; x += ff_a16(xb);
     L.qsm = x; x += 16 * (2 * D + 16);
@@ -148,30 +150,42 @@ __device__ __forceinline__ uint32_t warp_alloc(uint32_t *ctr, bool want) {
     return base + (uint32_t)__popc(m & ((1u << lane) - 1u));
 }
 
-// Bins of two targets (ranks from the top, 1-based; 0 = none) in a histogram
-// of nbins (a multiple of blockDim.x). out = {bin1, above1, bin2, above2},
-// kNone where a target is 0 or beyond the total. All threads call.
-__device__ __forceinline__ void find_two_bins(const uint32_t *hist, int nbins, uint32_t need1, uint32_t need2,
-                                           uint32_t *scan, uint32_t *out) {
+// Four counters hist[hi - 3 .. hi] (hi + 1 a multiple of 4, 16-byte aligned)
+// in one 16-byte load, highest first.
+__device__ __forceinline__ void load_top4(const uint32_t *hist, int hi, uint32_t (&v)[4]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(hist + hi - 3);
+    v[0] = u.w;
+    v[1] = u.z;
+    v[2] = u.y;
+    v[3] = u.x;
+}
+
+// Bins of two targets (ranks from the top, 1-based; 0 = none) in the
+// kRadixBins-bin histogram, four bins per thread of the CTA's kFFThreads.
+// out = {bin1, above1, bin2, above2}, kNone where a target is 0 or beyond
+// the total. All threads call.
+__device__ __forceinline__ void find_two_bins(const uint32_t *hist, uint32_t need1, uint32_t need2, uint32_t *scan,
+                                              uint32_t *out) {
+    static_assert(kRadixBins == 4 * kFFThreads, "four bins per thread");
     if (threadIdx.x == 0) out[0] = out[1] = out[2] = out[3] = kNone;
-    const int per = nbins / blockDim.x;
-    const int hi = nbins - 1 - threadIdx.x * per;
-    uint32_t local = 0;
-    for (int j = 0; j < per; ++j) local += hist[hi - j];
+    const int hi = kRadixBins - 1 - threadIdx.x * 4;
+    uint32_t hv[4];
+    load_top4(hist, hi, hv);
+    const uint32_t local = hv[0] + hv[1] + hv[2] + hv[3];
     uint32_t total;
     const uint32_t above = block_exclusive_scan(local, scan, total);
     for (int t = 0; t < 2; ++t) {
         const uint32_t need = t == 0 ? need1 : need2;
         if (need >= 1 && above < need && need <= above + local) {
             uint32_t a = above;
-            for (int j = 0; j < per; ++j) {
-                const uint32_t c = hist[hi - j];
-                if (need <= a + c) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (need <= a + hv[j]) {
                     out[2 * t] = (uint32_t)(hi - j);
                     out[2 * t + 1] = a;
                     break;
                 }
-                a += c;
+                a += hv[j];
             }
         }
     }
@@ -185,8 +199,9 @@ __device__ __forceinline__ void warp_find_fine(const uint32_t *fine, uint32_t ba
                                             uint32_t *out) {
     const int lane = threadIdx.x & 31;
     const int hi = kFFFine - 1 - lane * 4;
-    uint32_t local = 0;
-    for (int j = 0; j < 4; ++j) local += fine[hi - j];
+    uint32_t fv[4];
+    load_top4(fine, hi, fv);
+    const uint32_t local = fv[0] + fv[1] + fv[2] + fv[3];
     uint32_t x = local;
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
@@ -199,8 +214,9 @@ __device__ __forceinline__ void warp_find_fine(const uint32_t *fine, uint32_t ba
         const uint32_t need = t == 0 ? need1 : need2;
         if (need >= 1 && above < need && need <= above + local) {
             uint32_t a = above;
+#pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t c = fine[hi - j];
+                const uint32_t c = fv[j];
                 if (need <= a + c) {
                     out[t] = (uint32_t)(hi - j);
                     out[2 + t] = a;
@@ -250,22 +266,32 @@ __device__ __forceinline__ void append_issue(const uint16_t *K_new, const uint16
     }
 }
 
-// kpn [DP] (shared bf16) <- the projected row; wsm and kvn landed and visible.
-// The caller synchronises before reading kpn.
+// kpn [DP] (shared bf16) <- the projected row; wsm and kvn landed and
+// visible. Warp w takes dims [w DT/16, (w+1) DT/16) and lane l output l % DP
+// (lanes of one warp read consecutive Wk entries: no bank conflicts); the 16
+// warps' fp32 partial sums meet in red [16 x 32] and are rounded once to bf16.
+// Needs 16 warps; the caller synchronises before reading kpn.
 template <int DT, int DP>
-__device__ __forceinline__ void append_project(const uint16_t *wsm, const uint16_t *kn, uint16_t *kpn) {
+__device__ __forceinline__ void append_project(const uint16_t *wsm, const uint16_t *kn, float *red, uint16_t *kpn) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int DPL = DT / 32, OPW = (DP + 15) / 16;
+    constexpr int DPW = DT / 16;      // dims per warp
+    constexpr int LPJ = 32 / DP;      // lanes per output
+    constexpr int DPL = DPW / LPJ;    // dims per lane
+    static_assert(DPL * LPJ == DPW && DPL >= 1, "dims split evenly over the lanes of an output");
+    static_assert(kFFThreads == 512, "16 warps");
+    const int j = lane % DP, d0 = warp * DPW + (lane / DP) * DPL;
+    float acc = 0.f;
 #pragma unroll
-    for (int o = 0; o < OPW; ++o) {
-        const int j = warp * OPW + o;
-        if (j >= DP) break;   // (warp-uniform)
-        float acc = 0.f;
+    for (int i = 0; i < DPL; ++i) acc = fmaf(bf16_to_f(kn[d0 + i]), bf16_to_f(wsm[(d0 + i) * DP + j]), acc);
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    if ((int)threadIdx.x < DP) {
+        float sum = 0.f;
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc = fmaf(bf16_to_f(kn[lane + 32 * i]), bf16_to_f(wsm[(lane + 32 * i) * DP + j]), acc);
+        for (int w = 0; w < 16; ++w)
 #pragma unroll
-        for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, x);
-        if (lane == 0) kpn[j] = f_to_bf16(acc);
+            for (int hh = 0; hh < LPJ; ++hh) sum += red[w * 32 + hh * DP + threadIdx.x];
+        kpn[threadIdx.x] = f_to_bf16(sum);
     }
 }
 
@@ -282,6 +308,73 @@ __device__ __forceinline__ void append_store(const uint8_t *kvn, const uint16_t 
     } else if (x < 2 * CR + CP) {
         reinterpret_cast<uint4 *>(Kp + ((int64_t)row * cap + n) * DP)[x - 2 * CR] =
             reinterpret_cast<const uint4 *>(kpn)[x - 2 * CR];
+    }
+}
+
+// The row's merge, spread over its C CTAs (after the row's second barrier):
+// CTA c takes outputs x in [c NX, (c + 1) NX) of the G x D, NX = ceil(G D /
+// C). A thread per (chunk u, output x) loads m, l and acc of that chunk (all
+// loads in flight together), finds M_x = max_u m over shared memory and
+// leaves w l and w acc, w = exp2(m - M_x); a thread per output sums them over
+// the chunks and rounds once to bf16. scratch: 3 C NX floats of shared
+// memory. C NX <= G D + C <= 2048 + 148 fits kMergePer pairs per thread.
+constexpr int kMergePer = 5;
+__device__ __forceinline__ void row_merge_slice(const float *prow, int C, int c, int G, int D, uint16_t *out_rows,
+                                                float *scratch, int32_t *dev_status) {
+    const int sg = 2 + D, GD = G * D;
+    const int NX = (GD + C - 1) / C;
+    const int x_lo = c * NX;
+    const int nx = GD - x_lo < NX ? GD - x_lo : NX;   // (<= 0 for trailing CTAs)
+    const int CN = C * NX;
+    if (CN > kMergePer * (int)blockDim.x) {   // (not reached for G <= 16, D <= 128)
+        if (threadIdx.x == 0) set_status(dev_status, TB_ERR_UNSUPPORTED);
+        return;
+    }
+    float *mm = scratch, *pl = scratch + CN, *pa = scratch + 2 * CN;
+    float m[kMergePer], l[kMergePer], av[kMergePer];
+#pragma unroll
+    for (int k = 0; k < kMergePer; ++k) {
+        const int t = threadIdx.x + k * blockDim.x;
+        const int u = t / NX, xl = t % NX;
+        m[k] = -INFINITY;
+        l[k] = av[k] = 0.f;
+        if (t < CN && xl < nx) {
+            const int x = x_lo + xl, g = x / D, d = x % D;
+            const float *p = prow + ((int64_t)u * G + g) * sg;
+            m[k] = __ldcg(p);
+            l[k] = __ldcg(p + 1);
+            av[k] = __ldcg(p + 2 + d);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kMergePer; ++k) {
+        const int t = threadIdx.x + k * blockDim.x;
+        if (t < CN) mm[t] = m[k];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kMergePer; ++k) {
+        const int t = threadIdx.x + k * blockDim.x;
+        if (t < CN) {
+            const int xl = t % NX;
+            float M = -INFINITY;
+#pragma unroll 6
+            for (int u = 0; u < C; ++u) M = fmaxf(M, mm[u * NX + xl]);
+            const float w = rescale_w(m[k], M);
+            pl[t] = w * l[k];
+            pa[t] = w * av[k];
+        }
+    }
+    __syncthreads();
+    for (int xl = threadIdx.x; xl < nx; xl += blockDim.x) {
+        float L = 0.f, A = 0.f;
+#pragma unroll 6
+        for (int u = 0; u < C; ++u) {
+            L += pl[u * NX + xl];
+            A += pa[u * NX + xl];
+        }
+        if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
+        out_rows[x_lo + xl] = f_to_bf16(L > 0.f ? A / L : 0.f);
     }
 }
 
@@ -395,8 +488,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     const int qg = threadIdx.x / (DT / 8), qc = threadIdx.x % (DT / 8);   // Q tile chunk of this thread
     uint4 qv = make_uint4(0, 0, 0, 0);
     if (qg < G) qv = *reinterpret_cast<const uint4 *>(qrow + qg * DT + qc * 8);
-    // the owner's Wk rows are staged where the candidate lists go later
-    static_assert(DT * DP * 2 <= 2 * kCandCap * 4, "Wk of one head fits the candidate lists");
+    // the owner's Wk rows (and the projection's partial sums) are staged
+    // where the candidate lists go later
+    static_assert(DT * DP * 2 <= kCandCap * 4 && kFFThreads * 4 <= kCandCap * 4, "append staging fits");
     uint8_t *wsm = smb + Y.ckey;
     uint8_t *kvn = smb + Y.knew;
     if (owner) append_issue<DT, DP>(a.K_new, a.V_new, a.Wk, row, h, wsm, kvn);   // (in commit group 0)
@@ -450,7 +544,8 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 __syncthreads();
                 if (owner && grp == 0) {   // Wk, K_new and V_new arrived with group 0
                     append_project<DT, DP>(reinterpret_cast<const uint16_t *>(wsm),
-                                           reinterpret_cast<const uint16_t *>(kvn), kpn);
+                                           reinterpret_cast<const uint16_t *>(kvn),
+                                           reinterpret_cast<float *>(S.cidx), kpn);
                     __syncthreads();
                 }
                 if (grp == g_n) {   // the fresh Kp row replaces the copied one before it is scored
@@ -543,7 +638,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         if (t_c + R <= Lv) need_lo = (uint32_t)(t_c + R);
     }
     uint32_t *bins = S.misc;   // {Bhi, Ahi, Blo, Alo}
-    find_two_bins(S.hist, kRadixBins, need_hi, need_lo, S.scan, bins);
+    find_two_bins(S.hist, need_hi, need_lo, S.scan, bins);
     const uint32_t Bhi = bins[0], Blo = bins[2];
     uint32_t F0 = 0;
     if (Bhi != kNone) F0 = Bhi >= 3 ? Bhi - 3 : 0;
@@ -634,9 +729,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     }
     group_arrive(&rc->bar);
 
-    // ---- 4b. gather the K/V rows of the tokens above the window: every one
-    // of them is kept. The attention list is these, then the window's kept
-    // tokens (wk, known after the exchange).
+    // ---- 4b. the attention list: the tokens above the window (every one of
+    // them is kept), then the window's kept tokens (wk, known after the
+    // exchange); its K/V rows are gathered into X, the first ones now.
     int32_t *wk = reinterpret_cast<int32_t *>(S.hist);
     auto att_tok = [&](int i) -> int64_t { return i < n_above ? stok[i] : wk[i - n_above]; };
     constexpr int CPR = DT / 8;   // 16-byte chunks per row
@@ -787,6 +882,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         __syncthreads();
         const int n_att = n_above + (int)cnt[CN_WK];
         for (int i = threadIdx.x; i < LIST; i += blockDim.x) kept[i] = i < n_att ? 1 : 0;
+        // the first round's window rows are requested now
+        const int nr0 = n_att < a.stage_cap ? n_att : a.stage_cap;
+        gather_rows(0, n_r1, nr0);
         // ---- 6. attention over the gathered rows, round by round
         MmaAttn<NT> A;
         A.m0 = A.m1 = -INFINITY;
@@ -796,8 +894,10 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         const float qscale = a.scale * kLog2e;
         for (int r0 = 0; r0 < n_att; r0 += a.stage_cap) {
             const int nr = n_att - r0 < a.stage_cap ? n_att - r0 : a.stage_cap;
-            if (r0 > 0) __syncthreads();   // the previous round's rows are consumed
-            gather_rows(r0, r0 > 0 ? 0 : n_r1, nr);
+            if (r0 > 0) {
+                __syncthreads();   // the previous round's rows are consumed
+                gather_rows(r0, 0, nr);
+            }
             // the padding rows up to a multiple of 16 hold zeros in V
             const int npad = (nr + 15) & ~15;
             for (int s = nr + warp * RPW + lane / (2 * CPR); s < npad; s += kFFWarps * RPW)
@@ -833,46 +933,68 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             }
         }
         __syncthreads();
-        for (int x = threadIdx.x; x < G * DT; x += blockDim.x) {
-            const int g = x / DT, d = x % DT;
+        // weight of warp w's state in head g: exp2(m_wg - M_g), computed once
+        // per (w, g); wts[kFFWarps G + g] = M_g
+        float *wts = ws + kFFWarps * G * sg;
+        if ((int)threadIdx.x < kFFWarps * G) {
+            const int w = threadIdx.x / G, g = threadIdx.x % G;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kFFWarps; ++w) M = fmaxf(M, ws[((int64_t)w * G + g) * sg]);
+            for (int v = 0; v < kFFWarps; ++v) M = fmaxf(M, ws[(v * G + g) * sg]);
+            wts[threadIdx.x] = rescale_w(ws[(w * G + g) * sg], M);
+            if (w == 0) wts[kFFWarps * G + g] = M;
+        }
+        __syncthreads();
+        for (int x = threadIdx.x; x < G * DT; x += blockDim.x) {
+            const int g = x / DT, d = x % DT;
             float L = 0.f, Acc = 0.f;
 #pragma unroll
             for (int w = 0; w < kFFWarps; ++w) {
-                const float *sw = ws + ((int64_t)w * G + g) * sg;
-                const float wt = rescale_w(sw[0], M);
+                const float *sw = ws + (w * G + g) * sg;
+                const float wt = wts[w * G + g];
                 L = fmaf(wt, sw[1], L);
                 Acc = fmaf(wt, sw[2 + d], Acc);
             }
             float *o = prow + ((int64_t)c * G + g) * sg;
             if (d == 0) {
-                o[0] = M;
+                o[0] = wts[kFFWarps * G + g];
                 o[1] = L;
             }
             o[2 + d] = Acc;
         }
-        // ---- 6c. the row's last CTA merges; the others write idx / sel meanwhile
-        const bool merged = row_merge_last(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT,
-                                           &cnt[CN_FLAG], false, a.dev_status);
-        (void)merged;
-        // idx / sel: slots from the row's per-block kept counts
+        // ---- 6c. the row's second barrier; every CTA merges a slice of the
+        // outputs. The last CTA to count itself done resets the row's control
+        // words (all have passed the barrier by then).
+        group_arrive(&rc->bar);
+        // ---- 6d. idx / sel while the other CTAs finish: slots from the row's
+        // per-block kept counts
         block_scan_inplace(bcnt, nblk, S.scan);
-        int32_t *irow = a.idx + (int64_t)row * a.k;
-        int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
-        for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
-            const int64_t t = tok_of(e);
-            const bool kp = e < Lv && composite(S.keys[e], (uint32_t)t) >= T;
-            const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
-            const uint32_t slot = bcnt[t >> 5] + (uint32_t)__popc(km & ((1u << lane) - 1u));
-            if (kp && slot < (uint32_t)a.k) {
-                irow[slot] = (int32_t)t;
-                srow[slot] = (int32_t)t;
+        {
+            int32_t *irow = a.idx + (int64_t)row * a.k;
+            int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
+            for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
+                const int64_t t = tok_of(e);
+                const bool kp = e < Lv && composite(S.keys[e], (uint32_t)t) >= T;
+                const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
+                const uint32_t slot = bcnt[t >> 5] + (uint32_t)__popc(km & ((1u << lane) - 1u));
+                if (kp && slot < (uint32_t)a.k) {
+                    irow[slot] = (int32_t)t;
+                    srow[slot] = (int32_t)t;
+                }
+                if (kp && slot >= (uint32_t)a.k) set_status(a.dev_status, TB_ERR_INVALID_ARG);
             }
-            if (kp && slot >= (uint32_t)a.k) set_status(a.dev_status, TB_ERR_INVALID_ARG);
+            if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
         }
-        if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
+        if (!group_wait(&rc->bar, 2u * (uint32_t)C, S.abort_flag, a.dev_status)) return;
+        uint32_t done_prev = 0;
+        if (threadIdx.x == 0) done_prev = atomicAdd(&rc->done, 1u);
+        row_merge_slice(prow, C, c, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT,
+                        reinterpret_cast<float *>(X), a.dev_status);
+        if (threadIdx.x == 0 && done_prev == (uint32_t)(C - 1)) {
+            rc->bar = 0;
+            rc->ncand = 0;
+            rc->done = 0;
+        }
     } else {
         cp_async_wait_all();
         FFGeneral gp;
@@ -898,7 +1020,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
         // ---- 7. the row's last CTA merges
         (void)row_merge_last(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT, &cnt[CN_FLAG],
-                             true, a.dev_status);
+                             true, a.dev_status, reinterpret_cast<float *>(X));
     }
 }
 

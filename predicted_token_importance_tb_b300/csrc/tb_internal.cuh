@@ -80,9 +80,8 @@ __device__ __forceinline__ bool group_wait(uint32_t *ctr, uint32_t target, int *
                 }
             }
         }
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
     }
-    __syncthreads();
+    __syncthreads();   // (thread 0's acquire orders the CTA's later reads)
     return *abort_flag == 0;
 }
 
