@@ -766,13 +766,24 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         hd4 = __ldcg(reinterpret_cast<const uint4 *>(rrec));
         hvalid = __ldcg(reinterpret_cast<const uint32_t *>(rrec) + 4);
     }
+    // entries 2 q and 2 q + 1 per 16-byte load, q = rsub + P j: thread entry
+    // i is record entry ent_index(i)
+    auto ent_index = [&](int i) -> int { return 2 * (rsub + P * (i >> 1)) + (i & 1); };
 #pragma unroll
-    for (int i = 0; i < kFFEntPerThread; ++i) {
-        const int e = rsub + P * i;
-        ent[i] = (rr < C && e < kFFEntMax) ? __ldcg(reinterpret_cast<const uint2 *>(rrec + sizeof(FFHdr)) + e)
-                                           : make_uint2(0, 0);
+    for (int j = 0; j < kFFEntPerThread / 2; ++j) {
+        const int q = rsub + P * j;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (rr < C && 2 * q + 1 < kFFEntMax) v = __ldcg(reinterpret_cast<const uint4 *>(rrec + sizeof(FFHdr)) + q);
+        ent[2 * j] = make_uint2(v.x, v.y);
+        ent[2 * j + 1] = make_uint2(v.z, v.w);
     }
-    for (int x = threadIdx.x; x < nblk; x += blockDim.x) bcnt[x] = __ldcg(blkab + x);
+    // per-block counts above the owners' windows, four blocks per load
+    for (int x4 = threadIdx.x; 4 * x4 < nblk; x4 += blockDim.x) {
+        const uint32_t v = __ldcg(reinterpret_cast<const uint32_t *>(blkab) + x4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (4 * x4 + j < nblk) bcnt[4 * x4 + j] = (v >> (8 * j)) & 0xFFu;
+    }
     if (rr < C && rsub == 0) {
         atomicMax(&cnt[CN_L], hd4.y);
         atomicMin(&cnt[CN_H], hd4.z);
@@ -789,7 +800,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         uint32_t n_hi = 0, n_c = 0;
 #pragma unroll
         for (int i = 0; i < kFFEntPerThread; ++i) {
-            const bool have = rr < C && (uint32_t)(rsub + P * i) < hd4.w;
+            const bool have = rr < C && (uint32_t)ent_index(i) < hd4.w;
             const uint32_t pf = ent[i].x >> 16;
             const bool hi_side = have && pf > Hw;
             const bool cand = have && !hi_side && pf >= Lw;
