@@ -8,7 +8,8 @@
 // slots: S = Q K^T with m16n8k16 bf16 MMAs (the G query heads are the rows
 // of a 16-row tile, zero-padded; fp32 accumulation), an online softmax in the
 // exp2 domain (fp32), and O += P V with P rounded to bf16. Slots whose flag
-// is zero are masked; their V rows must hold finite values (zeros).
+// is zero (or, with FLAGS = false, slots >= n) are masked; their V rows must
+// hold finite values (zeros).
 #pragma once
 
 #include "async_copy.cuh"
@@ -37,8 +38,9 @@ struct MmaAttn {
 };
 
 // Attend slots [0, n) of the gathered rows (K row at X + s*SB, V row at
-// +2D) for the slots whose kept flag is set; chunks of 16 slots per warp.
-template <int DT, int NW>
+// +2D) for the slots whose kept flag (kept[kept_off + s]) is set, or for all
+// of them with FLAGS = false (kept unused); chunks of 16 slots per warp.
+template <int DT, int NW, bool FLAGS = true>
 __device__ __forceinline__ void mma_attend(MmaAttn<DT / 8> &A, const uint8_t *X, int SB, int n, const uint8_t *kept,
                                            int kept_off, const uint8_t *qsm, float qscale) {
     constexpr int NT = DT / 8, KS = DT / 16, QS = 2 * DT + 16;
@@ -50,8 +52,15 @@ __device__ __forceinline__ void mma_attend(MmaAttn<DT / 8> &A, const uint8_t *X,
         // S = Q K^T for slots s0 .. s0+15 (two n-tiles of 8)
         // kept flags of this lane's columns s0 + 8j + 2(lane%4) + {0,1}
         // (the flags are zero past the gathered rows)
-        const uint32_t f0 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 2 * (lane & 3));
-        const uint32_t f1 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 8 + 2 * (lane & 3));
+        uint32_t f0, f1;
+        if (FLAGS) {
+            f0 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 2 * (lane & 3));
+            f1 = *reinterpret_cast<const uint16_t *>(kept + kept_off + s0 + 8 + 2 * (lane & 3));
+        } else {   // the same byte pattern from the count
+            const int c0 = s0 + 2 * (lane & 3);
+            f0 = (c0 < n ? 0x01u : 0u) | (c0 + 1 < n ? 0x100u : 0u);
+            f1 = (c0 + 8 < n ? 0x01u : 0u) | (c0 + 9 < n ? 0x100u : 0u);
+        }
         // S = Q K^T, two independent accumulator chains per n-tile (even / odd k-steps)
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};

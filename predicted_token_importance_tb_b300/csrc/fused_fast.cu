@@ -9,32 +9,35 @@
 // holds a sample of the whole row and its local score distribution follows
 // the row's.
 //
-//   1. The CTA owning token n appends K_new / V_new and projects K_new.
-//   2. Bulk copies bring the CTA's blocks of Kp into shared memory; the
-//      scores become order-preserving keys.
-//   3. Locally about t_c = k L_c / n of the CTA's L_c tokens are kept, with a
+//   1. Copies bring the CTA's blocks of Kp into shared memory; the CTA owning
+//      token n also stages Wk, K_new and V_new, projects K_new and puts the
+//      fresh Kp row in place before it is scored. Scores become
+//      order-preserving keys.
+//   2. Locally about t_c = k L_c / n of the CTA's L_c tokens are kept, with a
 //      binomial spread sigma = sqrt(t_c (1 - k/n)). From its histogram the
 //      CTA picks a window of 16-bit score prefixes [lo, hi] holding its local
 //      ranks t_c -+ (5 sigma + 4) and publishes: the count above the window,
 //      per-block counts above it, and every (key, token) inside it.
-//   4. It starts gathering the K/V rows of its tokens above and inside the
-//      window into shared memory (cp.async), then waits for the row's
-//      single exchange.
-//   5. All records of the row are read. If the windows intersect in [L, H]
+//   3. It starts gathering the K/V rows of its tokens above the window (all
+//      of them are kept) into shared memory, then waits for the row's single
+//      exchange.
+//   4. All records of the row are read. If the windows intersect in [L, H]
 //      and the row's k-th largest element lies there, the exact threshold T
 //      (the composite of score key and token, lower token first) follows from
 //      the entries inside [L, H]: a fine histogram finds the 16-bit bin of
-//      the k-th element and a rank count inside that bin finds T. Per-block
-//      kept counts of the whole row then give every CTA the slots of its kept
-//      tokens in the ascending idx / sel rows.
+//      the k-th element and a rank count inside that bin finds T. The
+//      window's kept tokens join the gather. Per-block kept counts of the
+//      whole row give every CTA the slots of its kept tokens in the
+//      ascending idx / sel rows.
 //      Otherwise (a window missed: rare unless the score layout is blocky)
 //      the CTAs re-split the row into contiguous chunks through the workspace
 //      and run the general distributed radix select (topk_core.cuh).
-//   6. Attention over the gathered rows runs on the tensor cores: per warp,
+//   5. Attention over the gathered rows runs on the tensor cores: per warp,
 //      chunks of 16 rows, S = Q K^T and O += P V as m16n8k16 bf16 MMAs with
-//      fp32 accumulation and an online softmax (exp2 domain, fp32); rows
-//      that are not kept are masked. The warps' states are combined and the
-//      row's last CTA merges the C partial states.
+//      fp32 accumulation and an online softmax (exp2 domain, fp32). The
+//      warps' states are combined into one partial per CTA; after a second
+//      row barrier (idx / sel are written while it fills) every CTA merges a
+//      slice of the row's outputs from the C partials.
 #include <string.h>
 
 #include "async_copy.cuh"
@@ -50,7 +53,7 @@ constexpr int kFFEntMax = kFastEntMax;
 constexpr int kFFEntPerThread = 8;  // entries of one record a thread reads
 constexpr int kFFStageMax = 512;    // K/V rows gathered into shared memory per round
 constexpr int kFFFine = 128;        // fine bins: 4 coarse bins x 32
-constexpr int kFFKpGroups = 4;      // Kp blocks arrive in groups, each on its own barrier
+constexpr int kFFKpGroups = 4;      // Kp blocks arrive in commit groups, scored as each lands
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 
 struct FFHdr {
@@ -58,7 +61,7 @@ struct FFHdr {
 };
 constexpr int kFFRecBytes = kFastRecBytes;
 static_assert(sizeof(FFHdr) == 32, "record header is 32 bytes");
-static_assert(kFFKpGroups == 4, "cp_async_wait_pending covers four groups");
+static_assert(kFFKpGroups <= 8, "cp_async_wait_pending covers eight groups");
 
 struct FFArgs {
     const uint16_t *q, *q_imp, *K_new, *V_new, *Wk;
@@ -79,8 +82,7 @@ struct FFArgs {
 
 // Shared-memory layout (byte offsets, each 16-byte aligned).
 struct FFLayout {
-    int X, qsm, keys, hist, fine, ckey, cidx, ccount, scan, misc, abort_, cnt, bcnt, stok, skey, kept, kpn, knew, bar,
-        total;
+    int X, qsm, keys, hist, fine, ckey, cidx, ccount, scan, misc, abort_, cnt, bcnt, stok, skey, kpn, knew, total;
 };
 
 __host__ __device__ inline int ff_a16(int x) { return (x + 15) & ~15; }
@@ -91,7 +93,7 @@ __host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int 
     int x = 0;
     int xb = NB * 32 * dp * 2;                                   // Kp blocks
     const int sb = stage_cap * ff_slot_bytes(D);                 // gathered K/V rows
-    const int wb = (kFFWarps * G * (2 + D) + kFFWarps * G + G) * 4;   // per-warp attention states, weights
+    const int wb = kFFWarps * G * (2 + D) * 4;                         // per-warp attention states
     const int mb = 4 * C * G * 4 > 3 * (G * D + C) * 4 ? 4 * C * G * 4 : 3 * (G * D + C) * 4;   // merge scratch
     const int cb = comb_floats_for(kFFThreads, G, D) * 4;        // general path's combine scratch
     if (sb > xb) xb = sb;
@@ -113,10 +115,8 @@ __host__ __device__ inline FFLayout ff_layout(int NB, int C, int stage_cap, int 
     L.bcnt = x; x += ff_a16(NB * C * 4);
     L.stok = x; x += ff_a16(NB * 32 * 4);
     L.skey = x; x += ff_a16(NB * 32 * 4);
-    L.kept = x; x += ff_a16(NB * 32);
     L.kpn = x; x += ff_a16(dp * 2);
     L.knew = x; x += ff_a16(D * 4);   // K_new and V_new rows (bf16)
-    L.bar = x; x += 8 * kFFKpGroups;
     L.total = x;
     return L;
 }
@@ -126,14 +126,28 @@ enum {
     CN_ABOVE = 0, CN_WIN, CN_CAND, CN_AE, CN_L, CN_H, CN_VALID, CN_ASUM, CN_RANGE, CN_BM, CN_FLAG, CN_WK
 };
 
-// Wait until at most n (0..3) of this thread's cp.async groups are pending.
+// Wait until at most n (0..7) of this thread's cp.async groups are pending.
 __device__ __forceinline__ void cp_async_wait_pending(int n) {
     switch (n) {
         case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
         case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
         case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
     }
+}
+
+// Order-preserving fp32 <-> uint32 for maxima by integer atomics (NaN-free
+// inputs; -inf maps above 0, so a zero word is below every value).
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_inv(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 // Warp-aggregated slot allocation on a shared counter: lanes with `want`
@@ -449,9 +463,8 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     uint32_t *bcnt = reinterpret_cast<uint32_t *>(smb + Y.bcnt);
     int32_t *stok = reinterpret_cast<int32_t *>(smb + Y.stok);
     uint32_t *skey = reinterpret_cast<uint32_t *>(smb + Y.skey);
-    uint8_t *kept = smb + Y.kept;
     uint16_t *kpn = reinterpret_cast<uint16_t *>(smb + Y.kpn);
-    const int LIST = NB * 32;   // capacity of stok / skey / kept
+    const int LIST = NB * 32;   // capacity of stok / skey
 
     auto tok_of = [&](int e) -> int64_t { return ((int64_t)(c + (e >> 5) * C) << 5) + (e & 31); };
 
@@ -879,7 +892,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     float *prow = a.part + (int64_t)row * C * G * (2 + DT);
     if (fast) {
         // ---- 5c. per-block kept counts of the row; the window's kept tokens
-        // -> wk; flags of the attention list (zero past its end)
+        // -> wk
 #pragma unroll
         for (int i = 0; i < kFFEntPerThread; ++i)
             if (((is_cand >> i) & 1u) && composite(ent[i].x, ent[i].y) >= T) atomicAdd(&bcnt[ent[i].y >> 5], 1u);
@@ -892,7 +905,6 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         }
         __syncthreads();
         const int n_att = n_above + (int)cnt[CN_WK];
-        for (int i = threadIdx.x; i < LIST; i += blockDim.x) kept[i] = i < n_att ? 1 : 0;
         // the first round's window rows are requested now
         const int nr0 = n_att < a.stage_cap ? n_att : a.stage_cap;
         gather_rows(0, n_r1, nr0);
@@ -915,14 +927,24 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 if (rl_v) st_shared_zero16_if(X + (size_t)s * SB + 2 * DT + rl_c * 16, true);
             cp_async_wait_all();
             __syncthreads();
-            mma_attend<DT, kFFWarps>(A, X, SB, nr, kept, r0, qsm, qscale);
+            mma_attend<DT, kFFWarps, false>(A, X, SB, nr, nullptr, 0, qsm, qscale);
         }
         // ---- 6b. combine the warps' states into this CTA's partial
         A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 1);
         A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 2);
         A.l1 += __shfl_xor_sync(0xFFFFFFFFu, A.l1, 1);
         A.l1 += __shfl_xor_sync(0xFFFFFFFFu, A.l1, 2);
-        __syncthreads();   // X is free: warp states go there
+        // the CTA's max per head: one shared atomicMax per warp and head on
+        // order-preserving keys (cnt[16 + g], zero = below every key)
+        uint32_t *mkey = cnt + 16;
+        {
+            const int g0 = lane >> 2;
+            if ((lane & 3) == 0) {
+                if (g0 < G) atomicMax(&mkey[g0], order_key(A.m0));
+                if (g0 + 8 < G) atomicMax(&mkey[g0 + 8], order_key(A.m1));
+            }
+        }
+        __syncthreads();   // (X is free: the warps' scaled states go there)
         float *ws = reinterpret_cast<float *>(X);
         const int sg = 2 + DT;
         {
@@ -931,29 +953,15 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             for (int half = 0; half < 2; ++half) {
                 const int g = g0 + 8 * half;
                 if (g < G) {
+                    const float wt = rescale_w(half ? A.m1 : A.m0, order_key_inv(mkey[g]));
                     float *w = ws + ((int64_t)warp * G + g) * sg;
-                    if ((lane & 3) == 0) {
-                        w[0] = half ? A.m1 : A.m0;
-                        w[1] = half ? A.l1 : A.l0;
-                    }
+                    if ((lane & 3) == 0) w[1] = wt * (half ? A.l1 : A.l0);
 #pragma unroll
                     for (int t = 0; t < NT; ++t)
                         *reinterpret_cast<float2 *>(w + 2 + 8 * t + d0) =
-                            make_float2(A.o[t][2 * half], A.o[t][2 * half + 1]);
+                            make_float2(wt * A.o[t][2 * half], wt * A.o[t][2 * half + 1]);
                 }
             }
-        }
-        __syncthreads();
-        // weight of warp w's state in head g: exp2(m_wg - M_g), computed once
-        // per (w, g); wts[kFFWarps G + g] = M_g
-        float *wts = ws + kFFWarps * G * sg;
-        if ((int)threadIdx.x < kFFWarps * G) {
-            const int w = threadIdx.x / G, g = threadIdx.x % G;
-            float M = -INFINITY;
-#pragma unroll
-            for (int v = 0; v < kFFWarps; ++v) M = fmaxf(M, ws[(v * G + g) * sg]);
-            wts[threadIdx.x] = rescale_w(ws[(w * G + g) * sg], M);
-            if (w == 0) wts[kFFWarps * G + g] = M;
         }
         __syncthreads();
         for (int x = threadIdx.x; x < G * DT; x += blockDim.x) {
@@ -962,13 +970,12 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
 #pragma unroll
             for (int w = 0; w < kFFWarps; ++w) {
                 const float *sw = ws + (w * G + g) * sg;
-                const float wt = wts[w * G + g];
-                L = fmaf(wt, sw[1], L);
-                Acc = fmaf(wt, sw[2 + d], Acc);
+                L += sw[1];
+                Acc += sw[2 + d];
             }
             float *o = prow + ((int64_t)c * G + g) * sg;
             if (d == 0) {
-                o[0] = wts[kFFWarps * G + g];
+                o[0] = order_key_inv(mkey[g]);
                 o[1] = L;
             }
             o[2 + d] = Acc;

@@ -110,7 +110,8 @@ def test_decode_small_per_step(fused):
 
 @pytest.mark.parametrize("B,Hq,Hkv,D,dp,N,k,agg", [(2, 8, 2, 128, 32, 5000, 500, 0), (1, 4, 4, 64, 16, 777, 1, 0),
                                                    (1, 8, 2, 128, 32, 3001, 3001, 0), (3, 6, 3, 64, 24, 2500, 99, 1),
-                                                   (1, 16, 1, 32, 8, 20000, 6000, 1), (4, 8, 8, 128, 16, 40, 7, 0)])
+                                                   (1, 16, 1, 32, 8, 20000, 6000, 1), (4, 8, 8, 128, 16, 40, 7, 0),
+                                                   (1, 16, 1, 128, 32, 20000, 2000, 0), (2, 32, 4, 64, 16, 9000, 900, 1)])
 def test_decode_fused_matches_oracle_shapes(B, Hq, Hkv, D, dp, N, k, agg):
     w = synth.small(B=B, Hq=Hq, Hkv=Hkv, D=D, dp=dp, N=N, k=k, seed=N + k, outliers=2)
     run_decode_parity(w, n0=w.N - 1, steps=2, agg=agg)
