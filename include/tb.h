@@ -12,7 +12,14 @@
  * Conventions shared by every call
  * --------------------------------
  *  - bf16 tensors travel as raw 16-bit patterns (tb_bf16). All tensor
- *    pointers are DEVICE pointers, 16-byte aligned, dense row-major.
+ *    pointers are DEVICE pointers, 16-byte aligned, dense row-major, with
+ *    one exception: K and V of tb_sparse_decode_attn and tb_decode_step may
+ *    be pinned host memory that the device reaches through unified
+ *    addressing (cudaMallocHost / cudaHostAlloc). That is the offloaded
+ *    cache of the TokenButler abstract and the gist.science summary
+ *    ("Significance"): only the selected rows (and the appended row) cross
+ *    the host link, while Kp, which every step streams whole, stays in
+ *    device memory. Same results, host-link speed.
  *  - Shapes: B batch, Hq query heads, Hkv KV heads (G = Hq/Hkv query heads
  *    share one KV head), D head dim, dp projected dim, cap cache rows.
  *      K, V  : [B, Hkv, cap, D]        Kp : [B, Hkv, cap, dp]
@@ -20,8 +27,8 @@
  *      q_imp : [B, Hq, dp]             s  : [B, Hkv, n] (fp32)
  *      idx   : [B, Hkv, k] (int32)     sel: [B, Hkv, sel_stride] (int32)
  *      out   : [B, Hq, D]
- *  - Limits: D and dp multiples of 8, D <= 256, dp <= 256, Hq % Hkv == 0,
- *    G <= 16, cap < 2^31. Violations return TB_ERR_UNSUPPORTED or
+ *  - Limits: D in {8, 16, 32, 64, 128, 256} (D/8 lanes tile a warp), dp a
+ *    multiple of 8 and <= 256, Hq % Hkv == 0, G <= 16, cap < 2^31. Violations return TB_ERR_UNSUPPORTED or
  *    TB_ERR_INVALID_ARG before anything is enqueued.
  *  - The caller owns all memory; the library allocates none. Scratch comes
  *    from a caller-provided workspace of tb_workspace_size() bytes that must

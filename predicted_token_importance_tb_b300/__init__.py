@@ -136,6 +136,18 @@ def _bf16(t, name):
     return _ptr(t)
 
 
+def _kv(t, name):
+    """K / V: a CUDA tensor, or a pinned host tensor (the offloaded cache: the device reads it through
+    unified addressing, only the selected rows cross the host link)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return ctypes.c_void_p(t.data_ptr())
+    return _bf16(t, name)
+
+
 def _i32(t, name):
     if t is not None and t.dtype != torch.int32:
         raise TypeError(f"{name} must be int32, got {t.dtype}")
@@ -230,7 +242,7 @@ def tb_expand(shape: Shape, idx, k: int, r: int, n_pred: int, n_t: int, sel, sel
 def tb_sparse_decode_attn(shape: Shape, q, K, V, sel, counts, sel_stride: int, scale: float, out, ws,
                           dev_status=None, stream=None):
     _check(load_library().tb_sparse_decode_attn(
-        ctypes.byref(shape.c()), _bf16(q, "q"), _bf16(K, "K"), _bf16(V, "V"), _i32(sel, "sel"),
+        ctypes.byref(shape.c()), _bf16(q, "q"), _kv(K, "K"), _kv(V, "V"), _i32(sel, "sel"),
         _i32(counts, "counts"), sel_stride, scale, _bf16(out, "out"), _ptr(ws), ws.numel(),
         _status_ptr(dev_status), _stream(stream)), "tb_sparse_decode_attn")
 
@@ -242,7 +254,7 @@ def tb_decode_step(shape: Shape, k: int, T: int, r: int, agg: int, scale: float,
     params = _StepParams(k, T, r, agg, scale, flags)
     _check(load_library().tb_decode_step(
         ctypes.byref(shape.c()), ctypes.byref(params), t, n, _bf16(q, "q"), _bf16(q_imp, "q_imp"),
-        _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"), _bf16(K, "K"), _bf16(V, "V"),
+        _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"), _kv(K, "K"), _kv(V, "V"),
         _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.byref(n_pred), _i32(sel, "sel"), sel_stride,
         _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), ws.numel(), _status_ptr(dev_status),
         _stream(stream)), "tb_decode_step")

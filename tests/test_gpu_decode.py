@@ -22,14 +22,15 @@ def _lib():
 
 
 def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=None, fused=True, agg=0,
-                      layer_hook=None):
+                      layer_hook=None, kv_host=False):
     """Drive `steps` decode steps per layer on the GPU and check every step against the oracle.
 
     The oracle starts from the GPU-projected prefix of Kp (identical inputs),
     projects each appended row itself, and makes its own selections; top-k
     sets are compared under the tie band, the selection rows exactly against
     the oracle's expansion of the GPU's prediction, and the output against the
-    oracle's attention over the GPU's selection.
+    oracle's attention over the GPU's selection. kv_host: K and V live in
+    pinned host memory (the offloaded cache).
     """
     k = w.k if k is None else k
     cap = n0 + steps
@@ -42,6 +43,8 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
         K, V, Wk = L["K"].cuda(), L["V"].cuda(), L["Wk"].cuda()
         Kp = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
         tb.tb_project_append(shape, K, cap, Wk, Kp, 0, n0)
+        if kv_host:
+            K, V = K.cpu().pin_memory(), V.cpu().pin_memory()
         dec = tb.DecodeLayer(shape, k, T=w.T, r=w.r, agg=agg, scale=w.scale, n_max=cap - 1, fused=fused)
         out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
         oK, oV = u16(L["K"]).copy(), u16(L["V"]).copy()
