@@ -50,6 +50,8 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--rotate", type=int, default=0, help="cache copies to rotate over (0: enough to defeat L2)")
+    ap.add_argument("--agg", default="mean", choices=["mean", "max"],
+                    help="how the G query heads' scores combine (mean: the default reading)")
     ap.add_argument("--offload", action="store_true",
                     help="K/V in pinned host memory (the offloaded cache); prints its own line")
     return ap.parse_args()
@@ -273,7 +275,8 @@ def run_ours(args, w):
     Kps = [Kp0] + [Kp0.clone() for _ in range(R - 1)]
     steps_in = [synth.make_step(w, 0, i, L["outlier_ch"]) for i in range(R)]
     dins = [{k: v.cuda() for k, v in d.items()} for d in steps_in]
-    dec = tb.DecodeLayer(shape, w.k, T=1, r=0, scale=w.scale, n_max=n0)
+    agg = tb.TB_AGG_MAX if args.agg == "max" else tb.TB_AGG_MEAN
+    dec = tb.DecodeLayer(shape, w.k, T=1, r=0, agg=agg, scale=w.scale, n_max=n0)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
 
     def step(i):
@@ -358,7 +361,7 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "dp": w.dp, "N": w.N,
-                       "k": w.k, "T": 1, "r": 0, "rotation_sets": R,
+                       "k": w.k, "T": 1, "r": 0, "agg": args.agg, "rotation_sets": R,
                        "l2_defeat": f"inputs rotate over {R} cache copies ({R * step_bytes / 1e6:.0f} MB touched per "
                                     f"rotation, L2 {l2 / 1e6:.0f} MB)",
                        "parallelism": f"replicas x{world}"},

@@ -94,6 +94,12 @@ typedef struct {
 /* tb_step_params.flags: run the step as separate kernels even where the
    single fused launch applies (same results; for comparison and debugging). */
 #define TB_STEP_UNFUSED 1
+/* tb_step_params.flags: budget-preserving neighbour fetching (a variant of
+   the gist.science summary's Neighbor Fetching, Optimizations): a prediction
+   keeps kc = max(1, k / (2r + 1)) centres instead of k, so the widened
+   selection holds at most k tokens (plus the tail). idx_state then holds kc
+   entries per row, packed ([B, Hkv, kc]). With r == 0 it changes nothing. */
+#define TB_STEP_BUDGET_NEIGHBOURS 2
 
 /* Text for a status code (static storage). */
 TB_API const char *tb_status_string(tb_status st);
@@ -192,7 +198,8 @@ TB_API tb_status tb_sparse_decode_attn(const tb_shape *shape, const tb_bf16 *q, 
  *   3. out = attention of q over sel.
  * K_new, V_new: [B, Hkv, D]. idx_state [B,Hkv,k], sel [B,Hkv,sel_stride] and
  * counts [B,Hkv] persist across the steps of an interval; sel_stride must be
- * >= min(n+1, k(2r+1)) + T - 1. The steps of an interval must be issued in
+ * >= min(n+1, kc(2r+1)) + T - 1, kc = k (or k / (2r+1), at least 1, with
+ * TB_STEP_BUDGET_NEIGHBOURS). The steps of an interval must be issued in
  * order with consecutive t and n. With T == 1 and r == 0 the whole step runs
  * as one fused kernel.
  */

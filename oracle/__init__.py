@@ -232,8 +232,17 @@ class DecodeState:
         self.n_pred = 0      # tokens present when it was made
 
 
+def centres(k: int, r: int, budget_neighbours: bool) -> int:
+    """Tokens a prediction keeps before widening: k, or with budget-preserving
+    neighbour fetching k // (2r + 1) (at least one), so that the widened
+    selection stays within k. Reading of the summary's Neighbor Fetching
+    (Optimizations): it names no budget rule; this variant is the plainest
+    one that keeps |E| <= k (parity unpinned by the pages)."""
+    return max(1, k // (2 * r + 1)) if budget_neighbours else k
+
+
 def decode_step(state: DecodeState, t: int, n: int, *, q, q_imp, K_new, V_new, Wk,
-                K, V, Kp, k: int, T: int, r: int, agg: int, scale: float):
+                K, V, Kp, k: int, T: int, r: int, agg: int, scale: float, budget_neighbours: bool = False):
     """One decode step of one layer, on CPU copies of the caches (updated in place).
 
     [summary] Optimizations: the predictor runs once every T steps, its
@@ -255,7 +264,7 @@ def decode_step(state: DecodeState, t: int, n: int, *, q, q_imp, K_new, V_new, W
     n_t = n + 1
     if t % T == 0:
         s, _ = score(q_imp, np.ascontiguousarray(Kp[:, :, :n_t, :]), agg)
-        state.idx = topk(s, k)
+        state.idx = topk(s, centres(k, r, budget_neighbours))
         state.n_pred = n_t
     sel, counts = expand(state.idx, r, state.n_pred, n_t)
     out = attn(q, K, V, sel, counts, scale)

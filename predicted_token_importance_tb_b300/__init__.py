@@ -32,6 +32,7 @@ TB_AGG_MEAN = 0
 TB_AGG_MAX = 1
 
 TB_STEP_UNFUSED = 1
+TB_STEP_BUDGET_NEIGHBOURS = 2
 
 EXPORTED = (
     "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
@@ -269,19 +270,22 @@ class DecodeLayer:
     """Per-layer decode state on the device: the selection reused across a prediction interval."""
 
     def __init__(self, shape: Shape, k: int, T: int = 1, r: int = 0, agg: int = TB_AGG_MEAN,
-                 scale: float | None = None, n_max: int | None = None, device=None, fused: bool = True):
+                 scale: float | None = None, n_max: int | None = None, device=None, fused: bool = True,
+                 budget_neighbours: bool = False):
         self.shape, self.k, self.T, self.r, self.agg = shape, k, T, r, agg
-        self.flags = 0 if fused else TB_STEP_UNFUSED
+        self.flags = (0 if fused else TB_STEP_UNFUSED) | (TB_STEP_BUDGET_NEIGHBOURS if budget_neighbours else 0)
+        # centres kept per prediction (idx_state row length)
+        self.kc = max(1, k // (2 * r + 1)) if budget_neighbours else k
         self.scale = scale if scale is not None else shape.D ** -0.5
         n_max = shape.cap - 1 if n_max is None else n_max
         dev = device or "cuda"
         rows = (shape.B, shape.Hkv)
-        self.sel_stride = sel_stride_for(k, T, r, n_max)
-        self.idx_state = torch.zeros(rows + (k,), dtype=torch.int32, device=dev)
+        self.sel_stride = sel_stride_for(self.kc, T, r, n_max)
+        self.idx_state = torch.zeros(rows + (self.kc,), dtype=torch.int32, device=dev)
         self.sel = torch.zeros(rows + (self.sel_stride,), dtype=torch.int32, device=dev)
         self.counts = torch.zeros(rows, dtype=torch.int32, device=dev)
         self.n_pred = ctypes.c_int64(0)
-        self.ws = workspace(shape, n_max, k, self.sel_stride, device=dev)
+        self.ws = workspace(shape, n_max, max(k, self.kc), self.sel_stride, device=dev)
         self.status = dev_status(dev)
 
     def step(self, t: int, n: int, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, out, stream=None):

@@ -179,12 +179,17 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     TB_PTR(V);
     TB_PTR(Kp);
     TB_PTR(out);
+    if (p->flags & ~(TB_STEP_UNFUSED | TB_STEP_BUDGET_NEIGHBOURS)) return TB_ERR_INVALID_ARG;
     const int64_t n_t = n + 1;
     const bool predict = (t % p->T) == 0;
-    if (predict && p->k > n_t) return TB_ERR_INVALID_ARG;
+    // centres per prediction: k, or k / (2r + 1) (at least one) when the
+    // widened selection must stay within the budget
+    const int32_t kc = (p->flags & TB_STEP_BUDGET_NEIGHBOURS) ? (p->k / (2 * p->r + 1) > 0 ? p->k / (2 * p->r + 1) : 1)
+                                                              : p->k;
+    if (predict && kc > n_t) return TB_ERR_INVALID_ARG;
     if (!predict && (*n_pred <= 0 || *n_pred > n)) return TB_ERR_INVALID_ARG;   // a step of this interval is missing
     const int64_t np = predict ? n_t : *n_pred;
-    int64_t body = (int64_t)p->k * (2 * (int64_t)p->r + 1);
+    int64_t body = (int64_t)kc * (2 * (int64_t)p->r + 1);
     if (body > np) body = np;
     if ((int64_t)sel_stride < body + (n_t - np)) return TB_ERR_INVALID_ARG;
     const int rows = shape->B * shape->Hkv;
@@ -234,9 +239,9 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
             e = launch_topk(rows, scores, n_t, n_t, p->k, idx_state, ctl, dev_status, stream, sel, sel_stride, counts);
             if (e != cudaSuccess) return from_cuda(e);
         } else {
-            e = launch_topk(rows, scores, n_t, n_t, p->k, idx_state, ctl, dev_status, stream);
+            e = launch_topk(rows, scores, n_t, n_t, kc, idx_state, ctl, dev_status, stream);
             if (e != cudaSuccess) return from_cuda(e);
-            e = launch_expand(rows, idx_state, p->k, p->r, n_t, n_t, sel, sel_stride, counts, dev_status, stream);
+            e = launch_expand(rows, idx_state, kc, p->r, n_t, n_t, sel, sel_stride, counts, dev_status, stream);
             if (e != cudaSuccess) return from_cuda(e);
         }
         *n_pred = n_t;

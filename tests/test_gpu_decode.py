@@ -22,7 +22,7 @@ def _lib():
 
 
 def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=None, fused=True, agg=0,
-                      layer_hook=None, kv_host=False):
+                      layer_hook=None, kv_host=False, budget_neighbours=False):
     """Drive `steps` decode steps per layer on the GPU and check every step against the oracle.
 
     The oracle starts from the GPU-projected prefix of Kp (identical inputs),
@@ -30,7 +30,8 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
     sets are compared under the tie band, the selection rows exactly against
     the oracle's expansion of the GPU's prediction, and the output against the
     oracle's attention over the GPU's selection. kv_host: K and V live in
-    pinned host memory (the offloaded cache).
+    pinned host memory (the offloaded cache). budget_neighbours: k // (2r+1)
+    centres per prediction.
     """
     k = w.k if k is None else k
     cap = n0 + steps
@@ -45,7 +46,8 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
         tb.tb_project_append(shape, K, cap, Wk, Kp, 0, n0)
         if kv_host:
             K, V = K.cpu().pin_memory(), V.cpu().pin_memory()
-        dec = tb.DecodeLayer(shape, k, T=w.T, r=w.r, agg=agg, scale=w.scale, n_max=cap - 1, fused=fused)
+        dec = tb.DecodeLayer(shape, k, T=w.T, r=w.r, agg=agg, scale=w.scale, n_max=cap - 1, fused=fused,
+                             budget_neighbours=budget_neighbours)
         out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
         oK, oV = u16(L["K"]).copy(), u16(L["V"]).copy()
         oKp = u16(Kp).copy()
@@ -59,7 +61,7 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
             tb.check_dev_status(dec.status, f"layer {layer} step {t}")
             ref_out, ref_sel, ref_cnt = oracle.decode_step(
                 st, t, n, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=L["Wk"], K=oK, V=oV,
-                Kp=oKp, k=k, T=w.T, r=w.r, agg=agg, scale=w.scale)
+                Kp=oKp, k=k, T=w.T, r=w.r, agg=agg, scale=w.scale, budget_neighbours=budget_neighbours)
             # appended rows
             gKp = u16(Kp[:, :, n])[:, :, None]
             kn = np.ascontiguousarray(oK[:, :, n:n + 1])
@@ -71,7 +73,7 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
             gidx = dec.idx_state.cpu().numpy()
             if t % w.T == 0:
                 s_ref, _ = oracle.score(d["q_imp"], np.ascontiguousarray(oKp[:, :, :n_t]), agg)
-                assert_topk_end_to_end(gidx, s_ref, k)
+                assert_topk_end_to_end(gidx, s_ref, dec.kc)
             # selection = the oracle's expansion of the GPU's prediction, plus the tail
             want_sel, want_cnt = oracle.expand(gidx, w.r, st.n_pred, n_t, sel_stride=dec.sel_stride)
             gcnt = dec.counts.cpu().numpy()
@@ -195,3 +197,11 @@ def test_decode_32layer_stack_interval_sampled_layers():
     # the 32-layer B=8 stack at full per-layer shape: layers 0 and 31, all 64 steps
     w = synth.WORKLOADS[2]
     run_decode_parity(w, n0=w.N, steps=w.steps, layers=(0, 31))
+
+
+def test_decode_budget_preserving_neighbours():
+    # k // (2r + 1) centres widened by +-r: the selection stays within the budget
+    w = synth.small(B=2, Hq=8, Hkv=2, D=128, dp=32, N=4000, k=300, T=3, r=2, seed=33, outliers=2)
+    dec = run_decode_parity(w, n0=w.N, steps=5, budget_neighbours=True)
+    assert dec.kc == 60
+    assert int(dec.counts.max().item()) <= w.k + w.T - 1

@@ -329,7 +329,7 @@ def test_planted_heavy_hitters_are_selected():
 
 # ------------------------------------------------------------------ decode steps
 
-def _run_steps(w, T, r, steps, k):
+def _run_steps(w, T, r, steps, k, budget_neighbours=False):
     L = synth.make_layer(w, cap=w.N + steps, n=w.N)
     K = oracle.as_u16(L["K"]).copy()
     V = oracle.as_u16(L["V"]).copy()
@@ -341,7 +341,7 @@ def _run_steps(w, T, r, steps, k):
         d = synth.make_step(w, 0, t, L["outlier_ch"])
         out, sel, cnt = oracle.decode_step(st, t, w.N + t, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"],
                                            V_new=d["V_new"], Wk=L["Wk"], K=K, V=V, Kp=Kp, k=k, T=T, r=r,
-                                           agg=oracle.AGG_MEAN, scale=w.scale)
+                                           agg=oracle.AGG_MEAN, scale=w.scale, budget_neighbours=budget_neighbours)
         outs.append((out, sel, cnt, st.idx.copy(), st.n_pred))
     return outs, (K, V, Kp, L)
 
@@ -372,3 +372,30 @@ def test_decode_interval_reuse_superset_and_tail():
             assert s[len(s) - (n_t - n_pred):] == list(range(n_pred, n_t))
             body = len(s) - (n_t - n_pred)
             assert k <= body <= min(n_pred, k * (2 * r + 1))
+
+
+def test_budget_preserving_neighbours_centres_and_bound():
+    # k // (2r + 1) centres (at least one); r = 0 keeps k
+    assert [oracle.centres(9, 1, True), oracle.centres(9, 0, True), oracle.centres(2, 2, True),
+            oracle.centres(9, 1, False)] == [3, 9, 1, 9]
+    w = synth.small(B=1, Hq=4, Hkv=2, D=16, dp=8, N=160, seed=13)
+    T, r, k = 3, 2, 25
+    kc = k // (2 * r + 1)
+    outs, (K, V, Kp, L) = _run_steps(w, T=T, r=r, steps=6, k=k, budget_neighbours=True)
+    for t, (out, sel, cnt, idx, n_pred) in enumerate(outs):
+        n_t = w.N + t + 1
+        assert idx.shape[-1] == kc
+        if t % T == 0:
+            # the centres are the top kc by a brute-force rank count on the step's own scores
+            d = synth.make_step(w, 0, t, L["outlier_ch"])
+            s_, _ = oracle.score(d["q_imp"], np.ascontiguousarray(Kp[:, :, :n_t]))
+            for b, h in itertools.product(range(w.B), range(w.Hkv)):
+                v = s_[b, h]
+                rank = [sum(1 for j in range(n_t) if (v[j], -j) > (v[i], -i)) for i in range(n_t)]
+                assert idx[b, h].tolist() == [i for i in range(n_t) if rank[i] < kc]
+        for b, h in itertools.product(range(w.B), range(w.Hkv)):
+            s = sel[b, h, : cnt[b, h]].tolist()
+            body = s[: len(s) - (n_t - n_pred)]
+            want = sorted({j for i in idx[b, h].tolist() for j in range(i - r, i + r + 1) if 0 <= j < n_pred})
+            assert body == want
+            assert kc <= len(body) <= k                                  # within the budget
