@@ -211,6 +211,49 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Sink and local-window buffers ("TokenButler: Token Importance is
+ * Predictable", gist.science summary, Inference Strategy: the first S tokens
+ * and a window of the newest tokens are always kept, the important tokens
+ * come from the predictor; Optimizations, Batching: keys are projected in
+ * batches of W tokens instead of at every step).
+ */
+typedef struct {
+    int32_t sink;     /* S >= 0: tokens [0, S) are always attended */
+    int32_t window;   /* W >= 1: at least the newest W tokens are always attended; Kp grows in batches of W */
+} tb_buffer_params;
+
+/*
+ * One decode step of one layer with the three buffers. With n_t = n + 1:
+ *   1. append: K[.,.,n] = K_new, V[.,.,n] = V_new (no projection here)
+ *   2. if t % T == 0:
+ *        P = *proj_end + W * floor((n_t - W - *proj_end) / W) if that adds a
+ *        batch: Kp[., ., *proj_end : P) = RNE(K rows . Wk) in one launch,
+ *        *proj_end = P; then the candidates [S, P) are scored, the top kc
+ *        kept in idx_state (kc = k, or the TB_STEP_BUDGET_NEIGHBOURS count,
+ *        at most P - S; indices relative to S) and
+ *          sel = [0, min(S, n_t)) ++ widen(idx + S, r) within [S, P)
+ *                ++ [max(P, min(S, n_t)), n_t),
+ *        *n_pred = n_t
+ *      else sel += [n]
+ *   3. out = attention of q over sel.
+ * So the window holds the tokens since the last batch, W to 2W - 1 of them
+ * at a prediction (plus the steps of the interval). *proj_end (host scalar)
+ * is the number of rows Kp holds; start it at the rows projected before
+ * (for instance by tb_project_append at prefill). sel_stride must be at least
+ * min(S, n_t) + min(P - S, kc (2r+1)) + (n_t - max(P, min(S, n_t))) + T - 1
+ * at every prediction (else TB_ERR_INVALID_ARG). params->flags may hold
+ * TB_STEP_BUDGET_NEIGHBOURS; the step always runs as separate kernels.
+ * Pointers and layouts as for tb_decode_step.
+ */
+TB_API tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *params,
+                                         const tb_buffer_params *buffers, int64_t t, int64_t n, const tb_bf16 *q,
+                                         const tb_bf16 *q_imp, const tb_bf16 *K_new, const tb_bf16 *V_new,
+                                         const tb_bf16 *Wk, tb_bf16 *K, tb_bf16 *V, tb_bf16 *Kp,
+                                         int32_t *idx_state, int64_t *n_pred, int64_t *proj_end, int32_t *sel,
+                                         int32_t sel_stride, int32_t *counts, tb_bf16 *out, void *ws,
+                                         size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/*
  * tb_topk without a workspace. The paper has no counterpart to this call; it
  * exists for callers that cannot allocate device memory at all, so cannot
  * hand tb_topk its scratch: code embedded in a host runtime that owns every

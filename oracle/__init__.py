@@ -269,3 +269,81 @@ def decode_step(state: DecodeState, t: int, n: int, *, q, q_imp, K_new, V_new, W
     sel, counts = expand(state.idx, r, state.n_pred, n_t)
     out = attn(q, K, V, sel, counts, scale)
     return out, sel, counts
+
+
+def buffered_select(idx, r: int, sink: int, proj_end: int, n_t: int) -> list:
+    """Selection rows of the buffered step: the sink [0, min(S, n_t)), the
+    windows [S+i-r, S+i+r] of the centres idx (relative to S) clipped to
+    [S, proj_end), then the local window [max(proj_end, min(S, n_t)), n_t).
+    idx [B, Hkv, kc] -> list of B*Hkv ascending lists."""
+    idx = np.asarray(idx)
+    S, P = int(sink), int(proj_end)
+    pre = min(S, n_t)
+    tail0 = max(P, pre)
+    rows = []
+    for b in range(idx.shape[0]):
+        for h in range(idx.shape[1]):
+            body = set()
+            for i in idx[b, h].tolist():
+                body.update(j for j in range(S + i - r, S + i + r + 1) if S <= j < P)
+            rows.append(list(range(pre)) + sorted(body) + list(range(tail0, n_t)))
+    return rows
+
+
+class BufferedState(DecodeState):
+    """Host-side state of the buffered step: also the number of rows Kp holds."""
+
+    def __init__(self, proj_end: int):
+        super().__init__()
+        self.proj_end = int(proj_end)
+
+
+def decode_step_buffered(state: BufferedState, t: int, n: int, *, q, q_imp, K_new, V_new, Wk, K, V, Kp,
+                         k: int, T: int, r: int, agg: int, scale: float, sink: int, window: int,
+                         budget_neighbours: bool = False):
+    """One decode step with sink and local-window buffers.
+
+    [summary] Inference Strategy: the first S tokens (sink) and a window of
+    the newest tokens are always kept, the important buffer is filled from
+    the predicted scores; Optimizations, Batching: keys are projected in
+    batches of W tokens instead of at every step. Readings: the window is the
+    tokens not yet projected; at a prediction step every whole batch of W
+    tokens older than the newest W is projected first, so the window then
+    holds W to 2W - 1 tokens; the important tokens are chosen among
+    [S, proj_end) and widened by +-r inside that range; between predictions
+    the new tokens join the selection (they are the window's newest).
+    Returns (out fp64 [B,Hq,D], sel, counts).
+    """
+    K_new = as_u16(K_new)
+    V_new = as_u16(V_new)
+    K[:, :, n, :] = K_new
+    V[:, :, n, :] = V_new
+    n_t = n + 1
+    S, W = int(sink), int(window)
+    if t % T == 0:
+        P = state.proj_end
+        while n_t - W - P >= W:
+            Kp[:, :, P:P + W, :], _ = project(np.ascontiguousarray(K[:, :, P:P + W, :]), Wk)
+            P += W
+        state.proj_end = P
+        nc = max(0, P - S)
+        kc = min(centres(k, r, budget_neighbours), nc)
+        if kc > 0:
+            s, _ = score(q_imp, np.ascontiguousarray(Kp[:, :, S:P, :]), agg)
+            idx = topk(s, kc)                                   # relative to S
+        else:
+            idx = np.zeros(K.shape[:2] + (0,), dtype=np.int32)
+        state.idx = idx
+        state.n_pred = n_t
+        state.sel_rows = buffered_select(idx, r, S, P, n_t)
+    else:
+        state.sel_rows = [row + [n] for row in state.sel_rows]
+    B, Hkv = K.shape[:2]
+    width = max(len(x) for x in state.sel_rows)
+    sel = np.full((B, Hkv, width), -1, dtype=np.int32)
+    counts = np.empty((B, Hkv), dtype=np.int32)
+    for x, row in enumerate(state.sel_rows):
+        sel[x // Hkv, x % Hkv, :len(row)] = row
+        counts[x // Hkv, x % Hkv] = len(row)
+    out = attn(q, K, V, sel, counts, scale)
+    return out, sel, counts

@@ -37,6 +37,7 @@ TB_STEP_BUDGET_NEIGHBOURS = 2
 EXPORTED = (
     "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
     "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step", "tb_topk_noalloc",
+    "tb_decode_step_buffered",
 )
 
 TB_TOPK_NOALLOC_MAX_ROWS = 64
@@ -56,6 +57,10 @@ class _Shape(ctypes.Structure):
 class _StepParams(ctypes.Structure):
     _fields_ = [("k", ctypes.c_int32), ("T", ctypes.c_int32), ("r", ctypes.c_int32),
                 ("agg", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_int32)]
+
+
+class _BufferParams(ctypes.Structure):
+    _fields_ = [("sink", ctypes.c_int32), ("window", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -100,6 +105,9 @@ def load_library(path: str = LIB_PATH):
         lib.tb_sparse_decode_attn.argtypes = [SP, P, P, P, P, P, i32, f32, P, P, sz, P, P]
         lib.tb_decode_step.argtypes = [SP, ctypes.POINTER(_StepParams), i64, i64, P, P, P, P, P, P, P, P, P,
                                        ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
+        lib.tb_decode_step_buffered.argtypes = [SP, ctypes.POINTER(_StepParams), ctypes.POINTER(_BufferParams), i64,
+                                                i64, P, P, P, P, P, P, P, P, P, ctypes.POINTER(i64),
+                                                ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
         for name in EXPORTED:
             if name != "tb_status_string" and name != "tb_version":
                 getattr(lib, name).restype = ctypes.c_int
@@ -261,6 +269,22 @@ def tb_decode_step(shape: Shape, k: int, T: int, r: int, agg: int, scale: float,
         _stream(stream)), "tb_decode_step")
 
 
+def tb_decode_step_buffered(shape: Shape, k: int, T: int, r: int, agg: int, scale: float, sink: int, window: int,
+                            t: int, n: int, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state,
+                            n_pred: "ctypes.c_int64", proj_end: "ctypes.c_int64", sel, sel_stride: int, counts, out,
+                            ws, dev_status=None, stream=None, flags: int = 0):
+    """One decode step with sink and local-window buffers (see include/tb.h). n_pred and proj_end are
+    ctypes.c_int64 carried across steps."""
+    params = _StepParams(k, T, r, agg, scale, flags)
+    bufs = _BufferParams(sink, window)
+    _check(load_library().tb_decode_step_buffered(
+        ctypes.byref(shape.c()), ctypes.byref(params), ctypes.byref(bufs), t, n, _bf16(q, "q"), _bf16(q_imp, "q_imp"),
+        _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"), _kv(K, "K"), _kv(V, "V"),
+        _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.byref(n_pred), ctypes.byref(proj_end),
+        _i32(sel, "sel"), sel_stride, _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), ws.numel(),
+        _status_ptr(dev_status), _stream(stream)), "tb_decode_step_buffered")
+
+
 def sel_stride_for(k: int, T: int, r: int, n_max: int) -> int:
     """Selection row length that every step of an interval fits in."""
     return min(n_max + 1, k * (2 * r + 1)) + T - 1
@@ -293,4 +317,39 @@ class DecodeLayer:
                        K_new=K_new, V_new=V_new, Wk=Wk, K=K, V=V, Kp=Kp, idx_state=self.idx_state,
                        n_pred=self.n_pred, sel=self.sel, sel_stride=self.sel_stride, counts=self.counts, out=out,
                        ws=self.ws, dev_status=self.status, stream=stream, flags=self.flags)
+        return out
+
+
+class BufferedDecodeLayer:
+    """Per-layer decode state with sink and local-window buffers: Kp grows in batches of `window` rows
+    (proj_end counts them; pass the rows projected at prefill), the predictor picks the important tokens
+    among [sink, proj_end)."""
+
+    def __init__(self, shape: Shape, k: int, sink: int, window: int, proj_end: int, T: int = 1, r: int = 0,
+                 agg: int = TB_AGG_MEAN, scale: float | None = None, n_max: int | None = None, device=None,
+                 budget_neighbours: bool = False):
+        self.shape, self.k, self.T, self.r, self.agg = shape, k, T, r, agg
+        self.sink, self.window = sink, window
+        self.flags = TB_STEP_BUDGET_NEIGHBOURS if budget_neighbours else 0
+        self.kc = max(1, k // (2 * r + 1)) if budget_neighbours else k
+        self.scale = scale if scale is not None else shape.D ** -0.5
+        n_max = shape.cap - 1 if n_max is None else n_max
+        dev = device or "cuda"
+        rows = (shape.B, shape.Hkv)
+        # sink + widened centres + window (up to 2W - 1 at a prediction) + the interval's steps
+        self.sel_stride = min(n_max + 1, sink + min(n_max + 1, self.kc * (2 * r + 1)) + 2 * window + T)
+        self.idx_state = torch.zeros(rows + (self.kc,), dtype=torch.int32, device=dev)
+        self.sel = torch.zeros(rows + (self.sel_stride,), dtype=torch.int32, device=dev)
+        self.counts = torch.zeros(rows, dtype=torch.int32, device=dev)
+        self.n_pred = ctypes.c_int64(0)
+        self.proj_end = ctypes.c_int64(proj_end)
+        self.ws = workspace(shape, n_max, max(k, self.kc), self.sel_stride, device=dev)
+        self.status = dev_status(dev)
+
+    def step(self, t: int, n: int, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, out, stream=None):
+        tb_decode_step_buffered(self.shape, self.k, self.T, self.r, self.agg, self.scale, self.sink, self.window,
+                                t, n, q=q, q_imp=q_imp, K_new=K_new, V_new=V_new, Wk=Wk, K=K, V=V, Kp=Kp,
+                                idx_state=self.idx_state, n_pred=self.n_pred, proj_end=self.proj_end, sel=self.sel,
+                                sel_stride=self.sel_stride, counts=self.counts, out=out, ws=self.ws,
+                                dev_status=self.status, stream=stream, flags=self.flags)
         return out

@@ -3,7 +3,8 @@
 // Importance is Predictable", gist.science summary, Core Architecture,
 // Key-Cache Projection). One CTA per (b, h); thread j < dp accumulates output
 // j over a slice of D, the slices are summed in shared memory (fp32), then
-// rounded once to bf16.
+// rounded once to bf16. With Kp == nullptr only the K/V rows are written (the
+// buffered step projects in batches instead).
 #include "tb_internal.cuh"
 #include "kernels.cuh"
 
@@ -32,28 +33,30 @@ append_kernel(const uint16_t *__restrict__ K_new, const uint16_t *__restrict__ V
         Vrow[d] = vn[d];
     }
     __syncthreads();
-    const uint16_t *W = Wk + (int64_t)h * D * dp;
-    uint16_t *kp = Kp + ((int64_t)row * cap + pos) * dp;
-    // outputs j in [j0, j0 + jn) at a time; the threads split D among them
-    const int slices = blockDim.x / (dp < (int)blockDim.x ? dp : (int)blockDim.x);
-    for (int j0 = 0; j0 < dp; j0 += blockDim.x / slices) {
-        const int jn = blockDim.x / slices;
-        const int j = j0 + (int)threadIdx.x % jn;
-        const int sl = (int)threadIdx.x / jn;
-        const int dlen = (D + slices - 1) / slices;
-        float a = 0.f;
-        if (j < dp) {
-            const int d0 = sl * dlen, d1 = min(D, d0 + dlen);
-            for (int d = d0; d < d1; ++d) a = fmaf(knew[d], bf16_to_f(W[(int64_t)d * dp + j]), a);
+    if (Kp != nullptr) {   // (uniform)
+        const uint16_t *W = Wk + (int64_t)h * D * dp;
+        uint16_t *kp = Kp + ((int64_t)row * cap + pos) * dp;
+        // outputs j in [j0, j0 + jn) at a time; the threads split D among them
+        const int slices = blockDim.x / (dp < (int)blockDim.x ? dp : (int)blockDim.x);
+        for (int j0 = 0; j0 < dp; j0 += blockDim.x / slices) {
+            const int jn = blockDim.x / slices;
+            const int j = j0 + (int)threadIdx.x % jn;
+            const int sl = (int)threadIdx.x / jn;
+            const int dlen = (D + slices - 1) / slices;
+            float a = 0.f;
+            if (j < dp) {
+                const int d0 = sl * dlen, d1 = min(D, d0 + dlen);
+                for (int d = d0; d < d1; ++d) a = fmaf(knew[d], bf16_to_f(W[(int64_t)d * dp + j]), a);
+            }
+            part[threadIdx.x] = a;
+            __syncthreads();
+            if (sl == 0 && j < dp) {
+                float tot = 0.f;
+                for (int x = 0; x < slices; ++x) tot += part[x * jn + (int)threadIdx.x % jn];
+                kp[j] = f_to_bf16(tot);
+            }
+            __syncthreads();
         }
-        part[threadIdx.x] = a;
-        __syncthreads();
-        if (sl == 0 && j < dp) {
-            float tot = 0.f;
-            for (int x = 0; x < slices; ++x) tot += part[x * jn + (int)threadIdx.x % jn];
-            kp[j] = f_to_bf16(tot);
-        }
-        __syncthreads();
     }
     if (sel && threadIdx.x == 0) {
         const int32_t c = counts[row];

@@ -20,6 +20,12 @@ cudaError_t launch_topk(int rows, const float *s, int64_t lds, int64_t n, int32_
 
 cudaError_t launch_expand(int rows, const int32_t *idx, int32_t k, int32_t r, int64_t n_pred, int64_t n_t,
                           int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status, cudaStream_t st);
+// sel row = [0, prefix_end) ++ windows of (idx + idx_off) clipped to
+// [body_lo, body_hi) ++ [tail_start, n_t) (ranges disjoint and ascending).
+cudaError_t launch_expand_ranges(int rows, const int32_t *idx, int32_t k, int32_t r, int64_t idx_off,
+                                 int64_t prefix_end, int64_t body_lo, int64_t body_hi, int64_t tail_start,
+                                 int64_t n_t, int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status,
+                                 cudaStream_t st);
 
 cudaError_t launch_attn(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
                         const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale, uint16_t *out,

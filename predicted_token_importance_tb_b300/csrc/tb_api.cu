@@ -251,4 +251,79 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     return from_cuda(e);
 }
 
+tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *p, const tb_buffer_params *bp,
+                                  int64_t t, int64_t n, const tb_bf16 *q, const tb_bf16 *q_imp,
+                                  const tb_bf16 *K_new, const tb_bf16 *V_new, const tb_bf16 *Wk, tb_bf16 *K,
+                                  tb_bf16 *V, tb_bf16 *Kp, int32_t *idx_state, int64_t *n_pred, int64_t *proj_end,
+                                  int32_t *sel, int32_t sel_stride, int32_t *counts, tb_bf16 *out, void *ws,
+                                  size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    TB_CHECK(check_shape(shape));
+    if (!p || !bp || !n_pred || !proj_end || !idx_state || !sel || !counts) return TB_ERR_INVALID_ARG;
+    if (p->T < 1 || p->r < 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
+    if (p->flags & ~(TB_STEP_UNFUSED | TB_STEP_BUDGET_NEIGHBOURS)) return TB_ERR_INVALID_ARG;
+    if (bp->sink < 0 || bp->window < 1) return TB_ERR_INVALID_ARG;
+    if (t < 0 || n < 0 || n + 1 > shape->cap) return TB_ERR_INVALID_ARG;
+    if (*proj_end < 0 || *proj_end > n) return TB_ERR_INVALID_ARG;
+    TB_PTR(q);
+    TB_PTR(q_imp);
+    TB_PTR(K_new);
+    TB_PTR(V_new);
+    TB_PTR(Wk);
+    TB_PTR(K);
+    TB_PTR(V);
+    TB_PTR(Kp);
+    TB_PTR(out);
+    const int64_t n_t = n + 1, S = bp->sink, W = bp->window;
+    const bool predict = (t % p->T) == 0;
+    if (!predict && (*n_pred <= 0 || *n_pred > n)) return TB_ERR_INVALID_ARG;   // a step of this interval is missing
+    const int32_t kc0 = (p->flags & TB_STEP_BUDGET_NEIGHBOURS) ? (p->k / (2 * p->r + 1) > 0 ? p->k / (2 * p->r + 1) : 1)
+                                                               : p->k;
+    // batches that have left the window, and the ranges of the selection
+    int64_t P = *proj_end;
+    if (predict && n_t - W - P >= W) P += W * ((n_t - W - P) / W);
+    const int64_t nc = P > S ? P - S : 0;                       // candidates [S, P)
+    const int32_t kc = predict ? (int32_t)(nc < kc0 ? nc : kc0) : 0;
+    const int64_t pre = S < n_t ? S : n_t;                      // sink prefix [0, pre)
+    const int64_t tail0 = P > pre ? P : pre;                     // window [tail0, n_t)
+    if (predict) {
+        int64_t body = (int64_t)kc * (2 * (int64_t)p->r + 1);
+        if (body > nc) body = nc;
+        if ((int64_t)sel_stride < pre + body + (n_t - tail0) + (p->T - 1)) return TB_ERR_INVALID_ARG;
+    }
+    const int rows = shape->B * shape->Hkv;
+    const WsLayout L = layout_for(*shape, n_t, sel_stride, 0);
+    if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    RowCtl *ctl = reinterpret_cast<RowCtl *>(w + L.rowctl_off);
+    uint32_t *actl = reinterpret_cast<uint32_t *>(w + L.attn_ctl_off);
+    float *part = reinterpret_cast<float *>(w + L.part_off);
+    float *scores = reinterpret_cast<float *>(w + L.scores_off);
+    // 1. append K/V (and, inside an interval, the tail entry of the selection)
+    cudaError_t e = launch_append(*shape, K_new, V_new, nullptr, K, V, nullptr, n, predict ? nullptr : sel, sel_stride,
+                                  counts, dev_status, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (predict) {
+        // 2. the batches that left the window -> Kp; score the candidates, select, widen, add sink and window
+        if (P > *proj_end) {
+            e = launch_project(*shape, K + *proj_end * shape->D, shape->cap, Wk, Kp, *proj_end, P - *proj_end,
+                               dev_status, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            *proj_end = P;
+        }
+        if (kc > 0) {
+            e = launch_score(*shape, q_imp, Kp + S * shape->dp, nc, p->agg, scores, nc, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            e = launch_topk(rows, scores, nc, nc, kc, idx_state, ctl, dev_status, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+        e = launch_expand_ranges(rows, idx_state, kc, p->r, S, pre, S, P, tail0, n_t, sel, sel_stride, counts,
+                                 dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        *n_pred = n_t;
+    }
+    // 3. attention over the selection
+    e = launch_attn(*shape, q, K, V, sel, counts, sel_stride, p->scale, out, actl, part, dev_status, stream);
+    return from_cuda(e);
+}
+
 }  // extern "C"

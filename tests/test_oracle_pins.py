@@ -399,3 +399,45 @@ def test_budget_preserving_neighbours_centres_and_bound():
             want = sorted({j for i in idx[b, h].tolist() for j in range(i - r, i + r + 1) if 0 <= j < n_pred})
             assert body == want
             assert kc <= len(body) <= k                                  # within the budget
+
+
+def test_buffered_step_sink_window_batches_and_centres():
+    # sink and local-window buffers with batched projection: the structure of every selection
+    w = synth.small(B=1, Hq=4, Hkv=2, D=16, dp=8, N=90, seed=14)
+    S, W, T, r, k = 5, 8, 3, 1, 12
+    steps = 14
+    L = synth.make_layer(w, cap=w.N + steps, n=w.N)
+    K = oracle.as_u16(L["K"]).copy()
+    V = oracle.as_u16(L["V"]).copy()
+    Kp = np.zeros((w.B, w.Hkv, w.N + steps, w.dp), dtype=np.uint16)
+    P0 = 64                                            # rows projected at prefill
+    Kp[:, :, :P0], _ = oracle.project(np.ascontiguousarray(K[:, :, :P0]), L["Wk"])
+    st = oracle.BufferedState(P0)
+    for t in range(steps):
+        n = w.N + t
+        n_t = n + 1
+        d = synth.make_step(w, 0, t, L["outlier_ch"])
+        pe_before = st.proj_end
+        out, sel, cnt = oracle.decode_step_buffered(st, t, n, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"],
+                                                    V_new=d["V_new"], Wk=L["Wk"], K=K, V=V, Kp=Kp, k=k, T=T, r=r,
+                                                    agg=oracle.AGG_MEAN, scale=w.scale, sink=S, window=W)
+        P = st.proj_end
+        assert (P - pe_before) % W == 0 and P <= n_t
+        if t % T == 0:
+            assert W <= n_t - P < 2 * W                      # the window after the batches
+            want_kp, _ = oracle.project(np.ascontiguousarray(K[:, :, :P]), L["Wk"])
+            assert np.array_equal(Kp[:, :, :P], want_kp)      # batches equal one projection of all rows
+            s_, _ = oracle.score(d["q_imp"], np.ascontiguousarray(Kp[:, :, S:P]))
+            for b, h in itertools.product(range(w.B), range(w.Hkv)):
+                v = s_[b, h]
+                m = P - S
+                rank = [sum(1 for j in range(m) if (v[j], -j) > (v[i], -i)) for i in range(m)]
+                assert st.idx[b, h].tolist() == [i for i in range(m) if rank[i] < min(k, m)]
+        for b, h in itertools.product(range(w.B), range(w.Hkv)):
+            row = sel[b, h, : cnt[b, h]].tolist()
+            assert all(a < c for a, c in zip(row, row[1:]))   # ascending, unique
+            assert set(range(min(S, n_t))) <= set(row)        # sink
+            assert set(range(max(P, S), n_t)) <= set(row)     # window (and the interval's new tokens)
+            body = [j for j in row if S <= j < P]
+            assert len(body) <= min(k, P - S) * (2 * r + 1)
+            assert set(S + i for i in st.idx[b, h].tolist()) <= set(body)
