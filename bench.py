@@ -52,6 +52,8 @@ def _args():
     ap.add_argument("--rotate", type=int, default=0, help="cache copies to rotate over (0: enough to defeat L2)")
     ap.add_argument("--agg", default="mean", choices=["mean", "max"],
                     help="how the G query heads' scores combine (mean: the default reading)")
+    ap.add_argument("--buffers", default="",
+                    help="S,W: sink and local-window buffers with batched key projection; prints its own line")
     ap.add_argument("--offload", action="store_true",
                     help="K/V in pinned host memory (the offloaded cache); prints its own line")
     return ap.parse_args()
@@ -503,6 +505,97 @@ def run_offload(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_buffered(args, w):
+    """The buffered step (sink S, window W, Kp projected in batches of W) at the bench workload with a
+    prediction at every step. R cache sets rotate (L2 defeat); set j advances its own token position, so
+    the captured sequence holds the batch projections at their natural rate (one batch per W steps of a
+    set). The M captured steps are replayed as one CUDA graph."""
+    import predicted_token_importance_tb_b300 as tb
+
+    S, W = (int(x) for x in args.buffers.split(","))
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tb.load_library()
+    R = 16
+    m = max(W, 8)                      # steps per set in the captured sequence
+    n0 = w.N - 1 - m
+    cap = w.N
+    shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, cap)
+    L = synth.make_layer(w, cap=cap, n=n0)
+    Wk = L["Wk"].cuda()
+    K0, V0 = L["K"].cuda(), L["V"].cuda()
+    P0 = ((n0 + 1 - 2 * W) // W) * W   # prefill projected up to a batch boundary, a window's worth behind
+    Kp0 = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
+    tb.tb_project_append(shape, K0, cap, Wk, Kp0, 0, P0)
+    sets = []
+    for j in range(R):
+        K, V, Kp = (K0, V0, Kp0) if j == 0 else (K0.clone(), V0.clone(), Kp0.clone())
+        layer = tb.BufferedDecodeLayer(shape, w.k, sink=S, window=W, proj_end=P0, T=1, r=0, scale=w.scale,
+                                       n_max=cap - 1)
+        sets.append((K, V, Kp, layer))
+    dins = [{k: v.cuda() for k, v in synth.make_step(w, 0, i, L["outlier_ch"]).items()} for i in range(R)]
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    M = R * m
+
+    def seq():
+        for i in range(M):
+            j, t = i % R, i // R
+            K, V, Kp, layer = sets[j]
+            d = dins[j]
+            layer.step(t, n0 + t, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=Wk, K=K, V=V,
+                       Kp=Kp, out=out)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        seq()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for _, _, _, layer in sets:
+        tb.check_dev_status(layer.status, "buffered warm-up")
+    reps = max(1, args.steps // M)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    for _, _, _, layer in sets:
+        tb.check_dev_status(layer.status, "buffered timed steps")
+    ms = e0.elapsed_time(e1)
+    n_steps = reps * M
+    layer = sets[0][3]
+    rows = w.B * w.Hkv
+    sel_rows = int(layer.counts.sum().item())
+    P = layer.proj_end.value
+    # Kp stream of the candidates, the selected K/V rows, q / q_imp / out, the append (K_new, V_new in, the
+    # K/V rows out) and the batch projection per step (a K row in and a Kp row out per row, Wk once a batch)
+    step_bytes = (rows * (P - S) * w.dp * 2 + sel_rows * 2 * w.D * 2 + (w.B * w.Hq * w.D * 2) * 2
+                  + w.B * w.Hq * w.dp * 2 + rows * 2 * w.D * 2 * 2
+                  + rows * (w.D * 2 + w.dp * 2) + w.Hkv * w.D * w.dp * 2 // W)
+    hbm_peak, peak_kind = _peaks()
+    per_step = ms / 1e3 / n_steps
+    line = {
+        "metric": "decode steps/s with sink + local-window buffers and batched key projection, N=32K, budget 10%",
+        "value": n_steps / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": n_steps, "warmup": 3 * M,
+        "ms_per_step": ms / n_steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "sink": S, "window": W, "T": 1, "r": 0, "rotation_sets": R,
+                   "steps_per_set_in_graph": m},
+        "bytes_per_step": step_bytes, "selected_rows_per_step": sel_rows,
+        "roofline": {"bound": "hbm", "achieved": step_bytes / per_step / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": step_bytes / per_step / 1e9 / hbm_peak, "peak_source": peak_kind},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     w = _workload(args.workload)
@@ -510,6 +603,8 @@ def main():
         run_reference(args, w)
     elif args.offload:
         run_offload(args, w)
+    elif args.buffers:
+        run_buffered(args, w)
     else:
         run_ours(args, w)
 
