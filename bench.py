@@ -52,6 +52,8 @@ def _args():
     ap.add_argument("--rotate", type=int, default=0, help="cache copies to rotate over (0: enough to defeat L2)")
     ap.add_argument("--agg", default="mean", choices=["mean", "max"],
                     help="how the G query heads' scores combine (mean: the default reading)")
+    ap.add_argument("--predict", default="",
+                    help="B,E,F: the importance-query predictor (O = Hq dp of the workload); prints its own line")
     ap.add_argument("--buffers", default="",
                     help="S,W: sink and local-window buffers with batched key projection; prints its own line")
     ap.add_argument("--offload", action="store_true",
@@ -505,6 +507,64 @@ def run_offload(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_predict(args, w):
+    """The predictor MLP for B tokens (hidden E -> F -> Hq dp), weights rotated over enough copies to
+    defeat L2, M calls captured in one CUDA graph."""
+    import predicted_token_importance_tb_b300 as tb
+
+    B, E, F = (int(v) for v in args.predict.split(","))
+    O = w.Hq * w.dp
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tb.load_library()
+    g = torch.Generator().manual_seed(7)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    wbytes = (F * E + O * F) * 2
+    R = max(4, math.ceil(4 * l2 / wbytes))
+    W1s = [(torch.randn(F, E, generator=g) * E ** -0.5).to(torch.bfloat16).cuda() for _ in range(R)]
+    W2s = [(torch.randn(O, F, generator=g) * F ** -0.5).to(torch.bfloat16).cuda() for _ in range(R)]
+    xs = [torch.randn(B, E, generator=g).to(torch.bfloat16).cuda() for _ in range(R)]
+    q = torch.empty(B, O, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(B * F * 4, dtype=torch.uint8, device="cuda")
+    M = R * max(1, 2000 // R)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for i in range(M):
+            j = i % R
+            tb.tb_predict_queries(xs[j], W1s[j], W2s[j], q, ws=ws)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // M)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    n = reps * M
+    per = ms / 1e3 / n
+    nbytes = wbytes + B * E * 2 + B * O * 2 + 2 * B * F * 4
+    hbm_peak, peak_kind = _peaks()
+    line = {
+        "metric": "importance-query predictions/s (MLP forward)", "value": n / (ms / 1e3), "unit": "predictions/s",
+        "n_gpus": 1, "steps": n, "warmup": 3 * M, "ms_per_step": ms / n, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random weights)",
+        "config": {"tokens": B, "hidden": E, "mlp_width": F, "outputs": O, "weight_sets": R},
+        "bytes_per_step": nbytes, "kernels_per_step": 2,
+        "roofline": {"bound": "hbm", "achieved": nbytes / per / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": nbytes / per / 1e9 / hbm_peak, "peak_source": peak_kind},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_buffered(args, w):
     """The buffered step (sink S, window W, Kp projected in batches of W) at the bench workload with a
     prediction at every step. R cache sets rotate (L2 defeat); set j advances its own token position, so
@@ -605,6 +665,8 @@ def main():
         run_offload(args, w)
     elif args.buffers:
         run_buffered(args, w)
+    elif args.predict:
+        run_predict(args, w)
     else:
         run_ours(args, w)
 

@@ -211,6 +211,23 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * The importance-query predictor ("TokenButler: Token Importance is
+ * Predictable", gist.science summary, Core Architecture, Query Prediction: a
+ * lightweight MLP from a producer layer's hidden state to G low-dimensional
+ * query vectors per KV head), for B tokens:
+ *   h     = SiLU(x . W1^T)          x [B, E] bf16, W1 [F, E] bf16, h fp32
+ *   q_imp = RNE_bf16(h . W2^T)      W2 [O, F] bf16, q_imp [B, O] = [B, Hq, dp]
+ * The pages give no depth, width, activation or bias: two layers, no bias,
+ * SiLU (the activation of the base models' MLPs), fp32 accumulation and one
+ * rounding at the end are this library's reading. Limits: 1 <= B <= 16,
+ * E and F multiples of 8, B E 2 and B F 4 bytes <= 200 KB. ws: at least
+ * B F 4 bytes of device memory for h (no zero-fill needed).
+ */
+TB_API tb_status tb_predict_queries(const tb_bf16 *x, const tb_bf16 *W1, const tb_bf16 *W2, int32_t B,
+                                    int32_t E, int32_t F, int32_t O, tb_bf16 *q_imp, void *ws,
+                                    size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/*
  * Sink and local-window buffers ("TokenButler: Token Importance is
  * Predictable", gist.science summary, Inference Strategy: the first S tokens
  * and a window of the newest tokens are always kept, the important tokens

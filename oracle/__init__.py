@@ -347,3 +347,27 @@ def decode_step_buffered(state: BufferedState, t: int, n: int, *, q, q_imp, K_ne
         counts[x // Hkv, x % Hkv] = len(row)
     out = attn(q, K, V, sel, counts, scale)
     return out, sel, counts
+
+
+def silu(v):
+    """SiLU(v) = v / (1 + exp(-v)) in fp64."""
+    v = np.asarray(v, dtype=np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+def predict_queries(x, W1, W2):
+    """The importance-query predictor for B tokens.
+
+    [summary] Core Architecture, Query Prediction: a lightweight MLP maps the
+    producer layer's hidden state to G low-dimensional query vectors per KV
+    head. Reading (the pages give no depth, width, activation or bias): two
+    bias-free layers with SiLU between them, h = SiLU(x W1^T), q_imp =
+    RNE_bf16(h W2^T), exact products and fp64 sums here.
+    x [B, E], W1 [F, E], W2 [O, F] bf16 bits -> (q_imp bits [B, O], fp64 [B, O], h fp64 [B, F]).
+    """
+    xf = bf16_bits_to_f64(as_u16(x))
+    w1 = bf16_bits_to_f64(as_u16(W1))
+    w2 = bf16_bits_to_f64(as_u16(W2))
+    h = silu(xf @ w1.T)
+    y = h @ w2.T
+    return bf16_round(y), y, h

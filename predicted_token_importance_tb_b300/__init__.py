@@ -37,7 +37,7 @@ TB_STEP_BUDGET_NEIGHBOURS = 2
 EXPORTED = (
     "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
     "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step", "tb_topk_noalloc",
-    "tb_decode_step_buffered",
+    "tb_decode_step_buffered", "tb_predict_queries",
 )
 
 TB_TOPK_NOALLOC_MAX_ROWS = 64
@@ -105,6 +105,7 @@ def load_library(path: str = LIB_PATH):
         lib.tb_sparse_decode_attn.argtypes = [SP, P, P, P, P, P, i32, f32, P, P, sz, P, P]
         lib.tb_decode_step.argtypes = [SP, ctypes.POINTER(_StepParams), i64, i64, P, P, P, P, P, P, P, P, P,
                                        ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
+        lib.tb_predict_queries.argtypes = [P, P, P, i32, i32, i32, i32, P, P, sz, P, P]
         lib.tb_decode_step_buffered.argtypes = [SP, ctypes.POINTER(_StepParams), ctypes.POINTER(_BufferParams), i64,
                                                 i64, P, P, P, P, P, P, P, P, P, ctypes.POINTER(i64),
                                                 ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
@@ -283,6 +284,21 @@ def tb_decode_step_buffered(shape: Shape, k: int, T: int, r: int, agg: int, scal
         _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.byref(n_pred), ctypes.byref(proj_end),
         _i32(sel, "sel"), sel_stride, _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), ws.numel(),
         _status_ptr(dev_status), _stream(stream)), "tb_decode_step_buffered")
+
+
+def tb_predict_queries(x, W1, W2, q_imp, ws=None, dev_status=None, stream=None):
+    """q_imp [B, O] = RNE(SiLU(x W1^T) W2^T): x [B, E], W1 [F, E], W2 [O, F] bf16 (see include/tb.h).
+    ws: a device buffer of at least B F 4 bytes (allocated here if None)."""
+    B, E = x.shape[0], x.shape[-1]
+    F, O = W1.shape[0], W2.shape[0]
+    if W1.shape[-1] != E or W2.shape[-1] != F or q_imp.numel() != B * O:
+        raise ValueError("shapes: x [B, E], W1 [F, E], W2 [O, F], q_imp [B, O]")
+    if ws is None:
+        ws = torch.empty(B * F * 4, dtype=torch.uint8, device=x.device)
+    _check(load_library().tb_predict_queries(_bf16(x, "x"), _bf16(W1, "W1"), _bf16(W2, "W2"), B, E, F, O,
+                                             _bf16(q_imp, "q_imp"), _ptr(ws), ws.numel() * ws.element_size(),
+                                             _status_ptr(dev_status), _stream(stream)), "tb_predict_queries")
+    return q_imp
 
 
 def sel_stride_for(k: int, T: int, r: int, n_max: int) -> int:

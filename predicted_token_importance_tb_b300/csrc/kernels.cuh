@@ -76,4 +76,9 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
                               int32_t *sel, int32_t *counts, uint16_t *out, const FastWs &w, int32_t sel_stride,
                               int32_t *dev_status, cudaStream_t st);
 
+// The predictor MLP for B tokens: h [B, F] = SiLU(x W1^T) (fp32), q_imp [B, O] =
+// RNE(h W2^T). E and F multiples of 8, B <= 16.
+cudaError_t launch_predict(const uint16_t *x, const uint16_t *W1, const uint16_t *W2, int B, int E, int F, int O,
+                           float *h, uint16_t *q_imp, cudaStream_t st);
+
 }  // namespace tb

@@ -251,6 +251,22 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     return from_cuda(e);
 }
 
+tb_status tb_predict_queries(const tb_bf16 *x, const tb_bf16 *W1, const tb_bf16 *W2, int32_t B, int32_t E,
+                             int32_t F, int32_t O, tb_bf16 *q_imp, void *ws, size_t ws_bytes, int32_t *dev_status,
+                             cudaStream_t stream) {
+    (void)dev_status;   // nothing on this path is detected on the device
+    if (B < 1 || E < 1 || F < 1 || O < 1) return TB_ERR_INVALID_ARG;
+    if (B > 16 || E % 8 != 0 || F % 8 != 0) return TB_ERR_UNSUPPORTED;
+    if ((int64_t)B * E * 2 > 200 * 1024 || (int64_t)B * F * 4 > 200 * 1024) return TB_ERR_UNSUPPORTED;
+    TB_PTR(x);
+    TB_PTR(W1);
+    TB_PTR(W2);
+    TB_PTR(q_imp);
+    TB_PTR(ws);
+    if (ws_bytes < (size_t)B * F * 4) return TB_ERR_WORKSPACE;
+    return from_cuda(launch_predict(x, W1, W2, B, E, F, O, static_cast<float *>(ws), q_imp, stream));
+}
+
 tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *p, const tb_buffer_params *bp,
                                   int64_t t, int64_t n, const tb_bf16 *q, const tb_bf16 *q_imp,
                                   const tb_bf16 *K_new, const tb_bf16 *V_new, const tb_bf16 *Wk, tb_bf16 *K,

@@ -441,3 +441,25 @@ def test_buffered_step_sink_window_batches_and_centres():
             body = [j for j in row if S <= j < P]
             assert len(body) <= min(k, P - S) * (2 * r + 1)
             assert set(S + i for i in st.idx[b, h].tolist()) <= set(body)
+
+
+# ------------------------------------------------------------------ predictor
+
+def test_predictor_matches_torch_fp64_and_silu_identities():
+    g = torch.Generator().manual_seed(21)
+    B, E, F, O = 3, 64, 32, 24
+    x = torch.randn(B, E, generator=g).to(torch.bfloat16)
+    W1 = (torch.randn(F, E, generator=g) / 8).to(torch.bfloat16)
+    W2 = (torch.randn(O, F, generator=g) / 6).to(torch.bfloat16)
+    bits, y, h = oracle.predict_queries(x, W1, W2)
+    # the library routines: torch's SiLU and matmul in fp64 on the same bf16 values
+    ht = torch.nn.functional.silu(x.double() @ W1.double().T)
+    yt = ht @ W2.double().T
+    assert np.allclose(h, ht.numpy(), rtol=1e-12, atol=1e-14)
+    assert np.allclose(y, yt.numpy(), rtol=1e-12, atol=1e-14)
+    assert np.array_equal(bits, oracle.bf16_round(yt.numpy()))
+    # SiLU: odd part is the identity, zero at zero, -> v for large v, -> 0 for very negative v
+    v = np.linspace(-20, 20, 81)
+    assert np.allclose(oracle.silu(v) - oracle.silu(-v), v, rtol=0, atol=1e-12)
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12 and abs(oracle.silu(-40.0)) < 1e-12
