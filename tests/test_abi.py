@@ -63,3 +63,37 @@ def test_host_validation_without_gpu(lib_path):
                        None) == tb.TB_ERR_INVALID_ARG
     assert lib.tb_topk(ctypes.byref(ok), ctypes.c_void_p(16), 10, 5, ctypes.c_void_p(16), None, 0, None,
                        None) == tb.TB_ERR_WORKSPACE
+
+
+def test_host_validation_of_the_newer_calls(lib_path):
+    # the buffered step and the predictor check their arguments before any CUDA call
+    import predicted_token_importance_tb_b300 as tb
+    lib = tb.load_library()
+    fake = ctypes.c_void_p(1 << 20)              # aligned, never dereferenced: the checks fail first
+    sp = tb.Shape(1, 8, 2, 64, 16, 1000).c()
+    params = tb._StepParams(10, 1, 0, 0, 0.125, 0)
+    i64 = ctypes.c_int64
+    n_pred, proj_end = i64(0), i64(0)
+    for sink, window, want in [(4, 0, tb.TB_ERR_INVALID_ARG), (-1, 8, tb.TB_ERR_INVALID_ARG)]:
+        bufs = tb._BufferParams(sink, window)
+        st = lib.tb_decode_step_buffered(ctypes.byref(sp), ctypes.byref(params), ctypes.byref(bufs), 0, 100,
+                                         fake, fake, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(n_pred),
+                                         ctypes.byref(proj_end), fake, 64, fake, fake, fake, 1 << 30, None, None)
+        assert st == want
+    proj_end.value = 500                         # more rows projected than tokens
+    bufs = tb._BufferParams(4, 8)
+    st = lib.tb_decode_step_buffered(ctypes.byref(sp), ctypes.byref(params), ctypes.byref(bufs), 0, 100,
+                                     fake, fake, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(n_pred),
+                                     ctypes.byref(proj_end), fake, 64, fake, fake, fake, 1 << 30, None, None)
+    assert st == tb.TB_ERR_INVALID_ARG
+    bad_flags = tb._StepParams(10, 1, 0, 0, 0.125, 64)
+    st = lib.tb_decode_step(ctypes.byref(sp), ctypes.byref(bad_flags), 0, 100, fake, fake, fake, fake, fake, fake,
+                            fake, fake, fake, ctypes.byref(n_pred), fake, 64, fake, fake, fake, 1 << 30, None, None)
+    assert st == tb.TB_ERR_INVALID_ARG
+    # predictor: too many tokens, a width that is not a multiple of 8, a workspace too small
+    assert lib.tb_predict_queries(fake, fake, fake, 17, 64, 32, 16, fake, fake, 1 << 20, None, None) == \
+        tb.TB_ERR_UNSUPPORTED
+    assert lib.tb_predict_queries(fake, fake, fake, 2, 60, 32, 16, fake, fake, 1 << 20, None, None) == \
+        tb.TB_ERR_UNSUPPORTED
+    assert lib.tb_predict_queries(fake, fake, fake, 2, 64, 32, 16, fake, fake, 16, None, None) == \
+        tb.TB_ERR_WORKSPACE
