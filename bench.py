@@ -52,6 +52,8 @@ def _args():
     ap.add_argument("--rotate", type=int, default=0, help="cache copies to rotate over (0: enough to defeat L2)")
     ap.add_argument("--agg", default="mean", choices=["mean", "max"],
                     help="how the G query heads' scores combine (mean: the default reading)")
+    ap.add_argument("--ragged", default="",
+                    help="n1,n2,...: a batch of sequences of these lengths (the workload's heads, k); own line")
     ap.add_argument("--predict", default="",
                     help="B,E,F: the importance-query predictor (O = Hq dp of the workload); prints its own line")
     ap.add_argument("--buffers", default="",
@@ -507,6 +509,84 @@ def run_offload(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_ragged(args, w):
+    """The step for a ragged batch (T = 1, r = 0, the workload's heads and budget) at fixed positions, R
+    rotated cache sets, M steps captured in one CUDA graph."""
+    import predicted_token_importance_tb_b300 as tb
+
+    ns = [int(v) for v in args.ragged.split(",")]
+    B = len(ns)
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tb.load_library()
+    cap = max(ns) + 1
+    wb = synth.Workload(f"ragged-B{B}", B=B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, dp=w.dp, N=max(ns), k=w.k, seed=9)
+    k = min(w.k, min(ns) + 1)
+    shape = tb.Shape(B, w.Hq, w.Hkv, w.D, w.dp, cap)
+    L = synth.make_layer(wb, cap=cap, n=max(ns))
+    Wk = L["Wk"].cuda()
+    K0, V0 = L["K"].cuda(), L["V"].cuda()
+    Kp0 = torch.zeros((B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
+    tb.tb_project_append(shape, K0, cap, Wk, Kp0, 0, max(ns))
+    rows = B * w.Hkv
+    step_bytes = (sum((n + 1) * w.Hkv * w.dp * 2 for n in ns) + rows * k * 2 * w.D * 2 + (B * w.Hq * w.D * 2) * 2
+                  + B * w.Hq * w.dp * 2 + rows * w.D * 2 * 2 * 2 + w.Hkv * w.D * w.dp * 2 + rows * w.dp * 2)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(4 * l2 / step_bytes))
+    sets = [(K0, V0, Kp0)] + [(K0.clone(), V0.clone(), Kp0.clone()) for _ in range(R - 1)]
+    dins = [{kk: v.cuda() for kk, v in synth.make_step(wb, 0, i, L["outlier_ch"]).items()} for i in range(R)]
+    dec = tb.RaggedDecodeLayer(shape, k, T=1, r=0, scale=w.scale, n_max=cap - 1)
+    out = torch.empty((B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        K, V, Kp = sets[i % R]
+        d = dins[i % R]
+        dec.step(0, ns, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=Wk, K=K, V=V, Kp=Kp,
+                 out=out)
+
+    for i in range(R):
+        step(i)
+    torch.cuda.synchronize()
+    tb.check_dev_status(dec.status, "ragged warm-up")
+    M = R * max(1, 400 // R)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for i in range(M):
+            step(i)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // M)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    tb.check_dev_status(dec.status, "ragged timed steps")
+    ms = e0.elapsed_time(e1)
+    n = reps * M
+    per = ms / 1e3 / n
+    hbm_peak, peak_kind = _peaks()
+    line = {
+        "metric": "decode steps/s for a ragged batch (sequences of different lengths), budget k per sequence",
+        "value": n / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": n, "warmup": 3 * M, "ms_per_step": ms / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"lengths": ns, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "dp": w.dp, "k": k, "T": 1, "r": 0,
+                   "rotation_sets": R},
+        "tokens_per_s": n / (ms / 1e3) * B, "bytes_per_step": step_bytes,
+        "roofline": {"bound": "hbm", "achieved": step_bytes / per / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": step_bytes / per / 1e9 / hbm_peak, "peak_source": peak_kind},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_predict(args, w):
     """The predictor MLP for B tokens (hidden E -> F -> Hq dp), weights rotated over enough copies to
     defeat L2, M calls captured in one CUDA graph."""
@@ -667,6 +747,8 @@ def main():
         run_buffered(args, w)
     elif args.predict:
         run_predict(args, w)
+    elif args.ragged:
+        run_ragged(args, w)
     else:
         run_ours(args, w)
 

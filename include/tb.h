@@ -211,6 +211,26 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * tb_decode_step for a ragged batch: sequence b holds n[b] tokens before
+ * this step's append (SURVEY's f4 variant; the pages batch sequences without
+ * saying how). Per sequence the step is exactly tb_decode_step's: the new
+ * K/V/Kp rows go to position n[b], a prediction scores that sequence's
+ * n[b] + 1 tokens and keeps the top k, the widening stays inside them, and
+ * between predictions the sequence's new token joins its selection.
+ * n_host [B] (host) and n_dev [B] (device) hold the same values;
+ * n_pred [B] is the host state of the interval, one entry per sequence.
+ * Needs k <= n[b] + 1 for every b at a prediction and sel_stride >=
+ * min(max_b n[b] + 1, k (2r+1)) + T - 1. Always separate kernels.
+ */
+TB_API tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_params *params, int64_t t,
+                                       const int64_t *n_host, const int64_t *n_dev, const tb_bf16 *q,
+                                       const tb_bf16 *q_imp, const tb_bf16 *K_new, const tb_bf16 *V_new,
+                                       const tb_bf16 *Wk, tb_bf16 *K, tb_bf16 *V, tb_bf16 *Kp,
+                                       int32_t *idx_state, int64_t *n_pred, int32_t *sel, int32_t sel_stride,
+                                       int32_t *counts, tb_bf16 *out, void *ws, size_t ws_bytes,
+                                       int32_t *dev_status, cudaStream_t stream);
+
+/*
  * The importance-query predictor ("TokenButler: Token Importance is
  * Predictable", gist.science summary, Core Architecture, Query Prediction: a
  * lightweight MLP from a producer layer's hidden state to G low-dimensional

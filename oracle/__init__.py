@@ -371,3 +371,27 @@ def predict_queries(x, W1, W2):
     h = silu(xf @ w1.T)
     y = h @ w2.T
     return bf16_round(y), y, h
+
+
+def decode_step_ragged(states: list, t: int, ns, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, k: int, T: int,
+                       r: int, agg: int, scale: float, budget_neighbours: bool = False):
+    """A decode step for a batch of sequences of different lengths: sequence b
+    (n[b] tokens before the append) is exactly decode_step on its own slice
+    of every tensor. states: one DecodeState per sequence. K, V, Kp mutated.
+    Returns (out [B,Hq,D], sel [B,Hkv,width] padded with -1, counts [B,Hkv])."""
+    q, q_imp = as_u16(q), as_u16(q_imp)
+    K_new, V_new = as_u16(K_new), as_u16(V_new)
+    outs, sels, cnts = [], [], []
+    for b, nb in enumerate(ns):
+        Kb, Vb, Kpb = K[b:b + 1], V[b:b + 1], Kp[b:b + 1]
+        o, sl, c = decode_step(states[b], t, int(nb), q=q[b:b + 1], q_imp=q_imp[b:b + 1], K_new=K_new[b:b + 1],
+                               V_new=V_new[b:b + 1], Wk=Wk, K=Kb, V=Vb, Kp=Kpb, k=k, T=T, r=r, agg=agg,
+                               scale=scale, budget_neighbours=budget_neighbours)
+        outs.append(o)
+        sels.append(sl)
+        cnts.append(c)
+    width = max(x.shape[-1] for x in sels)
+    sel = np.full((len(ns), sels[0].shape[1], width), -1, dtype=np.int32)
+    for b, x in enumerate(sels):
+        sel[b, :, :x.shape[-1]] = x[0]
+    return np.concatenate(outs, axis=0), sel, np.concatenate(cnts, axis=0)

@@ -37,7 +37,7 @@ TB_STEP_BUDGET_NEIGHBOURS = 2
 EXPORTED = (
     "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
     "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step", "tb_topk_noalloc",
-    "tb_decode_step_buffered", "tb_predict_queries",
+    "tb_decode_step_buffered", "tb_predict_queries", "tb_decode_step_ragged",
 )
 
 TB_TOPK_NOALLOC_MAX_ROWS = 64
@@ -106,6 +106,10 @@ def load_library(path: str = LIB_PATH):
         lib.tb_decode_step.argtypes = [SP, ctypes.POINTER(_StepParams), i64, i64, P, P, P, P, P, P, P, P, P,
                                        ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
         lib.tb_predict_queries.argtypes = [P, P, P, i32, i32, i32, i32, P, P, sz, P, P]
+        # shape, params, t, n_host, n_dev, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, n_pred, sel,
+        # sel_stride, counts, out, ws, ws_bytes, dev_status, stream
+        lib.tb_decode_step_ragged.argtypes = [SP, ctypes.POINTER(_StepParams), i64, P, P, P, P, P, P, P, P, P, P, P,
+                                              P, P, i32, P, P, P, sz, P, P]
         lib.tb_decode_step_buffered.argtypes = [SP, ctypes.POINTER(_StepParams), ctypes.POINTER(_BufferParams), i64,
                                                 i64, P, P, P, P, P, P, P, P, P, ctypes.POINTER(i64),
                                                 ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
@@ -368,4 +372,45 @@ class BufferedDecodeLayer:
                                 idx_state=self.idx_state, n_pred=self.n_pred, proj_end=self.proj_end, sel=self.sel,
                                 sel_stride=self.sel_stride, counts=self.counts, out=out, ws=self.ws,
                                 dev_status=self.status, stream=stream, flags=self.flags)
+        return out
+
+
+class RaggedDecodeLayer:
+    """Per-layer decode state for a batch whose sequences have different lengths (see
+    tb_decode_step_ragged in include/tb.h): n_pred is kept per sequence."""
+
+    def __init__(self, shape: Shape, k: int, T: int = 1, r: int = 0, agg: int = TB_AGG_MEAN,
+                 scale: float | None = None, n_max: int | None = None, device=None, budget_neighbours: bool = False):
+        self.shape, self.k, self.T, self.r, self.agg = shape, k, T, r, agg
+        self.flags = TB_STEP_BUDGET_NEIGHBOURS if budget_neighbours else 0
+        self.kc = max(1, k // (2 * r + 1)) if budget_neighbours else k
+        self.scale = scale if scale is not None else shape.D ** -0.5
+        n_max = shape.cap - 1 if n_max is None else n_max
+        dev = device or "cuda"
+        rows = (shape.B, shape.Hkv)
+        self.sel_stride = sel_stride_for(self.kc, T, r, n_max)
+        self.idx_state = torch.zeros(rows + (self.kc,), dtype=torch.int32, device=dev)
+        self.sel = torch.zeros(rows + (self.sel_stride,), dtype=torch.int32, device=dev)
+        self.counts = torch.zeros(rows, dtype=torch.int32, device=dev)
+        self.n_pred = (ctypes.c_int64 * shape.B)()
+        self.n_host = (ctypes.c_int64 * shape.B)()
+        self.n_dev = torch.zeros(shape.B, dtype=torch.int64, device=dev)
+        self.ws = workspace(shape, n_max, max(k, self.kc), self.sel_stride, device=dev)
+        self.status = dev_status(dev)
+
+    def step(self, t: int, ns, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, out, stream=None):
+        """ns: tokens per sequence before this step's append (B ints)."""
+        ns = [int(v) for v in ns]
+        if ns != list(self.n_host):   # (unchanged lengths need no copy, so repeated steps can be captured)
+            for b, v in enumerate(ns):
+                self.n_host[b] = v
+            self.n_dev.copy_(torch.tensor(ns, dtype=torch.int64), non_blocking=False)
+        params = _StepParams(self.k, self.T, self.r, self.agg, self.scale, self.flags)
+        _check(load_library().tb_decode_step_ragged(
+            ctypes.byref(self.shape.c()), ctypes.byref(params), t, ctypes.cast(self.n_host, ctypes.c_void_p),
+            _ptr(self.n_dev), _bf16(q, "q"), _bf16(q_imp, "q_imp"), _bf16(K_new, "K_new"), _bf16(V_new, "V_new"),
+            _bf16(Wk, "Wk"), _kv(K, "K"), _kv(V, "V"), _bf16(Kp, "Kp"), _i32(self.idx_state, "idx_state"),
+            ctypes.cast(self.n_pred, ctypes.c_void_p), _i32(self.sel, "sel"), self.sel_stride,
+            _i32(self.counts, "counts"), _bf16(out, "out"), _ptr(self.ws), self.ws.numel(), _status_ptr(self.status),
+            _stream(stream)), "tb_decode_step_ragged")
         return out

@@ -16,12 +16,13 @@ __global__ void __launch_bounds__(kAppendThreads)
 append_kernel(const uint16_t *__restrict__ K_new, const uint16_t *__restrict__ V_new,
               const uint16_t *__restrict__ Wk, uint16_t *__restrict__ K, uint16_t *__restrict__ V,
               uint16_t *__restrict__ Kp, int64_t cap, int Hkv, int D, int dp, int64_t pos, int32_t *sel,
-              int32_t sel_stride, int32_t *counts, int32_t *dev_status) {
+              int32_t sel_stride, int32_t *counts, int32_t *dev_status, const int64_t *__restrict__ pos_seq) {
     extern __shared__ float sh[];   // knew[D] then partial[kAppendThreads]
     float *knew = sh;
     float *part = sh + D;
     const int row = blockIdx.x;
     const int h = row % Hkv;
+    if (pos_seq) pos = pos_seq[row / Hkv];   // ragged batch: this sequence's position
     const uint16_t *kn = K_new + (int64_t)row * D;
     const uint16_t *vn = V_new + (int64_t)row * D;
     uint16_t *Krow = K + ((int64_t)row * cap + pos) * D;
@@ -71,12 +72,12 @@ append_kernel(const uint16_t *__restrict__ K_new, const uint16_t *__restrict__ V
 
 cudaError_t launch_append(const tb_shape &sh, const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk,
                           uint16_t *K, uint16_t *V, uint16_t *Kp, int64_t pos, int32_t *sel, int32_t sel_stride,
-                          int32_t *counts, int32_t *dev_status, cudaStream_t st) {
+                          int32_t *counts, int32_t *dev_status, cudaStream_t st, const int64_t *pos_seq) {
     const int rows = sh.B * sh.Hkv;
     if (rows <= 0) return cudaSuccess;
     const size_t smem = (size_t)(sh.D + kAppendThreads) * sizeof(float);
     append_kernel<<<rows, kAppendThreads, smem, st>>>(K_new, V_new, Wk, K, V, Kp, sh.cap, sh.Hkv, sh.D, sh.dp, pos,
-                                                      sel, sel_stride, counts, dev_status);
+                                                      sel, sel_stride, counts, dev_status, pos_seq);
     return cudaGetLastError();
 }
 

@@ -21,9 +21,11 @@ constexpr int kExpandThreads = 1024;
 __global__ void __launch_bounds__(kExpandThreads)
 expand_kernel(const int32_t *__restrict__ idx, int32_t k, int32_t r, int64_t idx_off, int64_t prefix_end,
               int64_t body_lo, int64_t body_hi, int64_t tail_start, int64_t n_t, int32_t *__restrict__ sel,
-              int32_t sel_stride, int32_t *__restrict__ counts, int32_t *dev_status) {
+              int32_t sel_stride, int32_t *__restrict__ counts, int32_t *dev_status, const int64_t *__restrict__ n_seq,
+              int Hkv) {
     __shared__ uint32_t scan[33];
     const int row = blockIdx.x;
+    if (n_seq) body_hi = tail_start = n_t = n_seq[row / Hkv] + 1;   // ragged batch at a prediction
     const int32_t *irow = idx + (int64_t)row * k;
     int32_t *srow = sel + (int64_t)row * sel_stride;
     // the prefix [0, prefix_end) first
@@ -75,13 +77,22 @@ cudaError_t launch_expand(int rows, const int32_t *idx, int32_t k, int32_t r, in
                                 st);
 }
 
+cudaError_t launch_expand_ragged(int rows, int Hkv, const int64_t *n_seq, const int32_t *idx, int32_t k, int32_t r,
+                                 int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status,
+                                 cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    expand_kernel<<<rows, kExpandThreads, 0, st>>>(idx, k, r, 0, 0, 0, 0, 0, 0, sel, sel_stride, counts, dev_status,
+                                                   n_seq, Hkv);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_expand_ranges(int rows, const int32_t *idx, int32_t k, int32_t r, int64_t idx_off,
                                  int64_t prefix_end, int64_t body_lo, int64_t body_hi, int64_t tail_start,
                                  int64_t n_t, int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status,
                                  cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
     expand_kernel<<<rows, kExpandThreads, 0, st>>>(idx, k, r, idx_off, prefix_end, body_lo, body_hi, tail_start, n_t,
-                                                   sel, sel_stride, counts, dev_status);
+                                                   sel, sel_stride, counts, dev_status, nullptr, 1);
     return cudaGetLastError();
 }
 

@@ -9,8 +9,10 @@
 
 namespace tb {
 
+// n_seq (device, [B], may be null): sequence b holds n_seq[b] + 1 tokens; the
+// scores of its later positions are -inf.
 cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16_t *Kp, int64_t n, int agg,
-                         float *s, int64_t lds, cudaStream_t st);
+                         float *s, int64_t lds, cudaStream_t st, const int64_t *n_seq = nullptr);
 
 // rows x n scores (row stride lds) -> rows x k ascending indices; when sel
 // is given the indices also go to sel (row stride sel_stride) and k to counts.
@@ -20,6 +22,10 @@ cudaError_t launch_topk(int rows, const float *s, int64_t lds, int64_t n, int32_
 
 cudaError_t launch_expand(int rows, const int32_t *idx, int32_t k, int32_t r, int64_t n_pred, int64_t n_t,
                           int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status, cudaStream_t st);
+// A ragged batch at a prediction: row (b, h) widens within [0, n_seq[b] + 1).
+cudaError_t launch_expand_ragged(int rows, int Hkv, const int64_t *n_seq, const int32_t *idx, int32_t k, int32_t r,
+                                 int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status,
+                                 cudaStream_t st);
 // sel row = [0, prefix_end) ++ windows of (idx + idx_off) clipped to
 // [body_lo, body_hi) ++ [tail_start, n_t) (ranges disjoint and ascending).
 cudaError_t launch_expand_ranges(int rows, const int32_t *idx, int32_t k, int32_t r, int64_t idx_off,
@@ -39,9 +45,10 @@ cudaError_t launch_attn_mma(const tb_shape &sh, const uint16_t *q, const uint16_
 
 // One new row per (b, h): cache writes, its projection and (optionally) the
 // tail entry of the selection.
+// pos_seq (device, [B], may be null): per-sequence positions instead of pos.
 cudaError_t launch_append(const tb_shape &sh, const uint16_t *K_new, const uint16_t *V_new, const uint16_t *Wk,
                           uint16_t *K, uint16_t *V, uint16_t *Kp, int64_t pos, int32_t *sel, int32_t sel_stride,
-                          int32_t *counts, int32_t *dev_status, cudaStream_t st);
+                          int32_t *counts, int32_t *dev_status, cudaStream_t st, const int64_t *pos_seq = nullptr);
 
 // Kp rows [pos0, pos0 + n_new) from K_src (row stride src_stride per head).
 // path: 0 automatic, 1 CUDA cores, 2 tensor cores (tcgen05).

@@ -37,7 +37,7 @@ __device__ __forceinline__ float dot8(const float *q, uint4 v, float acc) {
 template <int NV>
 __global__ void __launch_bounds__(kScoreThreads)
 score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp, int64_t cap, int64_t n,
-             int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds) {
+             int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds, const int64_t *__restrict__ n_seq) {
     extern __shared__ float qs[];   // [G][dp] (MAX) or [dp] (MEAN)
     const int row = blockIdx.y;
     const int b = row / Hkv, h = row % Hkv;
@@ -56,6 +56,10 @@ score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp
     __syncthreads();
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= n) return;
+    if (n_seq && t > n_seq[b]) {   // beyond this sequence's tokens (n_seq[b] + 1 of them): never selected
+        s[(int64_t)row * lds + t] = -INFINITY;
+        return;
+    }
     const int nv = NV > 0 ? NV : dp / 8;
     const uint4 *p = reinterpret_cast<const uint4 *>(Kp + ((int64_t)row * cap + t) * dp);
     float out;
@@ -95,7 +99,7 @@ score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp
 }
 
 cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16_t *Kp, int64_t n, int agg,
-                         float *s, int64_t lds, cudaStream_t st) {
+                         float *s, int64_t lds, cudaStream_t st, const int64_t *n_seq) {
     const int rows = sh.B * sh.Hkv;
     if (n <= 0 || rows <= 0) return cudaSuccess;
     const int G = sh.Hq / sh.Hkv;
@@ -105,7 +109,7 @@ cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16
 #define TB_SCORE_CASE(NVC)                                                                                 \
     case NVC:                                                                                              \
         score_kernel<NVC><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv, sh.dp, agg, \
-                                                             s, lds);                                      \
+                                                             s, lds, n_seq);                                      \
         break;
     switch (nv) {
         TB_SCORE_CASE(1)
@@ -114,7 +118,7 @@ cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16
         TB_SCORE_CASE(8)
         default:
             score_kernel<0><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv, sh.dp, agg, s,
-                                                               lds);
+                                                               lds, n_seq);
     }
 #undef TB_SCORE_CASE
     return cudaGetLastError();

@@ -251,6 +251,77 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     return from_cuda(e);
 }
 
+tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_params *p, int64_t t, const int64_t *n_host,
+                                const int64_t *n_dev, const tb_bf16 *q, const tb_bf16 *q_imp, const tb_bf16 *K_new,
+                                const tb_bf16 *V_new, const tb_bf16 *Wk, tb_bf16 *K, tb_bf16 *V, tb_bf16 *Kp,
+                                int32_t *idx_state, int64_t *n_pred, int32_t *sel, int32_t sel_stride, int32_t *counts,
+                                tb_bf16 *out, void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    TB_CHECK(check_shape(shape));
+    if (!p || !n_host || !n_dev || !n_pred || !idx_state || !sel || !counts) return TB_ERR_INVALID_ARG;
+    if (p->T < 1 || p->r < 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
+    if (p->flags & ~(TB_STEP_UNFUSED | TB_STEP_BUDGET_NEIGHBOURS)) return TB_ERR_INVALID_ARG;
+    if (t < 0) return TB_ERR_INVALID_ARG;
+    TB_PTR(q);
+    TB_PTR(q_imp);
+    TB_PTR(K_new);
+    TB_PTR(V_new);
+    TB_PTR(Wk);
+    TB_PTR(K);
+    TB_PTR(V);
+    TB_PTR(Kp);
+    TB_PTR(out);
+    const bool predict = (t % p->T) == 0;
+    const int32_t kc = (p->flags & TB_STEP_BUDGET_NEIGHBOURS) ? (p->k / (2 * p->r + 1) > 0 ? p->k / (2 * p->r + 1) : 1)
+                                                              : p->k;
+    int64_t n_lo = INT64_MAX, n_hi = -1;
+    for (int b = 0; b < shape->B; ++b) {
+        const int64_t nb = n_host[b];
+        if (nb < 0 || nb + 1 > shape->cap) return TB_ERR_INVALID_ARG;
+        if (!predict && (n_pred[b] <= 0 || n_pred[b] > nb)) return TB_ERR_INVALID_ARG;
+        n_lo = nb < n_lo ? nb : n_lo;
+        n_hi = nb > n_hi ? nb : n_hi;
+    }
+    const int64_t nt_hi = n_hi + 1;
+    if (predict && kc > n_lo + 1) return TB_ERR_INVALID_ARG;
+    int64_t body = (int64_t)kc * (2 * (int64_t)p->r + 1);
+    if (body > nt_hi) body = nt_hi;
+    int64_t tail = 0;   // the longest tail of the interval so far
+    if (!predict)
+        for (int b = 0; b < shape->B; ++b) tail = (n_host[b] + 1 - n_pred[b]) > tail ? n_host[b] + 1 - n_pred[b] : tail;
+    if ((int64_t)sel_stride < body + (predict ? 0 : tail)) return TB_ERR_INVALID_ARG;
+    const int rows = shape->B * shape->Hkv;
+    const WsLayout L = layout_for(*shape, nt_hi, sel_stride, 0);
+    if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    RowCtl *ctl = reinterpret_cast<RowCtl *>(w + L.rowctl_off);
+    uint32_t *actl = reinterpret_cast<uint32_t *>(w + L.attn_ctl_off);
+    float *part = reinterpret_cast<float *>(w + L.part_off);
+    float *scores = reinterpret_cast<float *>(w + L.scores_off);
+    // 1. append at each sequence's own position (and the tail entry inside an interval)
+    cudaError_t e = launch_append(*shape, K_new, V_new, Wk, K, V, Kp, 0, predict ? nullptr : sel, sel_stride, counts,
+                                  dev_status, stream, n_dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (predict) {
+        // 2. score up to the longest sequence (later positions of the shorter ones score -inf), select, widen
+        e = launch_score(*shape, q_imp, Kp, nt_hi, p->agg, scores, nt_hi, stream, n_dev);
+        if (e != cudaSuccess) return from_cuda(e);
+        if (p->r == 0 && p->T == 1) {
+            e = launch_topk(rows, scores, nt_hi, nt_hi, kc, idx_state, ctl, dev_status, stream, sel, sel_stride, counts);
+            if (e != cudaSuccess) return from_cuda(e);
+        } else {
+            e = launch_topk(rows, scores, nt_hi, nt_hi, kc, idx_state, ctl, dev_status, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            e = launch_expand_ragged(rows, shape->Hkv, n_dev, idx_state, kc, p->r, sel, sel_stride, counts, dev_status,
+                                     stream);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+        for (int b = 0; b < shape->B; ++b) n_pred[b] = n_host[b] + 1;
+    }
+    // 3. attention over the selection
+    e = launch_attn(*shape, q, K, V, sel, counts, sel_stride, p->scale, out, actl, part, dev_status, stream);
+    return from_cuda(e);
+}
+
 tb_status tb_predict_queries(const tb_bf16 *x, const tb_bf16 *W1, const tb_bf16 *W2, int32_t B, int32_t E,
                              int32_t F, int32_t O, tb_bf16 *q_imp, void *ws, size_t ws_bytes, int32_t *dev_status,
                              cudaStream_t stream) {

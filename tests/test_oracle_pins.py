@@ -463,3 +463,31 @@ def test_predictor_matches_torch_fp64_and_silu_identities():
     assert np.allclose(oracle.silu(v) - oracle.silu(-v), v, rtol=0, atol=1e-12)
     assert oracle.silu(0.0) == 0.0
     assert abs(oracle.silu(40.0) - 40.0) < 1e-12 and abs(oracle.silu(-40.0)) < 1e-12
+
+
+def test_ragged_step_with_equal_lengths_is_the_batched_step():
+    # the ragged oracle applies the step per sequence: with equal lengths it must equal the batched step
+    w = synth.small(B=3, Hq=4, Hkv=2, D=16, dp=8, N=100, seed=15)
+    steps, T, r, k = 5, 2, 1, 9
+    L = synth.make_layer(w, cap=w.N + steps, n=w.N)
+    arrs = []
+    for _ in range(2):
+        K = oracle.as_u16(L["K"]).copy()
+        V = oracle.as_u16(L["V"]).copy()
+        Kp = np.zeros((w.B, w.Hkv, w.N + steps, w.dp), dtype=np.uint16)
+        Kp[:, :, : w.N], _ = oracle.project(np.ascontiguousarray(K[:, :, : w.N]), L["Wk"])
+        arrs.append((K, V, Kp))
+    st = oracle.DecodeState()
+    sts = [oracle.DecodeState() for _ in range(w.B)]
+    for t in range(steps):
+        d = synth.make_step(w, 0, t, L["outlier_ch"])
+        kw = dict(q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=L["Wk"], k=k, T=T, r=r,
+                  agg=oracle.AGG_MEAN, scale=w.scale)
+        K, V, Kp = arrs[0]
+        o1, s1, c1 = oracle.decode_step(st, t, w.N + t, K=K, V=V, Kp=Kp, **kw)
+        K, V, Kp = arrs[1]
+        o2, s2, c2 = oracle.decode_step_ragged(sts, t, [w.N + t] * w.B, K=K, V=V, Kp=Kp, **kw)
+        assert np.array_equal(c1, c2) and np.array_equal(o1, o2)
+        for b, h in itertools.product(range(w.B), range(w.Hkv)):
+            assert np.array_equal(s1[b, h, : c1[b, h]], s2[b, h, : c2[b, h]])
+    assert np.array_equal(arrs[0][2], arrs[1][2])
