@@ -905,9 +905,11 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         }
         __syncthreads();
         const int n_att = n_above + (int)cnt[CN_WK];
-        // the first round's window rows are requested now
+        // the first round's window rows are requested now; while they arrive,
+        // the per-block kept counts become the blocks' first slots in idx / sel
         const int nr0 = n_att < a.stage_cap ? n_att : a.stage_cap;
         gather_rows(0, n_r1, nr0);
+        block_scan_inplace(bcnt, nblk, S.scan);
         // ---- 6. attention over the gathered rows, round by round
         MmaAttn<NT> A;
         A.m0 = A.m1 = -INFINITY;
@@ -985,8 +987,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         // words (all have passed the barrier by then).
         group_arrive(&rc->bar);
         // ---- 6d. idx / sel while the other CTAs finish: slots from the row's
-        // per-block kept counts
-        block_scan_inplace(bcnt, nblk, S.scan);
+        // per-block kept counts (scanned above)
         {
             int32_t *irow = a.idx + (int64_t)row * a.k;
             int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
