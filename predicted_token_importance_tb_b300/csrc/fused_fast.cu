@@ -244,6 +244,52 @@ __device__ __forceinline__ void warp_find_fine(const uint32_t *fine, uint32_t ba
     __syncwarp();
 }
 
+// Exclusive prefix over n <= 8 blockDim.x shared counters in place (v 16-byte
+// aligned; all threads call): eight consecutive counters per thread in two
+// 16-byte loads, a warp scan, the warps' totals through scratch (>= 32
+// words), one barrier between.
+__device__ __forceinline__ void scan8_inplace(uint32_t *v, int n, uint32_t *scratch) {
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int x0 = 8 * t;
+    uint32_t a[8];
+    if (x0 + 8 <= n) {
+        const uint4 p = *reinterpret_cast<const uint4 *>(v + x0), q = *reinterpret_cast<const uint4 *>(v + x0 + 4);
+        a[0] = p.x; a[1] = p.y; a[2] = p.z; a[3] = p.w;
+        a[4] = q.x; a[5] = q.y; a[6] = q.z; a[7] = q.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = x0 + j < n ? v[x0 + j] : 0u;
+    }
+    uint32_t loc = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) loc += a[j];
+    uint32_t inc = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    uint32_t run = inc - loc;
+    for (int w = 0; w < warp; ++w) run += scratch[w];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t c = a[j];
+        a[j] = run;
+        run += c;
+    }
+    if (x0 + 8 <= n) {
+        *reinterpret_cast<uint4 *>(v + x0) = make_uint4(a[0], a[1], a[2], a[3]);
+        *reinterpret_cast<uint4 *>(v + x0 + 4) = make_uint4(a[4], a[5], a[6], a[7]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (x0 + j < n) v[x0 + j] = a[j];
+    }
+    __syncthreads();
+}
+
 // Exclusive prefix over n shared counters in place (all threads call).
 __device__ __forceinline__ void block_scan_inplace(uint32_t *v, int n, uint32_t *scan) {
     const int per = (n + blockDim.x - 1) / blockDim.x;
@@ -909,7 +955,8 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         // the per-block kept counts become the blocks' first slots in idx / sel
         const int nr0 = n_att < a.stage_cap ? n_att : a.stage_cap;
         gather_rows(0, n_r1, nr0);
-        block_scan_inplace(bcnt, nblk, S.scan);
+        if (nblk <= 8 * kFFThreads) scan8_inplace(bcnt, nblk, S.scan);
+        else block_scan_inplace(bcnt, nblk, S.scan);
         // ---- 6. attention over the gathered rows, round by round
         MmaAttn<NT> A;
         A.m0 = A.m1 = -INFINITY;
