@@ -61,7 +61,7 @@ struct FFHdr {
 };
 constexpr int kFFRecBytes = kFastRecBytes;
 static_assert(sizeof(FFHdr) == 32, "record header is 32 bytes");
-static_assert(kFFKpGroups <= 8, "cp_async_wait_pending covers eight groups");
+static_assert(kFFKpGroups == 4, "four commit groups (40, 30, 20, 10 % of the blocks)");
 
 struct FFArgs {
     const uint16_t *q, *q_imp, *K_new, *V_new, *Wk;
@@ -555,14 +555,17 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     if (owner) append_issue<DT, DP>(a.K_new, a.V_new, a.Wk, row, h, wsm, kvn);   // (in commit group 0)
 
     // ---- 1a. Kp blocks -> shared memory: 16-byte cp.async by every thread,
-    // consecutive threads on consecutive chunks; owned block j belongs to
-    // commit group j / gsz, so scoring can start on the first groups
-    const int gsz = (nb + kFFKpGroups - 1) / kFFKpGroups > 0 ? (nb + kFFKpGroups - 1) / kFFKpGroups : 1;
+    // consecutive threads on consecutive chunks, in commit groups of 40, 30,
+    // 20 and 10 % of the CTA's blocks: scoring starts on the first groups,
+    // and little of it is left once the last one lands
+    const int gb1 = (4 * nb) / 10, gb2 = (7 * nb) / 10, gb3 = (9 * nb) / 10;   // first blocks of groups 1..3
+    auto group_of = [&](int j) -> int { return (j >= gb1) + (j >= gb2) + (j >= gb3); };
     {
         constexpr int CPB = 32 * DP * 2 / 16;   // 16-byte chunks per block
         const uint16_t *Kpr = a.Kp + (int64_t)row * a.cap * DP;
         for (int g = 0; g < kFFKpGroups; ++g) {
-            const int j0 = g * gsz, j1 = min(nb, j0 + gsz);
+            const int j0 = g == 0 ? 0 : g == 1 ? gb1 : g == 2 ? gb2 : gb3;
+            const int j1 = g == 0 ? gb1 : g == 1 ? gb2 : g == 2 ? gb3 : nb;
             for (int x = threadIdx.x; x < (j1 - j0) * CPB; x += blockDim.x) {
                 const int j = j0 + x / CPB, ch = x % CPB;
                 const int64_t blk = (int64_t)c + (int64_t)j * C;
@@ -592,11 +595,11 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         int grp = -1;
         // the owner's appended token: local row and the group of its block
         const int en = (blk_n / C) * 32 + (int)(a.n & 31);
-        const int g_n = owner ? (blk_n / C) / gsz : -1;
+        const int g_n = owner ? group_of(blk_n / C) : -1;
         for (int tt = 0; tt < ntile; tt += kFFWarps) {
             // every thread waits for its own copies of the group, then the CTA
             // barrier makes all threads' copies of it visible
-            const int gt = min((tt + kFFWarps - 1) >> 1, nb - 1) / gsz;   // last group any warp needs now
+            const int gt = group_of(min((tt + kFFWarps - 1) >> 1, nb - 1));   // last group any warp needs now
             while (grp < gt) {
                 ++grp;
                 cp_async_wait_pending(kFFKpGroups - 1 - grp);
