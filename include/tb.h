@@ -277,8 +277,9 @@ typedef struct {
  * at a prediction (plus the steps of the interval). *proj_end (host scalar)
  * is the number of rows Kp holds; start it at the rows projected before
  * (for instance by tb_project_append at prefill). sel_stride must be at least
- * min(S, n_t) + min(P - S, kc (2r+1)) + (n_t - max(P, min(S, n_t))) + T - 1
- * at every prediction (else TB_ERR_INVALID_ARG). params->flags may hold
+ * min(S, n_t) + min(P - S, kc (2r+1)) + (n_t - max(P, min(S, n_t))) at every
+ * prediction (else TB_ERR_INVALID_ARG), and each later step of the interval
+ * adds one entry (TB_ERR_INVALID_ARG on the device when it does not fit). params->flags may hold
  * TB_STEP_BUDGET_NEIGHBOURS; the step always runs as separate kernels.
  * Pointers and layouts as for tb_decode_step.
  */

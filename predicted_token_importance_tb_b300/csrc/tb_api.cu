@@ -375,7 +375,8 @@ tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *p
     if (predict) {
         int64_t body = (int64_t)kc * (2 * (int64_t)p->r + 1);
         if (body > nc) body = nc;
-        if ((int64_t)sel_stride < pre + body + (n_t - tail0) + (p->T - 1)) return TB_ERR_INVALID_ARG;
+        if ((int64_t)sel_stride < pre + body + (n_t - tail0)) return TB_ERR_INVALID_ARG;   // (the interval's
+        // later steps add one entry each; the append kernel checks those on the device)
     }
     const int rows = shape->B * shape->Hkv;
     const WsLayout L = layout_for(*shape, n_t, sel_stride, 0);

@@ -107,3 +107,15 @@ def test_buffered_prefill_far_behind_and_budget_neighbours():
 def test_buffered_host_kv():
     w = synth.small(B=1, Hq=8, Hkv=2, D=128, dp=32, N=800, k=50, seed=54, outliers=2)
     run_buffered_parity(w, n0=w.N, steps=4, S=4, W=32, T=2, r=1, k=50, P0=700, kv_host=True)
+
+
+def test_buffered_window_wider_than_the_batches_so_far():
+    # W above the unprojected span: no batch is projected, the candidates are the prefill rows
+    w = synth.small(B=1, Hq=8, Hkv=2, D=64, dp=16, N=500, k=20, seed=55)
+    run_buffered_parity(w, n0=w.N, steps=3, S=0, W=300, T=1, r=0, k=20, P0=400, agg=1)
+
+
+def test_buffered_sink_covers_every_projected_row():
+    # S >= proj_end: no candidates at all; the selection is the sink and the window
+    w = synth.small(B=2, Hq=4, Hkv=2, D=128, dp=32, N=300, k=10, seed=56)
+    run_buffered_parity(w, n0=w.N, steps=3, S=280, W=64, T=2, r=1, k=10, P0=200)

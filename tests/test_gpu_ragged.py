@@ -19,8 +19,9 @@ def _lib():
     tb.load_library()
 
 
-@pytest.mark.parametrize("T,r,ns", [(1, 0, [1500, 2201, 3000]), (2, 1, [2999, 1024, 1777]), (3, 2, [700, 701, 1600])])
-def test_ragged_batch_matches_oracle(T, r, ns):
+@pytest.mark.parametrize("T,r,ns,agg,bn", [(1, 0, [1500, 2201, 3000], 0, False), (2, 1, [2999, 1024, 1777], 0, False),
+                                          (3, 2, [700, 701, 1600], 0, False), (2, 1, [900, 2500], 1, True)])
+def test_ragged_batch_matches_oracle(T, r, ns, agg, bn):
     steps = 5
     B = len(ns)
     w = synth.small(B=B, Hq=8, Hkv=2, D=128, dp=32, N=max(ns), k=100, seed=61 + T, outliers=2)
@@ -30,7 +31,7 @@ def test_ragged_batch_matches_oracle(T, r, ns):
     K, V, Wk = L["K"].cuda(), L["V"].cuda(), L["Wk"].cuda()
     Kp = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
     tb.tb_project_append(shape, K, cap, Wk, Kp, 0, max(ns))
-    dec = tb.RaggedDecodeLayer(shape, w.k, T=T, r=r, scale=w.scale, n_max=cap - 1)
+    dec = tb.RaggedDecodeLayer(shape, w.k, T=T, r=r, agg=agg, scale=w.scale, n_max=cap - 1, budget_neighbours=bn)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
     oK, oV, oKp = u16(L["K"]).copy(), u16(L["V"]).copy(), u16(Kp).copy()
     sts = [oracle.DecodeState() for _ in range(B)]
@@ -43,7 +44,8 @@ def test_ragged_batch_matches_oracle(T, r, ns):
         torch.cuda.synchronize()
         tb.check_dev_status(dec.status, f"step {t}")
         oracle.decode_step_ragged(sts, t, cur, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"],
-                                  Wk=L["Wk"], K=oK, V=oV, Kp=oKp, k=w.k, T=T, r=r, agg=0, scale=w.scale)
+                                  Wk=L["Wk"], K=oK, V=oV, Kp=oKp, k=w.k, T=T, r=r, agg=agg, scale=w.scale,
+                                  budget_neighbours=bn)
         gidx = dec.idx_state.cpu().numpy()
         gsel, gcnt = dec.sel.cpu().numpy(), dec.counts.cpu().numpy()
         for b, n in enumerate(cur):
@@ -56,8 +58,8 @@ def test_ragged_batch_matches_oracle(T, r, ns):
             oKp[b, :, n] = g[0, :, 0]            # both score the GPU's row from here on
             assert dec.n_pred[b] == sts[b].n_pred
             if t % T == 0:
-                s_ref, _ = oracle.score(d["q_imp"][b:b + 1], np.ascontiguousarray(oKp[b:b + 1, :, : n + 1]))
-                assert_topk_end_to_end(gidx[b:b + 1], s_ref, w.k)
+                s_ref, _ = oracle.score(d["q_imp"][b:b + 1], np.ascontiguousarray(oKp[b:b + 1, :, : n + 1]), agg)
+                assert_topk_end_to_end(gidx[b:b + 1], s_ref, dec.kc)
             want, wcnt = oracle.expand(gidx[b:b + 1], r, sts[b].n_pred, n + 1, sel_stride=dec.sel_stride)
             assert np.array_equal(gcnt[b], wcnt[0])
             for h in range(w.Hkv):
