@@ -149,7 +149,7 @@ __device__ bool chunk_select_attend(AttnLane<GM> &A, RowCtl *rc, SelectSmem &S, 
         const uint32_t bpos = block_exclusive_scan(bf, S.scan, btot);
         if (kept) {
             const uint32_t slot = R.offset + base_kept + pos;
-            irow[slot] = (int32_t)(t0 + e);
+            if (irow) irow[slot] = (int32_t)(t0 + e);
             srow[slot] = (int32_t)(t0 + e);
         }
         if (bf) list[n_bin + bpos] = e;

@@ -75,6 +75,7 @@ struct FFArgs {
     uint32_t *keys_g;    // rows x keys_stride: keys in token order (general path)
     int32_t *dev_status;
     int64_t cap, n, keys_stride;
+    int64_t keep_lo, keep_hi;   // tokens t < keep_lo or t >= keep_hi are always kept (maximal key)
     int Hq, Hkv, D, k, agg, sel_stride;
     float scale;
     int C, NB, blk_stride, stage_cap;
@@ -678,7 +679,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 const int e = tw * 16 + g + 8 * q;
                 uint32_t key = 0;
                 if (e < Lv) {
-                    key = score_key(q ? v1 : v0, nan_seen);
+                    const int64_t t = tok_of(e);
+                    // forced tokens (their Kp rows need not exist) rank above every score
+                    key = (t < a.keep_lo || t >= a.keep_hi) ? 0xFFFFFFFFu : score_key(q ? v1 : v0, nan_seen);
                     atomicAdd(&S.hist[key >> 21], 1u);
                 }
                 S.keys[e] = key;
@@ -1039,7 +1042,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         // ---- 6d. idx / sel while the other CTAs finish: slots from the row's
         // per-block kept counts (scanned above)
         {
-            int32_t *irow = a.idx + (int64_t)row * a.k;
+            int32_t *irow = a.idx ? a.idx + (int64_t)row * a.k : nullptr;
             int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
             for (int e = threadIdx.x; e < nb * 32; e += blockDim.x) {
                 const int64_t t = tok_of(e);
@@ -1047,7 +1050,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
                 const uint32_t slot = bcnt[t >> 5] + (uint32_t)__popc(km & ((1u << lane) - 1u));
                 if (kp && slot < (uint32_t)a.k) {
-                    irow[slot] = (int32_t)t;
+                    if (irow) irow[slot] = (int32_t)t;
                     srow[slot] = (int32_t)t;
                 }
                 if (kp && slot >= (uint32_t)a.k) set_status(a.dev_status, TB_ERR_INVALID_ARG);
@@ -1069,7 +1072,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         FFGeneral gp;
         gp.rc = rc;
         gp.kg = a.keys_g + (int64_t)row * a.keys_stride;
-        gp.irow = a.idx + (int64_t)row * a.k;
+        gp.irow = a.idx ? a.idx + (int64_t)row * a.k : nullptr;
         gp.srow = a.sel + (int64_t)row * a.sel_stride;
         gp.dev_status = a.dev_status;
         gp.Kh = Kh;
@@ -1184,7 +1187,8 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
                               const uint16_t *q_imp, const uint16_t *K_new, const uint16_t *V_new,
                               const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx_state,
                               int32_t *sel, int32_t *counts, uint16_t *out, const FastWs &w, int32_t sel_stride,
-                              int32_t *dev_status, cudaStream_t st) {
+                              int32_t *dev_status, cudaStream_t st, int32_t k_keep, int64_t keep_lo,
+                              int64_t keep_hi) {
     FFPlan P;
     if (!ff_plan(sh, n + 1, P)) return cudaErrorNotSupported;
     FFArgs a;
@@ -1194,7 +1198,10 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
     a.ctl = w.ctl; a.part = w.part; a.rec = w.rec; a.blk_above = w.blk_above; a.keys_g = w.keys_g;
     a.dev_status = dev_status;
     a.cap = sh.cap; a.n = n; a.keys_stride = w.keys_stride;
-    a.Hq = sh.Hq; a.Hkv = sh.Hkv; a.D = sh.D; a.k = p.k; a.agg = p.agg; a.sel_stride = sel_stride;
+    a.Hq = sh.Hq; a.Hkv = sh.Hkv; a.D = sh.D; a.k = k_keep > 0 ? k_keep : p.k; a.agg = p.agg;
+    a.sel_stride = sel_stride;
+    a.keep_lo = keep_lo;
+    a.keep_hi = keep_hi;
     a.scale = p.scale;
     a.C = P.C; a.NB = P.NB; a.blk_stride = (int)w.blk_stride; a.stage_cap = P.stage_cap;
     cudaLaunchConfig_t cfg = {};

@@ -379,16 +379,48 @@ tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *p
         // later steps add one entry each; the append kernel checks those on the device)
     }
     const int rows = shape->B * shape->Hkv;
-    const WsLayout L = layout_for(*shape, n_t, sel_stride, 0);
+    // a prediction at every step without neighbours runs as the single-launch
+    // step: the sink and window tokens take the maximal key, so keeping
+    // k_keep = sink + kc + window tokens keeps exactly them and the top kc
+    // candidates, in ascending order
+    const int32_t k_keep = (int32_t)(pre + kc + (n_t - tail0));
+    const bool one_launch = predict && p->T == 1 && p->r == 0 && !(p->flags & TB_STEP_UNFUSED) &&
+                            (int64_t)sel_stride >= k_keep && fused_fast_supported(*shape, n_t, k_keep);
+    const WsLayout L = layout_for(*shape, n_t, sel_stride, one_launch ? fused_chunks(*shape, n_t) : 0);
     if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
     uint8_t *w = static_cast<uint8_t *>(ws);
     RowCtl *ctl = reinterpret_cast<RowCtl *>(w + L.rowctl_off);
     uint32_t *actl = reinterpret_cast<uint32_t *>(w + L.attn_ctl_off);
     float *part = reinterpret_cast<float *>(w + L.part_off);
     float *scores = reinterpret_cast<float *>(w + L.scores_off);
+    cudaError_t e;
+    if (one_launch) {
+        if (P > *proj_end) {   // the batches that left the window first
+            e = launch_project(*shape, K + *proj_end * shape->D, shape->cap, Wk, Kp, *proj_end, P - *proj_end,
+                               dev_status, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            *proj_end = P;
+        }
+        FastWs fw;
+        fw.ctl = ctl;
+        fw.part = part;
+        fw.rec = w + L.rec_off;
+        fw.blk_above = w + L.blk_off;
+        fw.blk_stride = L.blk_stride;
+        fw.keys_g = reinterpret_cast<uint32_t *>(scores);
+        fw.keys_stride = n_t;
+        // candidates [S, P): everything outside is forced (with P <= S, everything)
+        e = launch_fused_fast(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, nullptr, sel, counts, out, fw,
+                              sel_stride, dev_status, stream, k_keep, S, P > S ? P : S);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = launch_centres_from_sel(rows, sel, sel_stride, pre, kc, S, idx_state, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        *n_pred = n_t;
+        return TB_OK;
+    }
     // 1. append K/V (and, inside an interval, the tail entry of the selection)
-    cudaError_t e = launch_append(*shape, K_new, V_new, nullptr, K, V, nullptr, n, predict ? nullptr : sel, sel_stride,
-                                  counts, dev_status, stream);
+    e = launch_append(*shape, K_new, V_new, nullptr, K, V, nullptr, n, predict ? nullptr : sel, sel_stride,
+                      counts, dev_status, stream);
     if (e != cudaSuccess) return from_cuda(e);
     if (predict) {
         // 2. the batches that left the window -> Kp; score the candidates, select, widen, add sink and window
