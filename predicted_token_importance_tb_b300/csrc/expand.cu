@@ -96,18 +96,4 @@ cudaError_t launch_expand_ranges(int rows, const int32_t *idx, int32_t k, int32_
     return cudaGetLastError();
 }
 
-__global__ void centres_kernel(const int32_t *__restrict__ sel, int32_t sel_stride, int64_t pre, int32_t kc,
-                               int64_t base, int32_t *__restrict__ idx) {
-    const int row = blockIdx.x;
-    for (int j = threadIdx.x; j < kc; j += blockDim.x)
-        idx[(int64_t)row * kc + j] = (int32_t)(sel[(int64_t)row * sel_stride + pre + j] - base);
-}
-
-cudaError_t launch_centres_from_sel(int rows, const int32_t *sel, int32_t sel_stride, int64_t pre, int32_t kc,
-                                    int64_t base, int32_t *idx, cudaStream_t st) {
-    if (rows <= 0 || kc <= 0) return cudaSuccess;
-    centres_kernel<<<rows, 256, 0, st>>>(sel, sel_stride, pre, kc, base, idx);
-    return cudaGetLastError();
-}
-
 }  // namespace tb

@@ -76,6 +76,9 @@ struct FFArgs {
     int32_t *dev_status;
     int64_t cap, n, keys_stride;
     int64_t keep_lo, keep_hi;   // tokens t < keep_lo or t >= keep_hi are always kept (maximal key)
+    int32_t *centres;           // if set: the kept tokens of [keep_lo, keep_hi) minus keep_lo, ck per row,
+    int64_t cpre;               // taken from slots cpre .. cpre + ck of each sel row
+    int ck;
     int Hq, Hkv, D, k, agg, sel_stride;
     float scale;
     int C, NB, blk_stride, stage_cap;
@@ -1052,6 +1055,8 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 if (kp && slot < (uint32_t)a.k) {
                     if (irow) irow[slot] = (int32_t)t;
                     srow[slot] = (int32_t)t;
+                    if (a.centres && t >= a.keep_lo && t < a.keep_hi)
+                        a.centres[(int64_t)row * a.ck + ((int64_t)slot - a.cpre)] = (int32_t)(t - a.keep_lo);
                 }
                 if (kp && slot >= (uint32_t)a.k) set_status(a.dev_status, TB_ERR_INVALID_ARG);
             }
@@ -1090,9 +1095,14 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         gp.scale = a.scale;
         if (!ff_general_path<GM>(gp, S, stok, reinterpret_cast<float *>(X))) return;
         if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
-        // ---- 7. the row's last CTA merges
-        (void)row_merge_last(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT, &cnt[CN_FLAG],
-                             true, a.dev_status, reinterpret_cast<float *>(X));
+        // ---- 7. the row's last CTA merges (and copies the centres, when asked, from the finished sel row)
+        if (row_merge_last(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT, &cnt[CN_FLAG],
+                           true, a.dev_status, reinterpret_cast<float *>(X)) &&
+            a.centres) {
+            const int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
+            for (int j = threadIdx.x; j < a.ck; j += blockDim.x)
+                a.centres[(int64_t)row * a.ck + j] = __ldcg(srow + a.cpre + j) - (int32_t)a.keep_lo;
+        }
     }
 }
 
@@ -1188,7 +1198,7 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
                               const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx_state,
                               int32_t *sel, int32_t *counts, uint16_t *out, const FastWs &w, int32_t sel_stride,
                               int32_t *dev_status, cudaStream_t st, int32_t k_keep, int64_t keep_lo,
-                              int64_t keep_hi) {
+                              int64_t keep_hi, int32_t *centres, int64_t cpre, int32_t ck) {
     FFPlan P;
     if (!ff_plan(sh, n + 1, P)) return cudaErrorNotSupported;
     FFArgs a;
@@ -1202,6 +1212,9 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
     a.sel_stride = sel_stride;
     a.keep_lo = keep_lo;
     a.keep_hi = keep_hi;
+    a.centres = ck > 0 ? centres : nullptr;
+    a.cpre = cpre;
+    a.ck = ck;
     a.scale = p.scale;
     a.C = P.C; a.NB = P.NB; a.blk_stride = (int)w.blk_stride; a.stage_cap = P.stage_cap;
     cudaLaunchConfig_t cfg = {};

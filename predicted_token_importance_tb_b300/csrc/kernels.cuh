@@ -82,11 +82,12 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
                               const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx_state,
                               int32_t *sel, int32_t *counts, uint16_t *out, const FastWs &w, int32_t sel_stride,
                               int32_t *dev_status, cudaStream_t st, int32_t k_keep = 0, int64_t keep_lo = 0,
-                              int64_t keep_hi = INT64_MAX);
-// idx[row][j] = sel[row][pre + j] - base for j < kc (the centres of a buffered
-// step's selection, relative to its first candidate).
-cudaError_t launch_centres_from_sel(int rows, const int32_t *sel, int32_t sel_stride, int64_t pre, int32_t kc,
-                                    int64_t base, int32_t *idx, cudaStream_t st);
+                              int64_t keep_hi = INT64_MAX, int32_t *centres = nullptr, int64_t cpre = 0,
+                              int32_t ck = 0);
+// k_keep > 0: keep that many tokens instead of p.k, with the tokens outside
+// [keep_lo, keep_hi) forced in (maximal key); centres (ck per row, may be
+// null) then receive the kept tokens of [keep_lo, keep_hi) minus keep_lo,
+// which sit at sel slots cpre .. cpre + ck.
 
 // The predictor MLP for B tokens: h [B, F] = SiLU(x W1^T) (fp32), q_imp [B, O] =
 // RNE(h W2^T). E and F multiples of 8, B <= 16.

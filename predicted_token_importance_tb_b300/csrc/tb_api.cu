@@ -411,9 +411,7 @@ tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *p
         fw.keys_stride = n_t;
         // candidates [S, P): everything outside is forced (with P <= S, everything)
         e = launch_fused_fast(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, nullptr, sel, counts, out, fw,
-                              sel_stride, dev_status, stream, k_keep, S, P > S ? P : S);
-        if (e != cudaSuccess) return from_cuda(e);
-        e = launch_centres_from_sel(rows, sel, sel_stride, pre, kc, S, idx_state, stream);
+                              sel_stride, dev_status, stream, k_keep, S, P > S ? P : S, idx_state, pre, kc);
         if (e != cudaSuccess) return from_cuda(e);
         *n_pred = n_t;
         return TB_OK;
