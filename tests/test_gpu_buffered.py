@@ -20,7 +20,8 @@ def _lib():
     tb.load_library()
 
 
-def run_buffered_parity(w, n0, steps, S, W, T, r, k, P0, kv_host=False, budget_neighbours=False, agg=0):
+def run_buffered_parity(w, n0, steps, S, W, T, r, k, P0, kv_host=False, budget_neighbours=False, agg=0,
+                        layer_hook=None):
     """Drive the buffered step on the GPU; check, every step, the batches of Kp (1 ulp of the oracle's
     projection, then adopted by the oracle so both score identical inputs), the centres (top-k under the
     tie band), the selection exactly (the oracle's construction from the GPU's centres), and the output
@@ -28,6 +29,8 @@ def run_buffered_parity(w, n0, steps, S, W, T, r, k, P0, kv_host=False, budget_n
     cap = n0 + steps
     shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, cap)
     L = synth.make_layer(w, cap=cap, n=n0)
+    if layer_hook is not None:
+        layer_hook(L)
     K, V, Wk = L["K"].cuda(), L["V"].cuda(), L["Wk"].cuda()
     Kp = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
     tb.tb_project_append(shape, K, cap, Wk, Kp, 0, P0)
@@ -119,3 +122,21 @@ def test_buffered_sink_covers_every_projected_row():
     # S >= proj_end: no candidates at all; the selection is the sink and the window
     w = synth.small(B=2, Hq=4, Hkv=2, D=128, dp=32, N=300, k=10, seed=56)
     run_buffered_parity(w, n0=w.N, steps=3, S=280, W=64, T=2, r=1, k=10, P0=200)
+
+
+def test_buffered_single_launch_general_select():
+    # blocky scores send the single-launch step to its general select; the centres then come from the
+    # row's merging CTA
+    from test_gpu_decode import general_select_steps
+    w = synth.small(B=1, Hq=32, Hkv=8, D=128, dp=32, N=32767, k=3277, seed=57, outliers=4)
+
+    def hot_blocks(L):
+        g = torch.Generator().manual_seed(77)
+        nblk = L["K"].shape[2] // 32
+        hot = torch.randperm(nblk, generator=g)[: nblk // 10]
+        rows = (hot[:, None] * 32 + torch.arange(32)[None, :]).reshape(-1)
+        rows = rows[rows < L["K"].shape[2]]
+        L["K"][:, :, rows] = L["K"][:, :, rows] * 8
+
+    dec = run_buffered_parity(w, n0=w.N, steps=2, S=64, W=256, T=1, r=0, k=3277, P0=32256, layer_hook=hot_blocks)
+    assert sum(general_select_steps(dec)) > 0
