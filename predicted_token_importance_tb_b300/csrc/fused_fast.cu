@@ -481,7 +481,9 @@ __device__ __noinline__ bool ff_general_path(const FFGeneral g, SelectSmem S, in
     return true;
 }
 
-template <int CPT, int DT, int GM>
+// FK: the forced-keep variant (sink / window tokens at the maximal key,
+// centres written); the plain step compiles without that code.
+template <int CPT, int DT, int GM, bool FK>
 __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs a) {
     extern __shared__ __align__(128) uint8_t smb[];
     constexpr int DP = CPT * 8;
@@ -592,6 +594,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     // m16n8k16; per token the G dot products are averaged (or maxed), then the
     // order-preserving key and its coarse bin
     bool nan_seen = false;
+    const bool forcing = FK && (a.keep_lo > 0 || a.keep_hi < n_t);   // (uniform)
     {
         const int g = lane >> 2, q = lane & 3;
         const float invG = 1.0f / (float)G;
@@ -682,9 +685,13 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 const int e = tw * 16 + g + 8 * q;
                 uint32_t key = 0;
                 if (e < Lv) {
-                    const int64_t t = tok_of(e);
                     // forced tokens (their Kp rows need not exist) rank above every score
-                    key = (t < a.keep_lo || t >= a.keep_hi) ? 0xFFFFFFFFu : score_key(q ? v1 : v0, nan_seen);
+                    bool forced = false;
+                    if (forcing) {
+                        const int64_t t = tok_of(e);
+                        forced = t < a.keep_lo || t >= a.keep_hi;
+                    }
+                    key = forced ? 0xFFFFFFFFu : score_key(q ? v1 : v0, nan_seen);
                     atomicAdd(&S.hist[key >> 21], 1u);
                 }
                 S.keys[e] = key;
@@ -1053,9 +1060,9 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
                 const uint32_t km = __ballot_sync(0xFFFFFFFFu, kp);
                 const uint32_t slot = bcnt[t >> 5] + (uint32_t)__popc(km & ((1u << lane) - 1u));
                 if (kp && slot < (uint32_t)a.k) {
-                    if (irow) irow[slot] = (int32_t)t;
+                    if (!FK || irow) irow[slot] = (int32_t)t;
                     srow[slot] = (int32_t)t;
-                    if (a.centres && t >= a.keep_lo && t < a.keep_hi)
+                    if (FK && a.centres && t >= a.keep_lo && t < a.keep_hi)
                         a.centres[(int64_t)row * a.ck + ((int64_t)slot - a.cpre)] = (int32_t)(t - a.keep_lo);
                 }
                 if (kp && slot >= (uint32_t)a.k) set_status(a.dev_status, TB_ERR_INVALID_ARG);
@@ -1098,7 +1105,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         // ---- 7. the row's last CTA merges (and copies the centres, when asked, from the finished sel row)
         if (row_merge_last(rc, prow, C, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT, &cnt[CN_FLAG],
                            true, a.dev_status, reinterpret_cast<float *>(X)) &&
-            a.centres) {
+            FK && a.centres) {
             const int32_t *srow = a.sel + (int64_t)row * a.sel_stride;
             for (int j = threadIdx.x; j < a.ck; j += blockDim.x)
                 a.centres[(int64_t)row * a.ck + j] = __ldcg(srow + a.cpre + j) - (int32_t)a.keep_lo;
@@ -1117,14 +1124,18 @@ static int ff_gm(int G) { return G <= 1 ? 1 : G <= 4 ? 4 : 16; }
 
 template <int CPT, int DT, int GM>
 static int ff_occupancy(size_t smem) {
-    if (cudaFuncSetAttribute(fused_fast_kernel<CPT, DT, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fused_fast_kernel<CPT, DT, GM, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(fused_fast_kernel<CPT, DT, GM, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return 0;
-    int per = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fused_fast_kernel<CPT, DT, GM>, kFFThreads, smem) !=
-        cudaSuccess)
+    int per = 0, per_fk = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fused_fast_kernel<CPT, DT, GM, false>, kFFThreads, smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_fk, fused_fast_kernel<CPT, DT, GM, true>, kFFThreads,
+                                                      smem) != cudaSuccess)
         return 0;
-    return per;
+    return per < per_fk ? per : per_fk;
 }
 
 #define TB_FF_CASES(X) X(2, 64, 1) X(2, 64, 4) X(2, 64, 16) X(2, 128, 1) X(2, 128, 4) X(2, 128, 16) \
@@ -1227,8 +1238,10 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-#define TB_FF_LAUNCH(CP, DTT, GMC) \
-    if (P.cpt == CP && sh.D == DTT && P.gm == GMC) return cudaLaunchKernelEx(&cfg, fused_fast_kernel<CP, DTT, GMC>, a);
+#define TB_FF_LAUNCH(CP, DTT, GMC)                                                          \
+    if (P.cpt == CP && sh.D == DTT && P.gm == GMC)                                          \
+        return k_keep > 0 ? cudaLaunchKernelEx(&cfg, fused_fast_kernel<CP, DTT, GMC, true>, a) \
+                          : cudaLaunchKernelEx(&cfg, fused_fast_kernel<CP, DTT, GMC, false>, a);
     TB_FF_CASES(TB_FF_LAUNCH)
 #undef TB_FF_LAUNCH
     return cudaErrorNotSupported;
