@@ -212,8 +212,8 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
 
 /*
  * tb_decode_step for a ragged batch: sequence b holds n[b] tokens before
- * this step's append (SURVEY's f4 variant; the pages batch sequences without
- * saying how). Per sequence the step is exactly tb_decode_step's: the new
+ * this step's append (the pages batch sequences without saying how they may
+ * differ in length). Per sequence the step is exactly tb_decode_step's: the new
  * K/V/Kp rows go to position n[b], a prediction scores that sequence's
  * n[b] + 1 tokens and keeps the top k, the widening stays inside them, and
  * between predictions the sequence's new token joins its selection.

@@ -8,7 +8,9 @@ The arithmetic lives in ``tb_oracle.c`` (plain C, fp64, OpenMP over
 independent (batch, KV head) rows); this module compiles it with gcc when the
 shared object is missing or stale and marshals numpy arrays in and out. The
 only logic written here in Python is the step orchestration of the prediction
-interval (``decode_steps``), which is host-side control flow.
+interval and of the buffers (``decode_step``, ``decode_step_buffered``,
+``decode_step_ragged``), which is host-side control flow, and the predictor
+MLP (``predict_queries``: two numpy matmuls and SiLU in fp64).
 
 Sources: "TokenButler: Token Importance is Predictable" -- the arXiv abstract
 (searcharxiv.com / fugumt.com pages) and the gist.science technical summary,
@@ -16,11 +18,21 @@ sections "Core Architecture", "Inference Strategy" and "Optimizations".
 
 Parity status per function:
   bf16_round, project, score, topk, expand, attn   pinned by tests/test_oracle_pins.py
-  decode_steps (interval reuse + neighbour fetching + tail)
+  decode_step (interval reuse + neighbour fetching + tail)
       the reading of when to predict and what the tail is comes from no page
       (the pages give no schedule detail); its invariants (T=1 equals
       per-step selection, superset, bounds) are pinned, the schedule itself
       is "parity unpinned" by the pages.
+  centres (budget-preserving neighbours), decode_step_buffered /
+  buffered_select (sink, local window, batched projection)
+      readings of the pages' Inference Strategy and Batching; pinned by
+      brute-force rank counts and the structure of every selection, the
+      rules themselves "parity unpinned" by the pages.
+  decode_step_ragged   pinned by its equality with the batched step at equal
+      lengths.
+  silu, predict_queries   pinned against torch's SiLU and matmul in fp64 and
+      SiLU's odd-part identity; the MLP's shape is "parity unpinned" by the
+      pages.
 """
 from __future__ import annotations
 
