@@ -58,3 +58,9 @@ def test_decode_step_with_host_kv_matches_oracle(fused):
 def test_decode_interval_with_host_kv_matches_oracle():
     w = synth.small(B=1, Hq=8, Hkv=2, D=128, dp=32, N=3000, k=100, T=4, r=1, seed=44, outliers=4)
     run_decode_parity(w, n0=w.N, steps=6, kv_host=True)
+
+
+def test_llama_layer_step_with_host_kv():
+    # the 32K-token Llama-3-8B-shaped layer with its K/V in pinned host memory, through the single-launch step
+    w = synth.WORKLOADS[1]
+    run_decode_parity(w, n0=w.N - 1, steps=1, kv_host=True)

@@ -20,7 +20,8 @@ def _lib():
 
 
 @pytest.mark.parametrize("T,r,ns,agg,bn", [(1, 0, [1500, 2201, 3000], 0, False), (2, 1, [2999, 1024, 1777], 0, False),
-                                          (3, 2, [700, 701, 1600], 0, False), (2, 1, [900, 2500], 1, True)])
+                                          (3, 2, [700, 701, 1600], 0, False), (2, 1, [900, 2500], 1, True),
+                                          (1, 0, [8192, 32767], 0, False)])
 def test_ragged_batch_matches_oracle(T, r, ns, agg, bn):
     steps = 5
     B = len(ns)
