@@ -140,3 +140,14 @@ def test_buffered_single_launch_general_select():
 
     dec = run_buffered_parity(w, n0=w.N, steps=2, S=64, W=256, T=1, r=0, k=3277, P0=32256, layer_hook=hot_blocks)
     assert sum(general_select_steps(dec)) > 0
+
+
+def test_buffered_single_launch_everything_forced():
+    # S >= proj_end with a prediction at every step: the single-launch step keeps every token
+    w = synth.small(B=2, Hq=4, Hkv=2, D=128, dp=32, N=300, k=10, seed=58)
+    run_buffered_parity(w, n0=w.N, steps=2, S=280, W=64, T=1, r=0, k=10, P0=200)
+
+
+def test_buffered_single_launch_host_kv():
+    w = synth.small(B=1, Hq=8, Hkv=2, D=128, dp=32, N=4000, k=300, seed=59, outliers=2)
+    run_buffered_parity(w, n0=w.N, steps=3, S=16, W=128, T=1, r=0, k=300, P0=3700, kv_host=True)
