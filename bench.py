@@ -142,25 +142,33 @@ class ClockSampler:
 
 
 def _dist_init(n):
+    """One process per GPU under torchrun (NCCL); gloo on a host without CUDA (the replicas' host logic)."""
     if n <= 1:
         return 0, 1, None
     import torch.distributed as dist
-    dist.init_process_group("nccl")
+    cuda = torch.cuda.is_available()
+    dist.init_process_group("nccl" if cuda else "gloo")
     rank = dist.get_rank()
-    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+    if cuda:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
     return rank, dist.get_world_size(), dist
+
+
+def _dev():
+    return "cuda" if torch.cuda.is_available() else "cpu"
 
 
 def _barrier(dist):
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def _max_over_ranks(dist, x: float) -> float:
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_dev())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -168,7 +176,7 @@ def _max_over_ranks(dist, x: float) -> float:
 def _sum_over_ranks(dist, x: float) -> float:
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_dev())
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
 
