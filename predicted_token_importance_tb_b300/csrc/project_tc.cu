@@ -181,15 +181,28 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcArgs a) {
     // Wk[h]^T for every KV head, K-major with the 128-byte swizzle: element
     // (j, d) of head h lives in half kh = d / 64 at row j, byte 2*(d % 64)
     // of the row, whose 16-byte chunk index is XORed with (j % 8).
-    for (int x = threadIdx.x; x < a.Hkv * a.D * a.dp; x += blockDim.x) {
-        const int h = x / (a.D * a.dp);
-        const int rem = x % (a.D * a.dp);
-        const int d = rem / a.dp, j = rem % a.dp;
-        const int kh = d / kBoxCols, byte = (d % kBoxCols) * 2;
-        const int chunk = (byte >> 4) ^ (j & 7);
-        uint8_t *dst = smB + (size_t)h * b_head_bytes + (size_t)kh * a.dp * 128 + (size_t)j * 128 + chunk * 16 +
-                       (byte & 15);
-        *reinterpret_cast<uint16_t *>(dst) = a.Wk[x];
+    // (16-byte loads of eight consecutive j, four in flight per thread: the
+    // staging would otherwise wait out one L2 round trip per element)
+    {
+        const int n8 = a.Hkv * a.D * a.dp / 8;   // dp is a multiple of 8
+#pragma unroll 4
+        for (int x8 = threadIdx.x; x8 < n8; x8 += blockDim.x) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a.Wk) + x8);
+            const int x = 8 * x8;
+            const int h = x / (a.D * a.dp);
+            const int rem = x % (a.D * a.dp);
+            const int d = rem / a.dp, j0 = rem % a.dp;
+            const int kh = d / kBoxCols, byte = (d % kBoxCols) * 2;
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = j0 + i;
+                const int chunk = (byte >> 4) ^ (j & 7);
+                uint8_t *dst = smB + (size_t)h * b_head_bytes + (size_t)kh * a.dp * 128 + (size_t)j * 128 +
+                               chunk * 16 + (byte & 15);
+                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)(i & 1 ? wv[i >> 1] >> 16 : wv[i >> 1] & 0xFFFFu);
+            }
+        }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (threadIdx.x == 0) {
