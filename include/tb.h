@@ -120,9 +120,9 @@ TB_API tb_status tb_workspace_init(void *ws, size_t ws_bytes, cudaStream_t strea
 
 /*
  * Key projection into the low-dimensional cache ("Core Architecture",
- * Key-Cache Projection: a learned matrix maps the real keys of a consumer
- * layer to the importance space; "Optimizations", Batching: projections are
- * made for a batch of tokens at a time).
+ * Key-Cache Projection: the consumer layer's full keys are multiplied by a
+ * trained matrix into the importance space; "Optimizations", Batching: many
+ * tokens are projected in one call rather than one per step).
  *
  *   Kp[b,h,pos0+i,:] = RNE_bf16( K_src[b,h,i,:] . Wk[h] )   0 <= i < n_new
  *
@@ -137,8 +137,8 @@ TB_API tb_status tb_project_append(const tb_shape *shape, const tb_bf16 *K_src, 
                             void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /*
- * Importance scores ("Core Architecture", Scoring: the predicted queries are
- * dotted with the projected keys).
+ * Importance scores ("Core Architecture", Scoring: a token's importance is
+ * the inner product of the predicted query with its projected key).
  *
  *   s[b,h,t] = agg_{g<G} sum_i q_imp[b,h*G+g,i] * Kp[b,h,t,i]    0 <= t < n
  *
@@ -148,8 +148,8 @@ TB_API tb_status tb_score(const tb_shape *shape, const tb_bf16 *q_imp, const tb_
                    int32_t agg, float *s, int32_t *dev_status, cudaStream_t stream);
 
 /*
- * Fixed-budget per-token selection (arXiv abstract: dynamic per-token
- * selection under a fixed budget). For each (b,h) row of s [B,Hkv,n], idx
+ * Per-token selection with a fixed budget (arXiv abstract: individual tokens,
+ * k of them, are kept at each step). For each (b,h) row of s [B,Hkv,n], idx
  * receives the k tokens with the largest scores, ties to the lower index,
  * in ascending index order. 0 <= k <= n. -0.0 ties with +0.0; a NaN score
  * writes TB_ERR_NONFINITE to *dev_status (the NaN then ranks lowest).
@@ -233,8 +233,8 @@ TB_API tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_para
 /*
  * The importance-query predictor ("TokenButler: Token Importance is
  * Predictable", gist.science summary, Core Architecture, Query Prediction: a
- * lightweight MLP from a producer layer's hidden state to G low-dimensional
- * query vectors per KV head), for B tokens:
+ * small multi-layer perceptron from a producer layer's hidden state to G
+ * low-dimensional importance queries for each KV head), for B tokens:
  *   h     = SiLU(x . W1^T)          x [B, E] bf16, W1 [F, E] bf16, h fp32
  *   q_imp = RNE_bf16(h . W2^T)      W2 [O, F] bf16, q_imp [B, O] = [B, Hq, dp]
  * The pages give no depth, width, activation or bias: two layers, no bias,

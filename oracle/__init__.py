@@ -370,9 +370,9 @@ def silu(v):
 def predict_queries(x, W1, W2):
     """The importance-query predictor for B tokens.
 
-    [summary] Core Architecture, Query Prediction: a lightweight MLP maps the
-    producer layer's hidden state to G low-dimensional query vectors per KV
-    head. Reading (the pages give no depth, width, activation or bias): two
+    [summary] Core Architecture, Query Prediction: a small multi-layer
+    perceptron turns the producer layer's hidden state into G low-dimensional
+    importance queries for each KV head. Reading (the pages give no depth, width, activation or bias): two
     bias-free layers with SiLU between them, h = SiLU(x W1^T), q_imp =
     RNE_bf16(h W2^T), exact products and fp64 sums here.
     x [B, E], W1 [F, E], W2 [O, F] bf16 bits -> (q_imp bits [B, O], fp64 [B, O], h fp64 [B, F]).

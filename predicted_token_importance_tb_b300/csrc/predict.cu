@@ -1,7 +1,7 @@
 // The importance-query predictor's forward pass ("TokenButler: Token
 // Importance is Predictable", gist.science summary, Core Architecture, Query
-// Prediction: a lightweight MLP maps a producer layer's hidden state to G
-// low-dimensional query vectors per KV head).
+// Prediction: a small multi-layer perceptron turns a producer layer's hidden
+// state into G low-dimensional importance queries for each KV head).
 //
 //   h = SiLU(x W1^T)      x [B, E] bf16, W1 [F, E] bf16, h [B, F] fp32
 //   q_imp = RNE_bf16(h W2^T)            W2 [O, F] bf16, O = Hq dp

@@ -1,7 +1,7 @@
 // Distributed exact top-k (radix select) over one row held by a group of CTAs.
 //
 // Selection rule ("TokenButler: Token Importance is Predictable", arXiv
-// abstract: per-token selection under a fixed budget): keep the k tokens of
+// abstract: individual tokens are kept, k of them per row): keep the k tokens of
 // the row with the largest scores; ties go to the lower token index. Ordering
 // is by the 64-bit composite (key << 32) | (~token), key the order-preserving
 // image of the fp32 score, so every element has a distinct rank and the
