@@ -73,16 +73,17 @@ def _workload(name):
 
 def _traffic(workload: str):
     """DRAM bytes per launch of the step kernel from the committed ncu capture,
-    or None when the capture was taken on another workload or another build
-    of the library (the record carries the library's source hash)."""
+    or None when the capture was taken on another workload or on different
+    library code (the record carries the code hash: sources and headers with
+    comments removed, plus the compiler flags)."""
+    from predicted_token_importance_tb_b300 import build
     try:
         with open(os.path.join(ROOT, "profiles", "fused_fast_traffic.json")) as f:
             rec = json.load(f)
-        with open(os.path.join(ROOT, "predicted_token_importance_tb_b300", "libtb.so.buildhash")) as f:
-            build = f.read().strip()
+        code = build.code_hash()
     except (OSError, ValueError):
         return None
-    if rec.get("workload") != workload or rec.get("library_build_hash") != build:
+    if rec.get("workload") != workload or rec.get("code_hash") != code:
         return None
     return int(rec["dram_bytes_per_launch"])
 

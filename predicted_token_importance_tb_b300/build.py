@@ -45,6 +45,45 @@ def _hash() -> str:
     return h.hexdigest()
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs folded to one
+    space: two sources that compile to the same code (up to line numbers)
+    give the same text."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":                          # string or character literal, escapes kept
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def code_hash() -> str:
+    """Hash of the library's code: every source and header with comments and
+    layout removed, plus the compiler flags. A profile taken on one build
+    stays valid for another with the same code hash."""
+    h = hashlib.sha256()
+    for p in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "tb.h")]:
+        h.update(os.path.basename(p).encode())
+        with open(p, encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
 def nvcc() -> str:
     for c in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
         if c and (os.path.sep not in c or os.path.exists(c)):
