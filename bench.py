@@ -61,6 +61,9 @@ def _args():
                     help="S,W: sink and local-window buffers with batched key projection; prints its own line")
     ap.add_argument("--offload", action="store_true",
                     help="K/V in pinned host memory (the offloaded cache); prints its own line")
+    ap.add_argument("--prefill", action="store_true",
+                    help="the key projection of a whole prefill (tcgen05), on the B=2, N=65536 prefill "
+                         "workload unless --workload names another; prints its own line")
     return ap.parse_args()
 
 
@@ -74,14 +77,14 @@ def _workload(name):
 def _traffic(workload: str):
     """DRAM bytes per launch of the step kernel from the committed ncu capture,
     or None when the capture was taken on another workload or on different
-    library code (the record carries the code hash: sources and headers with
-    comments removed, plus the compiler flags)."""
+    code (the record carries the code hash of the kernel's translation units
+    and every header, comments removed, plus the compiler flags)."""
     from predicted_token_importance_tb_b300 import build
     try:
         with open(os.path.join(ROOT, "profiles", "fused_fast_traffic.json")) as f:
             rec = json.load(f)
-        code = build.code_hash()
-    except (OSError, ValueError):
+        code = build.code_hash(rec["code_units"])
+    except (OSError, ValueError, KeyError, TypeError):
         return None
     if rec.get("workload") != workload or rec.get("code_hash") != code:
         return None
@@ -664,6 +667,71 @@ def run_predict(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, w):
+    """Kp = RNE_bf16(K Wk) for all N rows of every (batch, KV head): one tb_project_append per step (the
+    tcgen05 kernel), M steps captured in one CUDA graph. K (B Hkv N D bf16) is larger than L2 at the
+    prefill workload, so each step streams it from HBM."""
+    import predicted_token_importance_tb_b300 as tb
+
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tb.load_library()
+    n = w.N
+    shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, n)
+    g = torch.Generator(device="cuda").manual_seed(4)
+    K = torch.randn((w.B, w.Hkv, n, w.D), device="cuda", generator=g).to(torch.bfloat16)
+    Wk = (torch.randn((w.Hkv, w.D, w.dp), device="cuda", generator=g) * w.D ** -0.5).to(torch.bfloat16)
+    Kp = torch.empty((w.B, w.Hkv, n, w.dp), dtype=torch.bfloat16, device="cuda")
+    kbytes = K.numel() * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    status = tb.dev_status()
+    tb.tb_project_append(shape, K, n, Wk, Kp, 0, n, dev_status=status)   # once eagerly: attributes, entry points
+    torch.cuda.synchronize()
+    M = 20
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for _ in range(M):
+            tb.tb_project_append(shape, K, n, Wk, Kp, 0, n, dev_status=status)
+    for _ in range(max(3, args.warmup // M)):
+        graph.replay()
+    torch.cuda.synchronize()
+    tb.check_dev_status(status)
+    reps = max(1, min(args.steps, 4000) // M)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    tb.check_dev_status(status)
+    ms = e0.elapsed_time(e1)
+    steps = reps * M
+    per = ms / 1e3 / steps
+    rows = w.B * w.Hkv * n
+    nbytes = rows * (2 * w.D + 2 * w.dp) + w.Hkv * w.D * w.dp * 2
+    hbm_peak, peak_kind = _peaks()
+    line = {
+        "metric": "prefill key projection: cached tokens projected/s (B x N per step, all KV heads)",
+        "value": w.B * n / per, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": max(3, args.warmup // M) * M, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hkv": w.Hkv, "D": w.D, "dp": w.dp, "N": n,
+                   "l2_defeat": f"K is {kbytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB"},
+        "bytes_per_step": nbytes, "flops_per_step": 2 * rows * w.D * w.dp, "kernels_per_step": 1,
+        "gpu_launches": steps,
+        "roofline": {"bound": "hbm", "achieved": nbytes / per / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": nbytes / per / 1e9 / hbm_peak, "kernel": "tb::project_tc_kernel",
+                     "peak_source": peak_kind},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_buffered(args, w):
     """The buffered step (sink S, window W, Kp projected in batches of W) at the bench workload with a
     prediction at every step. R cache sets rotate (L2 defeat); set j advances its own token position, so
@@ -768,6 +836,8 @@ def main():
         run_predict(args, w)
     elif args.ragged:
         run_ragged(args, w)
+    elif args.prefill:
+        run_prefill(args, w if args.workload != synth.WORKLOADS[1].name else _workload("prefill-B2-N65536-sweep"))
     else:
         run_ours(args, w)
 

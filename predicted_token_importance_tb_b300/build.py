@@ -71,12 +71,15 @@ def strip_comments(src: str) -> str:
     return " ".join("".join(out).split())
 
 
-def code_hash() -> str:
-    """Hash of the library's code: every source and header with comments and
-    layout removed, plus the compiler flags. A profile taken on one build
-    stays valid for another with the same code hash."""
+def code_hash(units=None) -> str:
+    """Hash of the library's code: the sources (all, or only the translation
+    units named in `units`, e.g. ("fused_fast.cu", "tb_api.cu")) and every
+    header, with comments and layout removed, plus the compiler flags. A
+    profile of a kernel stays valid across builds whose code hash over that
+    kernel's units is the same."""
+    srcs = _sources() if units is None else [os.path.join(CSRC, u) for u in sorted(units)]
     h = hashlib.sha256()
-    for p in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "tb.h")]:
+    for p in srcs + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "tb.h")]:
         h.update(os.path.basename(p).encode())
         with open(p, encoding="utf-8") as f:
             h.update(strip_comments(f.read()).encode())

@@ -14,9 +14,10 @@
 //           accumulators and commits to mbarriers;
 //   warps 2-5 read the accumulator back with tcgen05.ld (one output row per
 //           thread), round to bf16 and store the row.
-// Wk[h]^T of every KV head sits in shared memory in the same swizzled
-// K-major layout for the whole launch (written once by the CTA). Each CTA
-// takes a contiguous range of tiles.
+// Each CTA takes a contiguous range of tiles. Wk[h]^T of the KV heads that
+// range uses sits in shared memory in the same swizzled K-major layout for
+// the whole launch; warps 1-5 stage it while warp 0's first loads are in
+// flight.
 // Every wait is bounded; on a timeout the CTA records TB_ERR_TIMEOUT, waits
 // (bounded) for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
@@ -178,33 +179,8 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcArgs a) {
     const int tile_lo = (int)((int64_t)blockIdx.x * a.ntiles / gridDim.x);
     const int tile_hi = (int)((int64_t)(blockIdx.x + 1) * a.ntiles / gridDim.x);
 
-    // Wk[h]^T for every KV head, K-major with the 128-byte swizzle: element
-    // (j, d) of head h lives in half kh = d / 64 at row j, byte 2*(d % 64)
-    // of the row, whose 16-byte chunk index is XORed with (j % 8).
-    // (16-byte loads of eight consecutive j, four in flight per thread: the
-    // staging would otherwise wait out one L2 round trip per element)
-    {
-        const int n8 = a.Hkv * a.D * a.dp / 8;   // dp is a multiple of 8
-#pragma unroll 4
-        for (int x8 = threadIdx.x; x8 < n8; x8 += blockDim.x) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a.Wk) + x8);
-            const int x = 8 * x8;
-            const int h = x / (a.D * a.dp);
-            const int rem = x % (a.D * a.dp);
-            const int d = rem / a.dp, j0 = rem % a.dp;
-            const int kh = d / kBoxCols, byte = (d % kBoxCols) * 2;
-            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = j0 + i;
-                const int chunk = (byte >> 4) ^ (j & 7);
-                uint8_t *dst = smB + (size_t)h * b_head_bytes + (size_t)kh * a.dp * 128 + (size_t)j * 128 +
-                               chunk * 16 + (byte & 15);
-                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)(i & 1 ? wv[i >> 1] >> 16 : wv[i >> 1] & 0xFFFFu);
-            }
-        }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    // Barriers and the TMEM accumulators first, so that the producer can
+    // start streaming K before Wk is staged.
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&full[s], 1);
@@ -229,6 +205,41 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const uint32_t idesc = mma_idesc(kTcM, a.dp);
+
+    if (warp != 0) {
+        // Warps 1-5 stage Wk[h]^T of the KV heads this CTA's tiles use (a
+        // contiguous tile range touches one or two heads, all Hkv only when it
+        // spans that many), K-major with the 128-byte swizzle: element (j, d)
+        // of head h lives in half kh = d / 64 at row j, byte 2*(d % 64) of
+        // the row, whose 16-byte chunk index is XORed with (j % 8). 16-byte
+        // loads of eight consecutive j, four in flight per thread.
+        const int hd_lo = tile_lo / a.tiles_per_head;
+        const int hd_hi = (tile_hi - 1) / a.tiles_per_head;
+        const int nh = min(hd_hi - hd_lo + 1, a.Hkv);
+        const int n8h = a.D * a.dp / 8;   // dp is a multiple of 8
+        const int t = threadIdx.x - 32, nt = kTcThreads - 32;
+#pragma unroll 4
+        for (int x8 = t; x8 < nh * n8h; x8 += nt) {
+            const int h = (hd_lo + x8 / n8h) % a.Hkv;
+            const int x = 8 * (x8 % n8h);
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a.Wk + (size_t)h * a.D * a.dp + x));
+            const int d = x / a.dp, j0 = x % a.dp;
+            const int kh = d / kBoxCols, byte = (d % kBoxCols) * 2;
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = j0 + i;
+                const int chunk = (byte >> 4) ^ (j & 7);
+                uint8_t *dst = smB + (size_t)h * b_head_bytes + (size_t)kh * a.dp * 128 + (size_t)j * 128 +
+                               chunk * 16 + (byte & 15);
+                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)(i & 1 ? wv[i >> 1] >> 16 : wv[i >> 1] & 0xFFFFu);
+            }
+        }
+        // the writes become visible to the tensor cores' (async) proxy, then
+        // warps 1-5 meet before the first MMA reads them
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(kTcThreads - 32) : "memory");
+    }
 
     if (warp == 0) {
         // ---------------- producer: TMA loads of the K tiles

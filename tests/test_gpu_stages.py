@@ -28,7 +28,11 @@ def _status():
 # ------------------------------------------------------------------ projection
 
 @pytest.mark.parametrize("B,Hkv,n_new,D,dp,pos0", [(1, 8, 2048, 64, 16, 0), (2, 3, 1000, 128, 32, 17),
-                                                   (1, 2, 77, 32, 8, 5), (1, 4, 300, 128, 64, 0)])
+                                                   (1, 2, 77, 32, 8, 5), (1, 4, 300, 128, 64, 0),
+                                                   # several tiles per CTA, ranges crossing heads and batches
+                                                   (2, 3, 128 * 150 + 37, 128, 32, 0),
+                                                   # a CTA's range spans every KV head
+                                                   (160, 2, 128, 64, 16, 0)])
 def test_project_within_one_ulp(B, Hkv, n_new, D, dp, pos0):
     g = torch.Generator().manual_seed(n_new)
     cap = pos0 + n_new + 3
