@@ -212,8 +212,8 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
 
 /*
  * tb_decode_step for a ragged batch: sequence b holds n[b] tokens before
- * this step's append (the pages batch sequences without saying how they may
- * differ in length). Per sequence the step is exactly tb_decode_step's: the new
+ * this step's append (the method's descriptions batch sequences without
+ * saying how their lengths may differ). Per sequence the step is exactly tb_decode_step's: the new
  * K/V/Kp rows go to position n[b], a prediction scores that sequence's
  * n[b] + 1 tokens and keeps the top k, the widening stays inside them, and
  * between predictions the sequence's new token joins its selection.
@@ -237,7 +237,7 @@ TB_API tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_para
  * low-dimensional importance queries for each KV head), for B tokens:
  *   h     = SiLU(x . W1^T)          x [B, E] bf16, W1 [F, E] bf16, h fp32
  *   q_imp = RNE_bf16(h . W2^T)      W2 [O, F] bf16, q_imp [B, O] = [B, Hq, dp]
- * The pages give no depth, width, activation or bias: two layers, no bias,
+ * The method's descriptions give no depth, width, activation or bias: two layers, no bias,
  * SiLU (the activation of the base models' MLPs), fp32 accumulation and one
  * rounding at the end are this library's reading. Limits: 1 <= B <= 16,
  * E and F multiples of 8, B E 2 and B F 4 bytes <= 200 KB. ws: at least

@@ -88,9 +88,9 @@ void tbo_set_num_threads(int n)
 /* ------------------------------------------------------------------ */
 
 /*
- * [summary] Core Architecture, "Key-Cache Projection": for each consumer
- * layer the real keys are mapped into the low-dimensional importance space by
- * a learned matrix. One matrix per KV head (Wk[h] is D x dp).
+ * [summary] Core Architecture, "Key-Cache Projection": each consumer layer
+ * multiplies its full keys by a trained matrix into the low-dimensional
+ * importance space. One matrix per KV head (Wk[h] is D x dp).
  *
  *   Kp64[b,h,t,j] = sum_d K[b,h,t,d] * Wk[h,d,j]       (fp64)
  *   Kp[b,h,t,j]   = RNE_bf16(Kp64[b,h,t,j])             (the cache stores bf16)
@@ -132,8 +132,8 @@ void tbo_project(int B, int Hkv, int64_t n, int D, int dp,
 
 /*
  * [abstract] the importance queries are combined with the projected keys to
- * score tokens; [summary] Core Architecture, "Scoring": the predicted queries
- * are dotted with the projected keys.
+ * score tokens; [summary] Core Architecture, "Scoring": a token's importance
+ * is the inner product of a predicted query with the token's projected key.
  *
  * The G = Hq/Hkv query heads that share KV head h each carry their own
  * importance query; one budget is spent per KV head, so their G dot products
@@ -202,7 +202,7 @@ static int tbo_int_cmp(const void *pa, const void *pb)
 }
 
 /*
- * [abstract] "dynamic per-token selection under a fixed budget"; [summary]
+ * [abstract] individual tokens are chosen, a fixed number k of them; [summary]
  * Core Architecture, Scoring. Per row (one (batch, KV head) pair) keep the k
  * tokens with the largest scores, ties to the lower index, and report their
  * indices in ascending order.
@@ -236,7 +236,7 @@ int tbo_topk(int64_t rows, int64_t n, int64_t k, const double *s, int32_t *idx)
 /*
  * [summary] Optimizations, "Prediction Interval & Neighbor Fetching": the
  * selection made at a prediction step is reused until the next one, and every
- * selected token brings its spatial neighbours along.
+ * selected token brings the tokens next to it along.
  *
  * Reading used here: the prediction looked at the n_pred tokens present then;
  * each selected index i contributes [i-r, i+r] clipped to [0, n_pred); the

@@ -4,9 +4,9 @@ This module is shared by the tests, the benchmark and the smoke check. It
 draws random tensors and places them; it holds none of the method's
 arithmetic (no projection, scoring, selection or attention).
 
-The pages measure on RULER, LongBench, AIME24 and their own co-reference task
+TokenButler's evaluations use RULER, LongBench, AIME24 and their own co-reference task
 (gist.science summary, "Experimental Results"); none of that data is used.
-These seeded tensors stand in for them at the pages' context-length scale
+These seeded tensors stand in for them at those evaluations' context-length scale
 (16K-128K tokens) and at a Llama-3-8B-shaped attention layer.
 
 Recipe (all draws in fp32 from a CPU ``torch.Generator``, then rounded to bf16
