@@ -33,6 +33,8 @@ Parity status per function:
   silu, predict_queries   pinned against torch's SiLU and matmul in fp64 and
       SiLU's odd-part identity; the MLP's shape is "parity unpinned" by the
       pages.
+tests/test_oracle_mutants.py plants plausible mistakes in private copies of
+this package and checks that a pin fails for each.
 """
 from __future__ import annotations
 

@@ -358,6 +358,33 @@ def test_decode_interval_one_is_per_step_selection():
         assert np.array_equal(sel[:, :, :10], want) and np.all(cnt == 10)
 
 
+def test_prediction_sees_the_token_appended_at_its_own_step():
+    # Reading of the prediction interval: a prediction step scores the cache
+    # after its own append. The appended key is built to out-score every
+    # cached token by far (K_new_d = 8 sign((Wk qbar)_d), qbar the group's mean
+    # importance query), so the new token must be among the k kept.
+    w = synth.small(B=2, Hq=4, Hkv=2, D=16, dp=8, N=100, seed=15)
+    G = w.Hq // w.Hkv
+    L = synth.make_layer(w, cap=w.N + 1, n=w.N)
+    K = oracle.as_u16(L["K"]).copy()
+    V = oracle.as_u16(L["V"]).copy()
+    Kp = np.zeros((w.B, w.Hkv, w.N + 1, w.dp), dtype=np.uint16)
+    Kp[:, :, : w.N], _ = oracle.project(np.ascontiguousarray(K[:, :, : w.N]), L["Wk"])
+    d = synth.make_step(w, 0, 0, L["outlier_ch"])
+    Wk = _f64(oracle.as_u16(L["Wk"]))                                   # [Hkv, D, dp]
+    qbar = _f64(oracle.as_u16(d["q_imp"])).reshape(w.B, w.Hkv, G, w.dp).mean(axis=2)
+    direction = np.einsum("hdj,bhj->bhd", Wk, qbar)
+    K_new = torch.from_numpy(np.where(direction >= 0, 8.0, -8.0)).to(torch.bfloat16)
+    st = oracle.DecodeState()
+    out, sel, cnt = oracle.decode_step(st, 0, w.N, q=d["q"], q_imp=d["q_imp"], K_new=K_new, V_new=d["V_new"],
+                                       Wk=L["Wk"], K=K, V=V, Kp=Kp, k=5, T=4, r=0, agg=oracle.AGG_MEAN,
+                                       scale=w.scale)
+    assert st.n_pred == w.N + 1
+    for b, h in itertools.product(range(w.B), range(w.Hkv)):
+        assert w.N in st.idx[b, h].tolist()
+        assert w.N in sel[b, h, : cnt[b, h]].tolist()
+
+
 def test_decode_interval_reuse_superset_and_tail():
     w = synth.small(B=1, Hq=4, Hkv=2, D=16, dp=8, N=150, seed=12)
     T, r, k = 4, 1, 12
