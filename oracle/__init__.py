@@ -29,7 +29,8 @@ Parity status per function:
       brute-force rank counts and the structure of every selection, the
       rules themselves "parity unpinned" by the pages.
   decode_step_ragged   pinned by its equality with the batched step at equal
-      lengths.
+      lengths and, at unequal lengths, by torch SDPA in fp64 (full budget),
+      a brute-force rank count and independence between sequences.
   silu, predict_queries   pinned against torch's SiLU and matmul in fp64 and
       SiLU's odd-part identity; the MLP's shape is "parity unpinned" by the
       pages.

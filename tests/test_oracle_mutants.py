@@ -67,6 +67,9 @@ MUTANTS = [
      "list(range(pre)) + sorted(body) + list(range(tail0, n_t - 1))"),
     ("buffered_projects_into_window", PY, "while n_t - W - P >= W:", "while n_t - P >= W:"),
     ("buffered_neighbours_cross_sink", PY, "if S <= j < P)", "if 0 <= j < P)"),
+    # ragged batch (Python)
+    ("ragged_uses_first_length", PY, "o, sl, c = decode_step(states[b], t, int(nb),",
+     "o, sl, c = decode_step(states[b], t, int(ns[0]),"),
     # predictor (Python)
     ("silu_wrong_sign", PY, "return v / (1.0 + np.exp(-v))", "return v / (1.0 + np.exp(v))"),
     ("predictor_no_activation", PY, "h = silu(xf @ w1.T)", "h = xf @ w1.T"),

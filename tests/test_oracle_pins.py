@@ -518,3 +518,52 @@ def test_ragged_step_with_equal_lengths_is_the_batched_step():
         for b, h in itertools.product(range(w.B), range(w.Hkv)):
             assert np.array_equal(s1[b, h, : c1[b, h]], s2[b, h, : c2[b, h]])
     assert np.array_equal(arrs[0][2], arrs[1][2])
+
+
+def test_ragged_step_with_unequal_lengths():
+    # Sequences of different lengths in one batch: each sees only its own
+    # n_b + 1 rows. The shortest one keeps all of its tokens (k = n_0 + 1), so
+    # its output is dense attention over exactly those rows (torch SDPA in
+    # fp64); the others keep the brute-force top k of their own scores; and
+    # changing one sequence's data leaves the others' outputs unchanged.
+    w = synth.small(B=3, Hq=4, Hkv=2, D=16, dp=8, N=74, seed=16)
+    G = w.Hq // w.Hkv
+    ns = [40, 73, 55]
+    k = ns[0] + 1
+    L = synth.make_layer(w, cap=w.N + 1, n=w.N)
+    d = synth.make_step(w, 0, 0, L["outlier_ch"])
+
+    def run(K_in, q_in):
+        K = oracle.as_u16(K_in).copy()
+        V = oracle.as_u16(L["V"]).copy()
+        Kp = np.zeros((w.B, w.Hkv, w.N + 1, w.dp), dtype=np.uint16)
+        Kp[:, :, : w.N], _ = oracle.project(np.ascontiguousarray(K[:, :, : w.N]), L["Wk"])
+        sts = [oracle.DecodeState() for _ in range(w.B)]
+        out, sel, cnt = oracle.decode_step_ragged(sts, 0, ns, q=q_in, q_imp=d["q_imp"], K_new=d["K_new"],
+                                                  V_new=d["V_new"], Wk=L["Wk"], K=K, V=V, Kp=Kp, k=k, T=1, r=0,
+                                                  agg=oracle.AGG_MEAN, scale=w.scale)
+        return out, sel, cnt, K, V, Kp
+
+    out, sel, cnt, K, V, Kp = run(L["K"], d["q"])
+    for b, nb in enumerate(ns):
+        assert np.array_equal(K[b, :, nb], oracle.as_u16(d["K_new"])[b])
+        for h in range(w.Hkv):
+            row = sel[b, h, : cnt[b, h]].tolist()
+            assert cnt[b, h] == k and row == sorted(row) and max(row) <= nb
+            s, _ = oracle.score(oracle.as_u16(d["q_imp"])[b:b + 1], np.ascontiguousarray(Kp[b:b + 1, :, : nb + 1]))
+            v = s[0, h]
+            rank = [sum(1 for j in range(nb + 1) if (v[j], -j) > (v[i], -i)) for i in range(nb + 1)]
+            assert row == [i for i in range(nb + 1) if rank[i] < k]
+    n0 = ns[0] + 1
+    qf = torch.from_numpy(_f64(oracle.as_u16(d["q"]))[0]).reshape(1, w.Hq, 1, w.D)
+    Kf = torch.from_numpy(_f64(K[0, :, :n0])).repeat_interleave(G, dim=0)[None]
+    Vf = torch.from_numpy(_f64(V[0, :, :n0])).repeat_interleave(G, dim=0)[None]
+    dense = torch.nn.functional.scaled_dot_product_attention(qf, Kf, Vf, scale=w.scale)[0, :, 0].numpy()
+    assert np.allclose(out[0], dense, rtol=0, atol=1e-12)
+    # sequence 2's keys and queries changed: sequences 0 and 1 are unaffected
+    K2 = L["K"].clone()
+    K2[2] = -K2[2]
+    q2 = d["q"].clone()
+    q2[2] = -q2[2]
+    out_b, _, _, _, _, _ = run(K2, q2)
+    assert np.array_equal(out_b[:2], out[:2]) and not np.array_equal(out_b[2], out[2])
