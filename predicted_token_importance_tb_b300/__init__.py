@@ -178,6 +178,35 @@ def _status_ptr(dev_status):
     return _i32(dev_status, "dev_status") if dev_status is not None else None
 
 
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _need(t, elems: int, name: str):
+    """The library reads or writes `elems` elements of `t`: refuse a smaller tensor before any launch."""
+    if t is not None and t.numel() < elems:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call needs {elems}")
+
+
+def _need_step(shape: "Shape", q, q_imp, K_new, V_new, Wk, K, V, Kp, out):
+    B, Hq, Hkv, D, dp, cap = shape.B, shape.Hq, shape.Hkv, shape.D, shape.dp, shape.cap
+    for t, n, name in ((q, B * Hq * D, "q"), (q_imp, B * Hq * dp, "q_imp"), (K_new, B * Hkv * D, "K_new"),
+                       (V_new, B * Hkv * D, "V_new"), (Wk, Hkv * D * dp, "Wk"), (K, B * Hkv * cap * D, "K"),
+                       (V, B * Hkv * cap * D, "V"), (Kp, B * Hkv * cap * dp, "Kp"), (out, B * Hq * D, "out")):
+        _need(t, n, name)
+
+
+def _need_state(shape: "Shape", kc: int, sel_stride: int, idx_state, sel, counts):
+    rows = shape.B * shape.Hkv
+    _need(idx_state, rows * kc, "idx_state")
+    _need(sel, rows * sel_stride, "sel")
+    _need(counts, rows, "counts")
+
+
+def _centres(k: int, r: int, flags: int) -> int:
+    return max(1, k // (2 * r + 1)) if flags & TB_STEP_BUDGET_NEIGHBOURS else k
+
+
 # ------------------------------------------------------------------ workspace
 
 def tb_workspace_size(shape: Shape, n_max: int, k_max: int, sel_stride_max: int) -> int:
@@ -216,9 +245,14 @@ def tb_project_append(shape: Shape, K_src, src_stride: int, Wk, Kp, pos0: int, n
     lib = load_library()
     if K_src.dtype != torch.bfloat16:
         raise TypeError("K_src must be bfloat16")
+    if n_new > 0:
+        rows = (shape.B * shape.Hkv - 1) * src_stride + n_new
+        _need(K_src, (K_src_offset_rows + rows) * shape.D, "K_src")
+    _need(Wk, shape.Hkv * shape.D * shape.dp, "Wk")
+    _need(Kp, shape.B * shape.Hkv * shape.cap * shape.dp, "Kp")
     base = _ptr(K_src).value + K_src_offset_rows * shape.D * 2
     wsp = _ptr(ws) if ws is not None else None
-    wsb = ws.numel() if ws is not None else 0
+    wsb = _nbytes(ws) if ws is not None else 0
     _check(lib.tb_project_append(ctypes.byref(shape.c()), ctypes.c_void_p(base), src_stride, _bf16(Wk, "Wk"),
                                  _bf16(Kp, "Kp"), pos0, n_new, wsp, wsb, _status_ptr(dev_status),
                                  _stream(stream)), "tb_project_append")
@@ -227,6 +261,11 @@ def tb_project_append(shape: Shape, K_src, src_stride: int, Wk, Kp, pos0: int, n
 def tb_score(shape: Shape, q_imp, Kp, n: int, s, agg: int = TB_AGG_MEAN, dev_status=None, stream=None):
     if s.dtype != torch.float32:
         raise TypeError("s must be float32")
+    rows = shape.B * shape.Hkv
+    _need(q_imp, shape.B * shape.Hq * shape.dp, "q_imp")
+    if n > 0:
+        _need(Kp, ((rows - 1) * shape.cap + n) * shape.dp, "Kp")
+    _need(s, rows * n, "s")
     _check(load_library().tb_score(ctypes.byref(shape.c()), _bf16(q_imp, "q_imp"), _bf16(Kp, "Kp"), n, agg,
                                    _ptr(s), _status_ptr(dev_status), _stream(stream)), "tb_score")
 
@@ -234,7 +273,9 @@ def tb_score(shape: Shape, q_imp, Kp, n: int, s, agg: int = TB_AGG_MEAN, dev_sta
 def tb_topk(shape: Shape, s, n: int, k: int, idx, ws, dev_status=None, stream=None):
     if s.dtype != torch.float32:
         raise TypeError("s must be float32")
-    _check(load_library().tb_topk(ctypes.byref(shape.c()), _ptr(s), n, k, _i32(idx, "idx"), _ptr(ws), ws.numel(),
+    _need(s, shape.B * shape.Hkv * n, "s")
+    _need(idx, shape.B * shape.Hkv * max(k, 0), "idx")
+    _check(load_library().tb_topk(ctypes.byref(shape.c()), _ptr(s), n, k, _i32(idx, "idx"), _ptr(ws), _nbytes(ws),
                                   _status_ptr(dev_status), _stream(stream)), "tb_topk")
 
 
@@ -242,12 +283,18 @@ def tb_topk_noalloc(shape: Shape, s, n: int, k: int, idx, dev_status=None, strea
     """tb_topk for callers that cannot allocate: its scratch is a static array inside libtb."""
     if s.dtype != torch.float32:
         raise TypeError("s must be float32")
+    _need(s, shape.B * shape.Hkv * n, "s")
+    _need(idx, shape.B * shape.Hkv * max(k, 0), "idx")
     _check(load_library().tb_topk_noalloc(ctypes.byref(shape.c()), _ptr(s), n, k, _i32(idx, "idx"),
                                           _status_ptr(dev_status), _stream(stream)), "tb_topk_noalloc")
 
 
 def tb_expand(shape: Shape, idx, k: int, r: int, n_pred: int, n_t: int, sel, sel_stride: int, counts,
               dev_status=None, stream=None):
+    rows = shape.B * shape.Hkv
+    _need(idx, rows * max(k, 0), "idx")
+    _need(sel, rows * max(sel_stride, 0), "sel")
+    _need(counts, rows, "counts")
     _check(load_library().tb_expand(ctypes.byref(shape.c()), _i32(idx, "idx"), k, r, n_pred, n_t,
                                     _i32(sel, "sel"), sel_stride, _i32(counts, "counts"),
                                     _status_ptr(dev_status), _stream(stream)), "tb_expand")
@@ -255,9 +302,16 @@ def tb_expand(shape: Shape, idx, k: int, r: int, n_pred: int, n_t: int, sel, sel
 
 def tb_sparse_decode_attn(shape: Shape, q, K, V, sel, counts, sel_stride: int, scale: float, out, ws,
                           dev_status=None, stream=None):
+    rows = shape.B * shape.Hkv
+    _need(q, shape.B * shape.Hq * shape.D, "q")
+    _need(K, rows * shape.cap * shape.D, "K")
+    _need(V, rows * shape.cap * shape.D, "V")
+    _need(sel, rows * max(sel_stride, 0), "sel")
+    _need(counts, rows, "counts")
+    _need(out, shape.B * shape.Hq * shape.D, "out")
     _check(load_library().tb_sparse_decode_attn(
         ctypes.byref(shape.c()), _bf16(q, "q"), _kv(K, "K"), _kv(V, "V"), _i32(sel, "sel"),
-        _i32(counts, "counts"), sel_stride, scale, _bf16(out, "out"), _ptr(ws), ws.numel(),
+        _i32(counts, "counts"), sel_stride, scale, _bf16(out, "out"), _ptr(ws), _nbytes(ws),
         _status_ptr(dev_status), _stream(stream)), "tb_sparse_decode_attn")
 
 
@@ -266,11 +320,13 @@ def tb_decode_step(shape: Shape, k: int, T: int, r: int, agg: int, scale: float,
                    out, ws, dev_status=None, stream=None, flags: int = 0):
     """One decode step of one layer (see include/tb.h). n_pred is a ctypes.c_int64 carried across steps."""
     params = _StepParams(k, T, r, agg, scale, flags)
+    _need_step(shape, q, q_imp, K_new, V_new, Wk, K, V, Kp, out)
+    _need_state(shape, _centres(k, r, flags), sel_stride, idx_state, sel, counts)
     _check(load_library().tb_decode_step(
         ctypes.byref(shape.c()), ctypes.byref(params), t, n, _bf16(q, "q"), _bf16(q_imp, "q_imp"),
         _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"), _kv(K, "K"), _kv(V, "V"),
         _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.byref(n_pred), _i32(sel, "sel"), sel_stride,
-        _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), ws.numel(), _status_ptr(dev_status),
+        _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), _nbytes(ws), _status_ptr(dev_status),
         _stream(stream)), "tb_decode_step")
 
 
@@ -282,11 +338,13 @@ def tb_decode_step_buffered(shape: Shape, k: int, T: int, r: int, agg: int, scal
     ctypes.c_int64 carried across steps."""
     params = _StepParams(k, T, r, agg, scale, flags)
     bufs = _BufferParams(sink, window)
+    _need_step(shape, q, q_imp, K_new, V_new, Wk, K, V, Kp, out)
+    _need_state(shape, _centres(k, r, flags), sel_stride, idx_state, sel, counts)
     _check(load_library().tb_decode_step_buffered(
         ctypes.byref(shape.c()), ctypes.byref(params), ctypes.byref(bufs), t, n, _bf16(q, "q"), _bf16(q_imp, "q_imp"),
         _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"), _kv(K, "K"), _kv(V, "V"),
         _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.byref(n_pred), ctypes.byref(proj_end),
-        _i32(sel, "sel"), sel_stride, _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), ws.numel(),
+        _i32(sel, "sel"), sel_stride, _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), _nbytes(ws),
         _status_ptr(dev_status), _stream(stream)), "tb_decode_step_buffered")
 
 
@@ -336,7 +394,7 @@ class DecodeLayer:
         self._shape_c = shape.c()
         self._params = _StepParams(k, T, r, agg, self.scale, self.flags)
         self._own = (_i32(self.idx_state, "idx_state"), _i32(self.sel, "sel"), _i32(self.counts, "counts"),
-                     _ptr(self.ws), self.ws.numel(), _status_ptr(self.status))
+                     _ptr(self.ws), _nbytes(self.ws), _status_ptr(self.status))
         self._seen = {}
 
     def _args(self, tensors):
@@ -344,6 +402,7 @@ class DecodeLayer:
         got = self._seen.get(key)
         if got is None:
             q, q_imp, K_new, V_new, Wk, K, V, Kp, out = tensors
+            _need_step(self.shape, q, q_imp, K_new, V_new, Wk, K, V, Kp, out)
             got = (_bf16(q, "q"), _bf16(q_imp, "q_imp"), _bf16(K_new, "K_new"), _bf16(V_new, "V_new"),
                    _bf16(Wk, "Wk"), _kv(K, "K"), _kv(V, "V"), _bf16(Kp, "Kp"), _bf16(out, "out"))
             if len(self._seen) > 256:
@@ -421,6 +480,9 @@ class RaggedDecodeLayer:
     def step(self, t: int, ns, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, out, stream=None):
         """ns: tokens per sequence before this step's append (B ints)."""
         ns = [int(v) for v in ns]
+        if len(ns) != self.shape.B:
+            raise ValueError(f"ns holds {len(ns)} lengths; the batch has {self.shape.B} sequences")
+        _need_step(self.shape, q, q_imp, K_new, V_new, Wk, K, V, Kp, out)
         if ns != list(self.n_host):   # (unchanged lengths need no copy, so repeated steps can be captured)
             for b, v in enumerate(ns):
                 self.n_host[b] = v
@@ -431,6 +493,6 @@ class RaggedDecodeLayer:
             _ptr(self.n_dev), _bf16(q, "q"), _bf16(q_imp, "q_imp"), _bf16(K_new, "K_new"), _bf16(V_new, "V_new"),
             _bf16(Wk, "Wk"), _kv(K, "K"), _kv(V, "V"), _bf16(Kp, "Kp"), _i32(self.idx_state, "idx_state"),
             ctypes.cast(self.n_pred, ctypes.c_void_p), _i32(self.sel, "sel"), self.sel_stride,
-            _i32(self.counts, "counts"), _bf16(out, "out"), _ptr(self.ws), self.ws.numel(), _status_ptr(self.status),
+            _i32(self.counts, "counts"), _bf16(out, "out"), _ptr(self.ws), _nbytes(self.ws), _status_ptr(self.status),
             _stream(stream)), "tb_decode_step_ragged")
         return out

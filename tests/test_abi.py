@@ -97,3 +97,54 @@ def test_host_validation_of_the_newer_calls(lib_path):
         tb.TB_ERR_UNSUPPORTED
     assert lib.tb_predict_queries(fake, fake, fake, 2, 64, 32, 16, fake, fake, 16, None, None) == \
         tb.TB_ERR_WORKSPACE
+
+
+def test_binding_refuses_tensors_shorter_than_the_call_touches(lib_path):
+    # The Python binding compares every tensor's extent with what the call
+    # reads or writes before marshalling any pointer, so a short tensor is a
+    # ValueError on the host (CPU tensors suffice: the check comes first).
+    import torch
+    import predicted_token_importance_tb_b300 as tb
+    B, Hq, Hkv, D, dp, cap = 1, 4, 2, 64, 16, 128
+    shape = tb.Shape(B, Hq, Hkv, D, dp, cap)
+    bf = torch.bfloat16
+
+    def z(n, dtype=bf):
+        return torch.zeros(n, dtype=dtype)
+
+    K, V, Kp, Wk = z(B * Hkv * cap * D), z(B * Hkv * cap * D), z(B * Hkv * cap * dp), z(Hkv * D * dp)
+    with pytest.raises(ValueError, match="K_src"):
+        tb.tb_project_append(shape, z(B * Hkv * cap * D - 1), cap, Wk, Kp, 0, cap)
+    with pytest.raises(ValueError, match="K_src"):   # rows from an offset past the end
+        tb.tb_project_append(shape, K, cap, Wk, Kp, 5, cap, K_src_offset_rows=5)
+    with pytest.raises(ValueError, match="Wk"):
+        tb.tb_project_append(shape, K, cap, z(Hkv * D * dp - 8), Kp, 0, cap)
+    with pytest.raises(ValueError, match="Kp"):
+        tb.tb_project_append(shape, K, cap, Wk, z(B * Hkv * cap * dp - 1), 0, cap)
+    with pytest.raises(ValueError, match="^s "):
+        tb.tb_score(shape, z(B * Hq * dp), Kp, cap, z(B * Hkv * cap - 1, torch.float32))
+    with pytest.raises(ValueError, match="Kp"):
+        tb.tb_score(shape, z(B * Hq * dp), z(B * Hkv * cap * dp - 1), cap, z(B * Hkv * cap, torch.float32))
+    with pytest.raises(ValueError, match="idx"):
+        tb.tb_topk(shape, z(B * Hkv * cap, torch.float32), cap, 10, z(B * Hkv * 10 - 1, torch.int32), z(1, torch.uint8))
+    with pytest.raises(ValueError, match="sel"):
+        tb.tb_expand(shape, z(B * Hkv * 4, torch.int32), 4, 1, cap, cap, z(B * Hkv * 12 - 1, torch.int32), 12,
+                     z(B * Hkv, torch.int32))
+    with pytest.raises(ValueError, match="^V "):
+        tb.tb_sparse_decode_attn(shape, z(B * Hq * D), K, z(B * Hkv * cap * D - 1), z(B * Hkv * 8, torch.int32),
+                                 None, 8, 0.125, z(B * Hq * D), z(1, torch.uint8))
+    with pytest.raises(ValueError, match="out"):
+        tb.tb_decode_step(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, cap - 1, q=z(B * Hq * D), q_imp=z(B * Hq * dp),
+                          K_new=z(B * Hkv * D), V_new=z(B * Hkv * D), Wk=Wk, K=K, V=V, Kp=Kp,
+                          idx_state=z(B * Hkv * 8, torch.int32), n_pred=ctypes.c_int64(0),
+                          sel=z(B * Hkv * 8, torch.int32), sel_stride=8, counts=z(B * Hkv, torch.int32),
+                          out=z(B * Hq * D - 1), ws=z(1, torch.uint8))
+    with pytest.raises(ValueError, match="idx_state"):
+        tb.tb_decode_step(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, cap - 1, q=z(B * Hq * D), q_imp=z(B * Hq * dp),
+                          K_new=z(B * Hkv * D), V_new=z(B * Hkv * D), Wk=Wk, K=K, V=V, Kp=Kp,
+                          idx_state=z(B * Hkv * 8 - 1, torch.int32), n_pred=ctypes.c_int64(0),
+                          sel=z(B * Hkv * 8, torch.int32), sel_stride=8, counts=z(B * Hkv, torch.int32),
+                          out=z(B * Hq * D), ws=z(1, torch.uint8))
+    # the full-size tensors pass the extent checks and fail only at pointer marshalling (CPU tensors)
+    with pytest.raises(ValueError, match="CUDA device"):
+        tb.tb_project_append(shape, K, cap, Wk, Kp, 0, cap)
