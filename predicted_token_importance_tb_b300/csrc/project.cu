@@ -48,10 +48,10 @@ cudaError_t launch_project_simple(const tb_shape &sh, const uint16_t *K_src, int
     const int rows = sh.B * sh.Hkv;
     if (rows <= 0 || n_new <= 0) return cudaSuccess;
     const size_t smem = ((size_t)sh.D * sh.dp + (size_t)kProjRows * (sh.D + 1)) * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
+    static thread_local int attr_dev = -1;   // the attribute belongs to each device's context
+    if (attr_dev != dev_info().device) {
         cudaFuncSetAttribute(project_simple_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attr_set = true;
+        attr_dev = dev_info().device;
     }
     dim3 grid((unsigned)((n_new + kProjRows - 1) / kProjRows), (unsigned)rows);
     project_simple_kernel<<<grid, kProjThreads, smem, st>>>(K_src, src_stride, Wk, Kp, sh.cap, sh.Hkv, sh.D, sh.dp,

@@ -342,17 +342,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once per process; the initialisation of a function-local
+    // static is thread-safe
+    static const EncodeTiledFn fn = [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -395,10 +395,12 @@ cudaError_t launch_project_tc(const tb_shape &sh, const uint16_t *K_src, int64_t
     while (cols < 2 * sh.dp) cols <<= 1;
     a.tmem_cols = cols;
     const size_t smem = tc_smem_bytes(sh.Hkv, sh.D, sh.dp);
-    static size_t attr = 0;
-    if (attr < smem) {
+    static thread_local int attr_dev = -1;   // per thread and device: the attribute lives in each context
+    static thread_local size_t attr = 0;
+    if (attr_dev != dev_info().device || attr < smem) {
         cudaError_t e = cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        attr_dev = dev_info().device;
         attr = smem;
     }
     int grid = dev_info().sms > 0 ? dev_info().sms : 148;

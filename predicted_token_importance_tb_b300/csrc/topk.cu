@@ -64,9 +64,9 @@ struct TopkPlan {
 };
 
 static int topk_capacity(size_t smem) {
-    static int cached_dev = -1;
-    static size_t cached_smem = 0;
-    static int cached_cap = 0;
+    static thread_local int cached_dev = -1;   // per thread: no shared mutable state between callers
+    static thread_local size_t cached_smem = 0;
+    static thread_local int cached_cap = 0;
     const DevInfo &di = dev_info();
     if (cached_dev == di.device && cached_smem == smem) return cached_cap;
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
