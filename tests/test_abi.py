@@ -148,3 +148,37 @@ def test_binding_refuses_tensors_shorter_than_the_call_touches(lib_path):
     # the full-size tensors pass the extent checks and fail only at pointer marshalling (CPU tensors)
     with pytest.raises(ValueError, match="CUDA device"):
         tb.tb_project_append(shape, K, cap, Wk, Kp, 0, cap)
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "tb.h"
+
+int main(void) {
+    /* a plain C caller: the header compiles as C and the calls below need no GPU */
+    if (tb_version() != 1) return 1;
+    tb_shape ok = {1, 32, 8, 128, 32, 32768};
+    size_t bytes = 0;
+    if (tb_workspace_size(&ok, 32767, 3277, 3277, &bytes) != TB_OK || bytes == 0) return 2;
+    tb_shape bad = {1, 6, 4, 128, 32, 100};            /* Hq not a multiple of Hkv */
+    if (tb_workspace_size(&bad, 10, 4, 4, &bytes) != TB_ERR_INVALID_ARG) return 3;
+    if (tb_topk(&ok, (const float *)16, 10, 11, (int32_t *)16, NULL, 0, NULL, 0) != TB_ERR_INVALID_ARG) return 4;
+    printf("%s|%zu\n", tb_status_string(TB_ERR_WORKSPACE), bytes);
+    return 0;
+}
+"""
+
+
+def test_plain_c_client_compiles_links_and_runs(lib_path, tmp_path):
+    # include/tb.h is a C header and libtb.so a C library: a C program uses both without torch
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(lib_path)
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                    str(src), "-o", str(exe), f"-L{libdir}", "-l:libtb.so", f"-Wl,-rpath,{libdir}"], check=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert res.returncode == 0, (res.returncode, res.stderr)
+    text, nbytes = res.stdout.strip().split("|")
+    assert text == "workspace missing or too small" and int(nbytes) > 0
