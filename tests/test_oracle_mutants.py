@@ -21,6 +21,11 @@ C, PY = "tb_oracle.c", "__init__.py"
 
 # (name, file, text in the oracle, planted replacement)
 MUTANTS = [
+    # bf16 rounding
+    ("bf16_ties_away_from_zero", C, "double m = nearbyint(ldexp(a, -q));", "double m = round(ldexp(a, -q));"),
+    ("bf16_truncates", C, "double m = nearbyint(ldexp(a, -q));", "double m = floor(ldexp(a, -q));"),
+    ("bf16_nine_significant_bits", C, "int q = e - 8; ", "int q = e - 9; "),
+    ("bf16_subnormal_spacing", C, "if (q < -133) q = -133;", "if (q < -134) q = -134;"),
     # projection
     ("project_drops_last_term", C,
      "for (int d = 0; d < D; ++d)\n                        acc += tbo_bf16_to_double(Kh[t * D + d])",
