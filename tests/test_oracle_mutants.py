@@ -65,6 +65,11 @@ MUTANTS = [
      "s, _ = score(q_imp, np.ascontiguousarray(Kp[:, :, :n, :]), agg)"),
     ("interval_reuse_forgets_tail", PY, "    sel, counts = expand(state.idx, r, state.n_pred, n_t)\n",
      "    sel, counts = expand(state.idx, r, state.n_pred, state.n_pred)\n"),
+    ("decode_ignores_budget_rule", PY, "state.idx = topk(s, centres(k, r, budget_neighbours))",
+     "state.idx = topk(s, k)"),
+    ("decode_predicts_every_step", PY,
+     "if t % T == 0:\n        s, _ = score(q_imp, np.ascontiguousarray(Kp[:, :, :n_t, :]), agg)",
+     "if True:\n        s, _ = score(q_imp, np.ascontiguousarray(Kp[:, :, :n_t, :]), agg)"),
     ("centres_ignore_width", PY, "return max(1, k // (2 * r + 1)) if budget_neighbours else k",
      "return max(1, k // (r + 1)) if budget_neighbours else k"),
     # buffered step (Python)
@@ -72,6 +77,11 @@ MUTANTS = [
      "list(range(pre)) + sorted(body) + list(range(tail0, n_t - 1))"),
     ("buffered_projects_into_window", PY, "while n_t - W - P >= W:", "while n_t - P >= W:"),
     ("buffered_neighbours_cross_sink", PY, "if S <= j < P)", "if 0 <= j < P)"),
+    ("buffered_sink_one_short", PY, "pre = min(S, n_t)", "pre = min(S - 1, n_t)"),
+    ("buffered_centres_not_offset_by_sink", PY, "range(S + i - r, S + i + r + 1)", "range(i - r, i + r + 1)"),
+    ("buffered_scores_include_sink", PY, "Kp[:, :, S:P, :]", "Kp[:, :, 0:P, :]"),
+    ("buffered_reuse_drops_new_token", PY, "state.sel_rows = [row + [n] for row in state.sel_rows]",
+     "state.sel_rows = [list(row) for row in state.sel_rows]"),
     # ragged batch (Python)
     ("ragged_uses_first_length", PY, "o, sl, c = decode_step(states[b], t, int(nb),",
      "o, sl, c = decode_step(states[b], t, int(ns[0]),"),
