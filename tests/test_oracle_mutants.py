@@ -43,6 +43,9 @@ MUTANTS = [
      "return (a->i > b->i) ? -1 : (a->i < b->i);"),
     ("topk_keeps_smallest", C, "if (a->s > b->s) return -1;\n    if (a->s < b->s) return 1;",
      "if (a->s < b->s) return -1;\n    if (a->s > b->s) return 1;"),
+    ("topk_positive_zero_above_negative", C, "if (a->s > b->s) return -1;\n    if (a->s < b->s) return 1;",
+     "if (a->s > b->s || (a->s == b->s && signbit(b->s) && !signbit(a->s))) return -1;\n"
+     "    if (a->s < b->s || (a->s == b->s && signbit(a->s) && !signbit(b->s))) return 1;"),
     ("topk_output_in_rank_order", C, "qsort(out, (size_t)k, sizeof *out, tbo_int_cmp);", ""),
     ("topk_one_short", C, "for (int64_t j = 0; j < k; ++j) out[j] = p[j].i;",
      "for (int64_t j = 0; j < k; ++j) out[j] = p[j + (j == k - 1 && k < n)].i;"),
