@@ -28,8 +28,9 @@
  *      idx   : [B, Hkv, k] (int32)     sel: [B, Hkv, sel_stride] (int32)
  *      out   : [B, Hq, D]
  *  - Limits: D in {8, 16, 32, 64, 128, 256} (D/8 lanes tile a warp), dp a
- *    multiple of 8 and <= 256, Hq % Hkv == 0, G <= 16, cap < 2^31. Violations return TB_ERR_UNSUPPORTED or
- *    TB_ERR_INVALID_ARG before anything is enqueued.
+ *    multiple of 8 and <= 256, Hq % Hkv == 0, G <= 16, cap < 2^31.
+ *    Violations return TB_ERR_UNSUPPORTED or TB_ERR_INVALID_ARG before
+ *    anything is enqueued.
  *  - The caller owns all memory; the library allocates none. Scratch comes
  *    from a caller-provided workspace of tb_workspace_size() bytes that must
  *    be zero-filled before its first use (tb_workspace_init); every call that
@@ -213,10 +214,11 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
 /*
  * tb_decode_step for a ragged batch: sequence b holds n[b] tokens before
  * this step's append (the method's descriptions batch sequences without
- * saying how their lengths may differ). Per sequence the step is exactly tb_decode_step's: the new
- * K/V/Kp rows go to position n[b], a prediction scores that sequence's
- * n[b] + 1 tokens and keeps the top k, the widening stays inside them, and
- * between predictions the sequence's new token joins its selection.
+ * saying how their lengths may differ). Per sequence the step is exactly
+ * tb_decode_step's: the new K/V/Kp rows go to position n[b], a prediction
+ * scores that sequence's n[b] + 1 tokens and keeps the top k, the widening
+ * stays inside them, and between predictions the sequence's new token joins
+ * its selection.
  * n_host [B] (host) and n_dev [B] (device) hold the same values;
  * n_pred [B] is the host state of the interval, one entry per sequence.
  * Needs k <= n[b] + 1 for every b at a prediction and sel_stride >=
