@@ -38,6 +38,7 @@ MUTANTS = [
     ("score_heads_interleaved", C, "(int64_t)h * G + g) * dp", "(int64_t)g * Hkv + h) * dp"),
     ("score_max_is_min", C, "if (dot > best) best = dot;", "if (dot < best || best == -INFINITY) best = dot;"),
     ("score_wrong_sign", C, "dot += p;", "dot -= p;"),
+    ("score_drops_last_term", C, "for (int i = 0; i < dp; ++i) {", "for (int i = 0; i < dp - 1; ++i) {"),
     # top-k
     ("topk_ties_to_higher_index", C, "return (a->i < b->i) ? -1 : (a->i > b->i);",
      "return (a->i > b->i) ? -1 : (a->i < b->i);"),
@@ -58,6 +59,8 @@ MUTANTS = [
      "if (t >= 0 && t < n_pred - 1) mask[t] = 1;"),
     # attention
     ("attn_no_scale", C, "z[j] = scale * dot;", "z[j] = dot;"),
+    ("attn_denominator_skips_first_row", C, "for (int64_t j = 0; j < c; ++j) denom += exp(z[j] - zmax);",
+     "for (int64_t j = 1; j < c; ++j) denom += exp(z[j] - zmax);"),
     ("attn_gqa_mapping", C, "int h = hq / G;", "int h = hq % Hkv;"),
     ("attn_unnormalised", C, "double w = exp(z[j] - zmax) / denom;", "double w = exp(z[j] - zmax);"),
     ("attn_numerator_without_max", C, "double w = exp(z[j] - zmax) / denom;", "double w = exp(z[j]) / denom;"),
