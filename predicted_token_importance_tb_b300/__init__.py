@@ -127,6 +127,16 @@ def status_string(st: int) -> str:
         return f"status {st}"
 
 
+def tb_status_string(st: int) -> str:
+    """The library's text for a status code."""
+    return load_library().tb_status_string(int(st)).decode()
+
+
+def tb_version() -> int:
+    """The C ABI's version."""
+    return int(load_library().tb_version())
+
+
 def _check(st: int, what: str):
     if st != TB_OK:
         raise TBError(st, what)
@@ -346,6 +356,28 @@ def tb_decode_step_buffered(shape: Shape, k: int, T: int, r: int, agg: int, scal
         _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.byref(n_pred), ctypes.byref(proj_end),
         _i32(sel, "sel"), sel_stride, _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), _nbytes(ws),
         _status_ptr(dev_status), _stream(stream)), "tb_decode_step_buffered")
+
+
+def tb_decode_step_ragged(shape: Shape, k: int, T: int, r: int, agg: int, scale: float, t: int, n_host, n_dev, *,
+                          q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, n_pred, sel, sel_stride: int, counts,
+                          out, ws, dev_status=None, stream=None, flags: int = 0):
+    """One decode step for a batch of sequences of different lengths (see include/tb.h). n_host and n_pred
+    are ctypes int64 arrays of B entries on the host (n_pred carried across steps); n_dev is an int64
+    device tensor [B] holding the values of n_host."""
+    if len(n_host) != shape.B or len(n_pred) != shape.B:
+        raise ValueError(f"n_host and n_pred need {shape.B} entries")
+    if n_dev.dtype != torch.int64:
+        raise TypeError(f"n_dev must be int64, got {n_dev.dtype}")
+    _need(n_dev, shape.B, "n_dev")
+    _need_step(shape, q, q_imp, K_new, V_new, Wk, K, V, Kp, out)
+    _need_state(shape, _centres(k, r, flags), sel_stride, idx_state, sel, counts)
+    params = _StepParams(k, T, r, agg, scale, flags)
+    _check(load_library().tb_decode_step_ragged(
+        ctypes.byref(shape.c()), ctypes.byref(params), t, ctypes.cast(n_host, ctypes.c_void_p), _ptr(n_dev),
+        _bf16(q, "q"), _bf16(q_imp, "q_imp"), _bf16(K_new, "K_new"), _bf16(V_new, "V_new"), _bf16(Wk, "Wk"),
+        _kv(K, "K"), _kv(V, "V"), _bf16(Kp, "Kp"), _i32(idx_state, "idx_state"), ctypes.cast(n_pred, ctypes.c_void_p),
+        _i32(sel, "sel"), sel_stride, _i32(counts, "counts"), _bf16(out, "out"), _ptr(ws), _nbytes(ws),
+        _status_ptr(dev_status), _stream(stream)), "tb_decode_step_ragged")
 
 
 def tb_predict_queries(x, W1, W2, q_imp, ws=None, dev_status=None, stream=None):

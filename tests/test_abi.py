@@ -182,3 +182,37 @@ def test_plain_c_client_compiles_links_and_runs(lib_path, tmp_path):
     assert res.returncode == 0, (res.returncode, res.stderr)
     text, nbytes = res.stdout.strip().split("|")
     assert text == "workspace missing or too small" and int(nbytes) > 0
+
+
+def test_binding_has_a_function_of_the_same_name_for_every_entry_point(lib_path):
+    import predicted_token_importance_tb_b300 as tb
+    missing = [n for n in _declared() if not callable(getattr(tb, n, None))]
+    assert not missing, missing
+    assert tb.tb_version() == 1 and tb.tb_status_string(tb.TB_OK) == "ok"
+
+
+def test_ragged_binding_checks_its_arguments(lib_path):
+    import torch
+    import predicted_token_importance_tb_b300 as tb
+    B, Hq, Hkv, D, dp, cap = 2, 4, 2, 64, 16, 128
+    shape = tb.Shape(B, Hq, Hkv, D, dp, cap)
+    bf = torch.bfloat16
+
+    def z(n, dtype=bf):
+        return torch.zeros(n, dtype=dtype)
+
+    kw = dict(q=z(B * Hq * D), q_imp=z(B * Hq * dp), K_new=z(B * Hkv * D), V_new=z(B * Hkv * D),
+              Wk=z(Hkv * D * dp), K=z(B * Hkv * cap * D), V=z(B * Hkv * cap * D), Kp=z(B * Hkv * cap * dp),
+              idx_state=z(B * Hkv * 8, torch.int32), n_pred=(ctypes.c_int64 * B)(), sel=z(B * Hkv * 8, torch.int32),
+              sel_stride=8, counts=z(B * Hkv, torch.int32), out=z(B * Hq * D), ws=z(1, torch.uint8))
+    n_host = (ctypes.c_int64 * B)(40, 90)
+    with pytest.raises(ValueError, match="entries"):
+        tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, (ctypes.c_int64 * 1)(40),
+                                 z(B, torch.int64), **kw)
+    with pytest.raises(TypeError, match="int64"):
+        tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, n_host, z(B, torch.int32), **kw)
+    with pytest.raises(ValueError, match="^K "):
+        tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, n_host, z(B, torch.int64),
+                                 **{**kw, "K": z(B * Hkv * cap * D - 1)})
+    with pytest.raises(ValueError, match="CUDA device"):   # full extents pass; CPU tensors stop at marshalling
+        tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, n_host, z(B, torch.int64), **kw)
