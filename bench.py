@@ -49,6 +49,7 @@ def _args():
     ap.add_argument("--workload", default=synth.WORKLOADS[1].name)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-warm-l2", action="store_true", help="skip the labelled warm-L2 leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--rotate", type=int, default=0, help="cache copies to rotate over (0: enough to defeat L2)")
     ap.add_argument("--agg", default="mean", choices=["mean", "max"],
@@ -212,20 +213,30 @@ def _oracle_cores(w) -> int:
     return min(oracle.num_threads(), w.B * w.Hq)
 
 
-def cpu_baseline(w, seconds: float):
-    """The oracle as it stands, timed on this host's cores on a bounded sample of whole decode steps."""
+def cpu_baseline(w, seconds: float, threads: int = 0):
+    """The oracle as it stands, timed on this host's cores (or on `threads` of them) on a bounded sample of
+    whole decode steps."""
+    import oracle
     L, oK, oV, oKp, n0, d = _oracle_setup(w)
-    done = 0
-    t0 = time.perf_counter()
-    while True:
-        _oracle_step(w, L, d, oK, oV, oKp, n0)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": done / el, "unit": UNIT, "cores": _oracle_cores(w), "kind": "oracle",
+    before = oracle.num_threads()
+    if threads:
+        oracle.set_num_threads(threads)
+    try:
+        cores = _oracle_cores(w)
+        done = 0
+        t0 = time.perf_counter()
+        while True:
+            _oracle_step(w, L, d, oK, oV, oKp, n0)
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+    finally:
+        if threads:
+            oracle.set_num_threads(before)
+    return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{done} whole decode steps at N={w.N}, k={w.k} in {el:.1f} s (fp64 C, OpenMP over "
-                      f"(batch, head) rows)"}
+                      f"(batch, head) rows, {cores} thread(s))"}
 
 
 def run_reference(args, w):
@@ -329,30 +340,45 @@ def run_ours(args, w):
     rem = args.steps % M
     g_rem = graph_of(rem) if rem else None
     torch.cuda.synchronize()
-    # warm-up W steps
-    for _ in range(args.warmup // M):
+    # warm-up: at least W steps, and every graph the timed region replays is replayed (uploaded, its
+    # first launch paid) here first, so no freshly instantiated graph runs inside the timed region
+    warm_steps = 0
+    for _ in range(max(2, -(-args.warmup // M))):
         gM.replay()
-    if args.warmup % M:
-        graph_of(args.warmup % M).replay()
+        warm_steps += M
+    if g_rem is not None:
+        g_rem.replay()
+        warm_steps += rem
     torch.cuda.synchronize()
+
+    def timed_region():
+        """Barrier + synchronize, one untimed replay that keeps the GPU busy while the timed replays are
+        submitted (so host submission never shows as idle GPU time), then exactly args.steps steps
+        between two events on the launching stream, barrier + synchronize."""
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        _barrier(dist)
+        with torch.cuda.stream(s):
+            gM.replay()
+            e0.record(s)
+            for _ in range(args.steps // M):
+                gM.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            e1.record(s)
+        _barrier(dist)
+        return e0.elapsed_time(e1)
 
     clocks = ClockSampler(dev) if rank == 0 else None
     if clocks:
         clocks.start()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    _barrier(dist)
-    e0.record()
-    for _ in range(args.steps // M):
-        gM.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    e1.record()
-    _barrier(dist)
-    ms = e0.elapsed_time(e1)
+    ms = timed_region()
     clk = clocks.stop() if clocks else None
+    # four more identical regions, for the median the line also reports
+    repeats = [ms] + [timed_region() for _ in range(4)]
     tb.check_dev_status(dec.status, "bench timed region")
     ms = _max_over_ranks(dist, ms)
+    ms_median = _max_over_ranks(dist, statistics.median(repeats))
     sec = ms / 1e3
     steps_per_s_rank = args.steps / sec
     total_steps_per_s = steps_per_s_rank * world
@@ -364,19 +390,46 @@ def run_ours(args, w):
     per_step_s = sec / args.steps
     achieved = step_bytes_real / per_step_s / 1e9
 
+    # a labelled warm-L2 figure: the same step on one cache set, so its bytes stay in L2
+    warm = None
+    if not args.no_warm_l2:
+        mw = 200
+        gw = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw, stream=s):
+            for _ in range(mw):
+                step(0)
+        for _ in range(2):
+            gw.replay()
+        torch.cuda.synchronize()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            gw.replay()
+            w0.record(s)
+            for _ in range(5):
+                gw.replay()
+            w1.record(s)
+        torch.cuda.synchronize()
+        tb.check_dev_status(dec.status, "bench warm-L2 leg")
+        wus = w0.elapsed_time(w1) * 1e3 / (5 * mw)
+        warm = {"us_per_step": wus, "steps_per_s": 1e6 / wus, "steps": 5 * mw,
+                "note": "rotation off: one cache set, L2-resident after the first step (not the headline)"}
+        del gw
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
         e2e = _e2e(tb, w, shape, dec, Wk, Ks[0], Vs[0], Kps[0], n0, steps_in, dist, world)
 
     cpu = None
+    cpu1 = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
+        cpu1 = cpu_baseline(w, args.cpu_seconds / 3, threads=1)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": total_steps_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "warmup": warm_steps, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "dp": w.dp, "N": w.N,
                        "k": w.k, "T": 1, "r": 0, "agg": args.agg, "rotation_sets": R,
@@ -391,9 +444,14 @@ def run_ours(args, w):
                          "kernel": "tb decode step, %s kernel(s) per step" % kernels_per_step,
                          "peak_source": peak_kind},
             "cpu_baseline": cpu,
+            "cpu_baseline_1thread": cpu1,
             "e2e": e2e,
             "gpu_launches": int(round(args.steps * kernels_per_step)) if kernels_per_step else None,
             "kernels_per_step": kernels_per_step,
+            "kernel_us": ms * 1e3 / args.steps,
+            "median_of_5": {"us_per_step": ms_median * 1e3 / args.steps,
+                            "note": "median over five identical timed regions of the same length"},
+            "warm_l2": warm,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

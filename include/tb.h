@@ -311,8 +311,10 @@ TB_API tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_pa
  * Errors: B*Hkv > TB_TOPK_NOALLOC_MAX_ROWS returns TB_ERR_UNSUPPORTED; the
  * other checks and device-side errors are those of tb_topk.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture. All calls on a device share the one array, so
+ * (cudaGetSymbolAddress, with that device current) and keeps it for the life
+ * of the process; make that first call before any stream capture, and do not
+ * use the library across a cudaDeviceReset (the kept address would then
+ * point into the torn-down context). All calls on a device share the one array, so
  * calls that overlap on the GPU (concurrent streams, or several host threads)
  * race and give wrong results: serialise them.
  */

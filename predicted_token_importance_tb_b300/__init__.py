@@ -149,6 +149,10 @@ def _ptr(t):
         raise TypeError("expected a torch tensor")
     if not t.is_cuda:
         raise ValueError("tensor must be on a CUDA device")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device (and picks its static arrays there)
+        raise ValueError(f"tensor is on cuda:{t.device.index} but the current device is "
+                         f"cuda:{torch.cuda.current_device()}: make its device current first")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
@@ -364,8 +368,12 @@ def tb_decode_step_ragged(shape: Shape, k: int, T: int, r: int, agg: int, scale:
     """One decode step for a batch of sequences of different lengths (see include/tb.h). n_host and n_pred
     are ctypes int64 arrays of B entries on the host (n_pred carried across steps); n_dev is an int64
     device tensor [B] holding the values of n_host."""
-    if len(n_host) != shape.B or len(n_pred) != shape.B:
-        raise ValueError(f"n_host and n_pred need {shape.B} entries")
+    for arr, name in ((n_host, "n_host"), (n_pred, "n_pred")):
+        # the C side reads B int64 values from each: anything else would be read past its end or misread
+        if not isinstance(arr, ctypes.Array) or arr._type_ is not ctypes.c_int64:
+            raise TypeError(f"{name} must be a ctypes array (ctypes.c_int64 * {shape.B}), got {type(arr).__name__}")
+        if len(arr) != shape.B:
+            raise ValueError(f"n_host and n_pred need {shape.B} entries")
     if n_dev.dtype != torch.int64:
         raise TypeError(f"n_dev must be int64, got {n_dev.dtype}")
     _need(n_dev, shape.B, "n_dev")

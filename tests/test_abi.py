@@ -211,8 +211,24 @@ def test_ragged_binding_checks_its_arguments(lib_path):
                                  z(B, torch.int64), **kw)
     with pytest.raises(TypeError, match="int64"):
         tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, n_host, z(B, torch.int32), **kw)
+    # host arrays of another element type or a plain list: refused before the C side reads 8 B per entry
+    with pytest.raises(TypeError, match="n_host"):
+        tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, (ctypes.c_int32 * B)(40, 90),
+                                 z(B, torch.int64), **kw)
+    with pytest.raises(TypeError, match="n_pred"):
+        tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, n_host, z(B, torch.int64),
+                                 **{**kw, "n_pred": [0, 0]})
     with pytest.raises(ValueError, match="^K "):
         tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, n_host, z(B, torch.int64),
                                  **{**kw, "K": z(B * Hkv * cap * D - 1)})
     with pytest.raises(ValueError, match="CUDA device"):   # full extents pass; CPU tensors stop at marshalling
         tb.tb_decode_step_ragged(shape, 8, 1, 0, tb.TB_AGG_MEAN, 0.125, 0, n_host, z(B, torch.int64), **kw)
+
+
+def test_noalloc_row_limit_matches_the_header():
+    """The binding's copy of TB_TOPK_NOALLOC_MAX_ROWS is the header's value."""
+    import re
+    import predicted_token_importance_tb_b300 as tb
+    with open(os.path.join(ROOT, "include", "tb.h")) as f:
+        m = re.search(r"#define\s+TB_TOPK_NOALLOC_MAX_ROWS\s+(\d+)", f.read())
+    assert m and int(m.group(1)) == tb.TB_TOPK_NOALLOC_MAX_ROWS
