@@ -62,6 +62,13 @@ def _args():
                     help="S,W: sink and local-window buffers with batched key projection; prints its own line")
     ap.add_argument("--offload", action="store_true",
                     help="K/V in pinned host memory (the offloaded cache); prints its own line")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="L: one decode step of L consumer layers of the workload's shape (the selection of later "
+                         "layers overlapping the attention of earlier ones); prints its own line, per-layer figures")
+    ap.add_argument("--budget", type=float, default=0.0,
+                    help="budget as a fraction of N (k = ceil(frac N)) instead of the workload's k")
+    ap.add_argument("--pipeline", action="store_true",
+                    help="run the single-layer step as the three-kernel form instead of the cooperative kernel")
     ap.add_argument("--prefill", action="store_true",
                     help="the key projection of a whole prefill (tcgen05), on the B=2, N=65536 prefill "
                          "workload unless --workload names another; prints its own line")
@@ -305,7 +312,7 @@ def run_ours(args, w):
     steps_in = [synth.make_step(w, 0, i, L["outlier_ch"]) for i in range(R)]
     dins = [{k: v.cuda() for k, v in d.items()} for d in steps_in]
     agg = tb.TB_AGG_MAX if args.agg == "max" else tb.TB_AGG_MEAN
-    dec = tb.DecodeLayer(shape, w.k, T=1, r=0, agg=agg, scale=w.scale, n_max=n0)
+    dec = tb.DecodeLayer(shape, w.k, T=1, r=0, agg=agg, scale=w.scale, n_max=n0, pipeline=args.pipeline)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
 
     def step(i):
@@ -881,11 +888,119 @@ def run_buffered(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_layers(args, w):
+    """One decode step of L consumer layers of the workload's shape through tb_decode_layers: every layer's
+    selection (its n cached tokens scored against the producer's importance query, the top k kept) runs on a
+    second stream while earlier layers attend; each layer's attention waits for the previous layer's. R sets
+    of L layers rotate (L2 defeat); M steps are captured in one CUDA graph."""
+    import predicted_token_importance_tb_b300 as tb
+
+    Lc = args.layers
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tb.load_library()
+    n0 = w.N - 1
+    cap = w.N
+    shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, cap)
+    rows = w.B * w.Hkv
+    kp_bytes = rows * n0 * w.dp * 2                      # the selection streams the n cached tokens' Kp
+    qio_bytes = (w.B * w.Hq * w.D * 2) * 2 + w.B * w.Hq * w.dp * 2
+    append_bytes = rows * w.D * 2 * 2 * 2 + w.Hkv * w.D * w.dp * 2 + rows * w.dp * 2
+    layer_bytes_est = kp_bytes + rows * w.k * 2 * w.D * 2 + qio_bytes + append_bytes
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(4 * l2 / (Lc * layer_bytes_est)))
+    base = synth.make_layer(w, cap=cap, n=n0)
+    Wk = base["Wk"].cuda()
+    K0, V0 = base["K"].cuda(), base["V"].cuda()
+    Kp0 = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
+    tb.tb_project_append(shape, K0, cap, Wk, Kp0, 0, n0)
+    sets = []
+    for j in range(R):
+        lay = []
+        for l in range(Lc):
+            first = j == 0 and l == 0
+            lay.append((K0 if first else K0.clone(), V0 if first else V0.clone(), Kp0 if first else Kp0.clone()))
+        sets.append(lay)
+    dins = [[{k: v.cuda() for k, v in synth.make_step(w, l, j, base["outlier_ch"]).items()} for l in range(Lc)]
+            for j in range(R)]
+    outs = [torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda") for _ in range(Lc)]
+    stack = tb.DecodeStack(shape, Lc, w.k, scale=w.scale, n_max=n0)
+
+    def step(i):
+        j = i % R
+        lay, d = sets[j], dins[j]
+        stack.step(n0, q=[x["q"] for x in d], q_imp=[x["q_imp"] for x in d], K_new=[x["K_new"] for x in d],
+                   V_new=[x["V_new"] for x in d], Wk=[Wk] * Lc, K=[x[0] for x in lay], V=[x[1] for x in lay],
+                   Kp=[x[2] for x in lay], out=outs)
+
+    for i in range(R):
+        step(i)
+    torch.cuda.synchronize()
+    tb.check_dev_status(stack.status, "layers warm-up")
+    M = R * max(1, 100 // R)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(M):
+            step(i)
+    kernel_nodes = _count_kernel_nodes(g)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    tb.check_dev_status(stack.status, "layers graph warm-up")
+    reps = max(1, args.steps // (M * Lc))
+    clocks = ClockSampler(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        g.replay()
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    tb.check_dev_status(stack.status, "layers timed steps")
+    ms = e0.elapsed_time(e1)
+    steps = reps * M
+    per_step = ms / 1e3 / steps
+    per_layer = per_step / Lc
+    gather = sum(int(c.sum().item()) for c in stack.counts) / Lc * 2 * w.D * 2
+    layer_bytes = kp_bytes + gather + qio_bytes + append_bytes
+    hbm_peak, peak_kind = _peaks()
+    achieved = layer_bytes / per_layer / 1e9
+    line = {
+        "metric": "decode steps/s of an L-layer stack (per-layer time and HBM roofline), N=32K, budget 10%",
+        "value": 1.0 / per_step, "unit": "decode steps/s", "n_gpus": 1, "steps": steps, "warmup": 3 * M,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}-x{Lc}layers", "layers": Lc, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "dp": w.dp, "N": w.N, "k": w.k, "T": 1, "r": 0, "rotation_sets": R,
+                   "l2_defeat": f"{R} sets of {Lc} layers rotate ({R * Lc * layer_bytes / 1e6:.0f} MB, "
+                                f"L2 {l2 / 1e6:.0f} MB)"},
+        "us_per_layer": per_layer * 1e6, "bytes_per_layer": layer_bytes,
+        "tokens_per_s": w.B / per_step,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": peak_kind,
+                     "kernel": "per layer: selection kernel (second stream) + attention kernel, overlapped"},
+        "kernels_per_step": kernel_nodes / M if kernel_nodes is not None else None,
+        "gpu_launches": int(round(kernel_nodes / M * steps)) if kernel_nodes is not None else None,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     w = _workload(args.workload)
+    if args.budget > 0:
+        import dataclasses
+        w = dataclasses.replace(w, k=int(math.ceil(args.budget * w.N - 1e-9)))
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.layers:
+        run_layers(args, w)
     elif args.offload:
         run_offload(args, w)
     elif args.buffers:

@@ -101,6 +101,15 @@ typedef struct {
    selection holds at most k tokens (plus the tail). idx_state then holds kc
    entries per row, packed ([B, Hkv, kc]). With r == 0 it changes nothing. */
 #define TB_STEP_BUDGET_NEIGHBOURS 2
+/* tb_step_params.flags: run a step with a prediction, T == 1 and r == 0 as
+   three kernels with no grid-wide waits instead of the single cooperative
+   kernel: the top k of the n cached tokens is selected first (their scores,
+   then the exact cut), then token n is appended and displaces the k-th of
+   them when it scores above it, which is the top k of all n + 1 tokens. Needs
+   D in {64, 128}, dp in {16, 32, 64}, G <= 16, n >= 1024 and K/V in device
+   memory (otherwise the flag is ignored). Same results up to the fp32
+   rounding of the scores. These kernels also carry tb_decode_layers. */
+#define TB_STEP_PIPELINE 4
 
 /* Text for a status code (static storage). */
 TB_API const char *tb_status_string(tb_status st);
@@ -201,8 +210,9 @@ TB_API tb_status tb_sparse_decode_attn(const tb_shape *shape, const tb_bf16 *q, 
  * counts [B,Hkv] persist across the steps of an interval; sel_stride must be
  * >= min(n+1, kc(2r+1)) + T - 1, kc = k (or k / (2r+1), at least 1, with
  * TB_STEP_BUDGET_NEIGHBOURS). The steps of an interval must be issued in
- * order with consecutive t and n. With T == 1 and r == 0 the whole step runs
- * as one fused kernel.
+ * order with consecutive t and n. With T == 1 and r == 0 the step runs as one
+ * cooperative kernel where the shape allows (see TB_STEP_PIPELINE for the
+ * three-kernel form).
  */
 TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *params, int64_t t, int64_t n,
                          const tb_bf16 *q, const tb_bf16 *q_imp, const tb_bf16 *K_new,
@@ -210,6 +220,46 @@ TB_API tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *par
                          tb_bf16 *Kp, int32_t *idx_state, int64_t *n_pred, int32_t *sel,
                          int32_t sel_stride, int32_t *counts, tb_bf16 *out,
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* One layer's buffers for tb_decode_layers; each as for tb_decode_step. The
+   workspace (tb_workspace_size bytes, zero-filled once) is the layer's own:
+   the layers' kernels overlap on the GPU. */
+typedef struct {
+    const tb_bf16 *q, *q_imp, *K_new, *V_new, *Wk;
+    tb_bf16 *K, *V, *Kp;
+    int32_t *idx_state, *sel, *counts;
+    tb_bf16 *out;
+    void *ws;
+    size_t ws_bytes;
+} tb_layer_buffers;
+
+/*
+ * One decode step of L consumer layers that share one producer layer
+ * ("TokenButler: Token Importance is Predictable", gist.science summary,
+ * Core Architecture: the importance queries are predicted at a producer
+ * layer and scored against the projected keys of the layers after it).
+ * Layer l's result is exactly tb_decode_step's with a prediction, T == 1 and
+ * r == 0, on layers[l]; n is every layer's token count before the append.
+ *
+ * Because every layer's q_imp is known before the first of them runs, the
+ * selection of layer l (its n cached tokens scored against q_imp, the top k
+ * kept) needs nothing from layer l - 1 and runs on select_stream while
+ * earlier layers attend on `stream`. Layer l's attention kernel (the append
+ * of its new token, that token scored against the layer's k-th, the gather
+ * and the attention) runs on `stream` in layer order after its own
+ * selection; it gathers the kept rows first and reads q, K_new and V_new,
+ * which in a model come from layer l - 1's output, only once layer l - 1's
+ * attention kernel has finished. select_stream first waits for the work
+ * already on `stream`; on return `stream` waits for select_stream. Two
+ * events per host thread and device are created on first use (no device
+ * memory). Needs the shapes of TB_STEP_PIPELINE, k <=
+ * n + 1, sel_stride >= k, device-resident K/V and one workspace per layer;
+ * otherwise TB_ERR_UNSUPPORTED or TB_ERR_INVALID_ARG before anything is
+ * enqueued.
+ */
+TB_API tb_status tb_decode_layers(const tb_shape *shape, const tb_step_params *params, int64_t n, int32_t L,
+                                  const tb_layer_buffers *layers, int32_t sel_stride, int32_t *dev_status,
+                                  cudaStream_t stream, cudaStream_t select_stream);
 
 /*
  * tb_decode_step for a ragged batch: sequence b holds n[b] tokens before

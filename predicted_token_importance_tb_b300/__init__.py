@@ -33,11 +33,12 @@ TB_AGG_MAX = 1
 
 TB_STEP_UNFUSED = 1
 TB_STEP_BUDGET_NEIGHBOURS = 2
+TB_STEP_PIPELINE = 4
 
 EXPORTED = (
     "tb_status_string", "tb_version", "tb_workspace_size", "tb_workspace_init", "tb_project_append",
     "tb_score", "tb_topk", "tb_expand", "tb_sparse_decode_attn", "tb_decode_step", "tb_topk_noalloc",
-    "tb_decode_step_buffered", "tb_predict_queries", "tb_decode_step_ragged",
+    "tb_decode_step_buffered", "tb_predict_queries", "tb_decode_step_ragged", "tb_decode_layers",
 )
 
 TB_TOPK_NOALLOC_MAX_ROWS = 64
@@ -61,6 +62,14 @@ class _StepParams(ctypes.Structure):
 
 class _BufferParams(ctypes.Structure):
     _fields_ = [("sink", ctypes.c_int32), ("window", ctypes.c_int32)]
+
+
+class _LayerBuffers(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("q_imp", ctypes.c_void_p), ("K_new", ctypes.c_void_p),
+                ("V_new", ctypes.c_void_p), ("Wk", ctypes.c_void_p), ("K", ctypes.c_void_p), ("V", ctypes.c_void_p),
+                ("Kp", ctypes.c_void_p), ("idx_state", ctypes.c_void_p), ("sel", ctypes.c_void_p),
+                ("counts", ctypes.c_void_p), ("out", ctypes.c_void_p), ("ws", ctypes.c_void_p),
+                ("ws_bytes", ctypes.c_size_t)]
 
 
 @dataclass(frozen=True)
@@ -110,6 +119,9 @@ def load_library(path: str = LIB_PATH):
         # sel_stride, counts, out, ws, ws_bytes, dev_status, stream
         lib.tb_decode_step_ragged.argtypes = [SP, ctypes.POINTER(_StepParams), i64, P, P, P, P, P, P, P, P, P, P, P,
                                               P, P, i32, P, P, P, sz, P, P]
+        # shape, params, n, L, layers, sel_stride, dev_status, stream, select_stream
+        lib.tb_decode_layers.argtypes = [SP, ctypes.POINTER(_StepParams), i64, i32, ctypes.POINTER(_LayerBuffers), i32,
+                                         P, P, P]
         lib.tb_decode_step_buffered.argtypes = [SP, ctypes.POINTER(_StepParams), ctypes.POINTER(_BufferParams), i64,
                                                 i64, P, P, P, P, P, P, P, P, P, ctypes.POINTER(i64),
                                                 ctypes.POINTER(i64), P, i32, P, P, P, sz, P, P]
@@ -409,13 +421,17 @@ def sel_stride_for(k: int, T: int, r: int, n_max: int) -> int:
 
 
 class DecodeLayer:
-    """Per-layer decode state on the device: the selection reused across a prediction interval."""
+    """Per-layer decode state on the device: the selection reused across a prediction interval.
+
+    fused=False runs every step as separate kernels; pipeline=True runs a step with T = 1 and r = 0 as the
+    three-kernel form instead of the single cooperative kernel (both give the results of tb_decode_step)."""
 
     def __init__(self, shape: Shape, k: int, T: int = 1, r: int = 0, agg: int = TB_AGG_MEAN,
                  scale: float | None = None, n_max: int | None = None, device=None, fused: bool = True,
-                 budget_neighbours: bool = False):
+                 budget_neighbours: bool = False, pipeline: bool = False):
         self.shape, self.k, self.T, self.r, self.agg = shape, k, T, r, agg
-        self.flags = (0 if fused else TB_STEP_UNFUSED) | (TB_STEP_BUDGET_NEIGHBOURS if budget_neighbours else 0)
+        self.flags = ((0 if fused else TB_STEP_UNFUSED) | (TB_STEP_BUDGET_NEIGHBOURS if budget_neighbours else 0)
+                      | (TB_STEP_PIPELINE if pipeline else 0))
         # centres kept per prediction (idx_state row length)
         self.kc = max(1, k // (2 * r + 1)) if budget_neighbours else k
         self.scale = scale if scale is not None else shape.D ** -0.5
@@ -456,6 +472,81 @@ class DecodeLayer:
         _check(self._lib.tb_decode_step(ctypes.byref(self._shape_c), ctypes.byref(self._params), t, n, pq, pqi, pkn,
                                         pvn, pwk, pk, pv, pkp, idx, ctypes.byref(self.n_pred), sel, self.sel_stride,
                                         cnt, pout, ws, wsb, st, _stream(stream)), "tb_decode_step")
+        return out
+
+
+def tb_decode_layers(shape: Shape, k: int, agg: int, scale: float, n: int, layers, sel_stride: int,
+                     dev_status=None, stream=None, select_stream=None):
+    """One decode step of len(layers) consumer layers (see include/tb.h): layer l's selection runs on
+    select_stream while earlier layers attend on stream. layers: one dict per layer with the tensors of
+    tb_decode_step (q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, sel, counts, out) and its own zero-filled
+    workspace ws."""
+    if select_stream is None:
+        raise ValueError("tb_decode_layers needs a select_stream distinct from stream")
+    arr = (_LayerBuffers * len(layers))()
+    for i, y in enumerate(layers):
+        _need_step(shape, y["q"], y["q_imp"], y["K_new"], y["V_new"], y["Wk"], y["K"], y["V"], y["Kp"], y["out"])
+        _need_state(shape, k, sel_stride, y["idx_state"], y["sel"], y["counts"])
+        arr[i] = _LayerBuffers(
+            _bf16(y["q"], "q"), _bf16(y["q_imp"], "q_imp"), _bf16(y["K_new"], "K_new"), _bf16(y["V_new"], "V_new"),
+            _bf16(y["Wk"], "Wk"), _bf16(y["K"], "K"), _bf16(y["V"], "V"), _bf16(y["Kp"], "Kp"),
+            _i32(y["idx_state"], "idx_state"), _i32(y["sel"], "sel"), _i32(y["counts"], "counts"),
+            _bf16(y["out"], "out"), _ptr(y["ws"]), _nbytes(y["ws"]))
+    params = _StepParams(k, 1, 0, agg, scale, 0)
+    _check(load_library().tb_decode_layers(ctypes.byref(shape.c()), ctypes.byref(params), n, len(layers), arr,
+                                           sel_stride, _status_ptr(dev_status), _stream(stream),
+                                           _stream(select_stream)), "tb_decode_layers")
+
+
+class DecodeStack:
+    """Decode state of L consumer layers stepped together by tb_decode_layers (T = 1, r = 0): per layer its
+    selection, counts and own workspace. step() takes per-layer lists of the step's tensors."""
+
+    def __init__(self, shape: Shape, L: int, k: int, agg: int = TB_AGG_MEAN, scale: float | None = None,
+                 n_max: int | None = None, device=None):
+        self.shape, self.L, self.k, self.agg = shape, L, k, agg
+        self.scale = scale if scale is not None else shape.D ** -0.5
+        n_max = shape.cap - 1 if n_max is None else n_max
+        dev = device or "cuda"
+        rows = (shape.B, shape.Hkv)
+        self.sel_stride = k
+        self.idx_state = [torch.zeros(rows + (k,), dtype=torch.int32, device=dev) for _ in range(L)]
+        self.sel = [torch.zeros(rows + (k,), dtype=torch.int32, device=dev) for _ in range(L)]
+        self.counts = [torch.zeros(rows, dtype=torch.int32, device=dev) for _ in range(L)]
+        self.ws = [workspace(shape, n_max, k, k, device=dev) for _ in range(L)]
+        self.status = dev_status(dev)
+        self.select_stream = torch.cuda.Stream(device=dev)
+        self._lib = load_library()
+        self._shape_c = shape.c()
+        self._params = _StepParams(k, 1, 0, agg, self.scale, 0)
+        self._seen = {}
+
+    def _arr(self, per_layer):
+        key = tuple((id(x), x.data_ptr()) for y in per_layer for x in y)
+        got = self._seen.get(key)
+        if got is None:
+            arr = (_LayerBuffers * self.L)()
+            for l, (q, q_imp, K_new, V_new, Wk, K, V, Kp, out) in enumerate(per_layer):
+                _need_step(self.shape, q, q_imp, K_new, V_new, Wk, K, V, Kp, out)
+                arr[l] = _LayerBuffers(
+                    _bf16(q, "q"), _bf16(q_imp, "q_imp"), _bf16(K_new, "K_new"), _bf16(V_new, "V_new"),
+                    _bf16(Wk, "Wk"), _bf16(K, "K"), _bf16(V, "V"), _bf16(Kp, "Kp"),
+                    _i32(self.idx_state[l], "idx_state"), _i32(self.sel[l], "sel"), _i32(self.counts[l], "counts"),
+                    _bf16(out, "out"), _ptr(self.ws[l]), _nbytes(self.ws[l]))
+            if len(self._seen) > 64:
+                self._seen.clear()
+            self._seen[key] = got = arr
+        return got
+
+    def step(self, n: int, *, q, q_imp, K_new, V_new, Wk, K, V, Kp, out, stream=None):
+        """Each argument is a list of L tensors (layer order). n: tokens per layer before this step's append."""
+        per_layer = list(zip(q, q_imp, K_new, V_new, Wk, K, V, Kp, out))
+        if len(per_layer) != self.L:
+            raise ValueError(f"expected {self.L} layers, got {len(per_layer)}")
+        arr = self._arr(per_layer)
+        _check(self._lib.tb_decode_layers(ctypes.byref(self._shape_c), ctypes.byref(self._params), n, self.L, arr,
+                                          self.sel_stride, _status_ptr(self.status), _stream(stream),
+                                          _stream(self.select_stream)), "tb_decode_layers")
         return out
 
 

@@ -94,17 +94,62 @@ def nvcc() -> str:
     return "nvcc"
 
 
+OBJ_DIR = os.path.join(PKG, "_build")
+
+
+def _unit_hash(src: str) -> str:
+    """A translation unit's object is current when this matches: its source, every header, the flags."""
+    h = hashlib.sha256()
+    for p in [src] + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "tb.h")]:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
+def _compile(src: str, verbose: bool) -> str:
+    """nvcc -c of one translation unit into _build/ (skipped when its object is current)."""
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+    stamp = obj + ".buildhash"
+    h = _unit_hash(src)
+    if os.path.exists(obj) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == h:
+                return obj
+    flags = [f for f in NVCC_FLAGS if f != "-shared"]
+    tmp = obj + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *flags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", tmp]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+        print(" ".join(cmd), flush=True)
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, obj)
+    with open(stamp, "w") as f:
+        f.write(h)
+    return obj
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every translation unit (in parallel, each only when it changed) and link libtb.so."""
     h = _hash()
     if not force and os.path.exists(LIB) and os.path.exists(STAMP):
         with open(STAMP) as f:
             if f.read().strip() == h:
                 return LIB
+    from concurrent.futures import ThreadPoolExecutor
+    srcs = _sources()
+    if force:
+        for src in srcs:
+            stamp = os.path.join(OBJ_DIR, os.path.basename(src) + ".o.buildhash")
+            if os.path.exists(stamp):
+                os.remove(stamp)
+    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-o", tmp, *_sources()]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd), flush=True)
+    cmd = [nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-Xcompiler", "-fPIC",
+           "-o", tmp, *objs]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     with open(STAMP, "w") as f:

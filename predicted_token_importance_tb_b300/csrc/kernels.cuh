@@ -89,6 +89,33 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
 // null) then receive the kept tokens of [keep_lo, keep_hi) minus keep_lo,
 // which sit at sel slots cpre .. cpre + ck.
 
+// The decode step (T == 1, r == 0) as three kernels with no grid-wide waits
+// (pipe_step.cu): selection over the n cached tokens (scores, keys, the row's
+// histogram), the bracket (the exact cut and each chunk's output offset),
+// then the attention kernel that appends token n, lets it displace the row's
+// k-th token when it scores above it, and attends. The bracket and the
+// attention kernel are programmatic dependent launches. chain: the attention
+// kernel follows the previous layer's attention kernel on its stream and its
+// own layer's bracket kernel on another (the multi-layer step); otherwise it
+// follows its own bracket kernel.
+struct PipeGeom {
+    int C;    // chunks (CTAs) per row
+    int cs;   // tokens per chunk, a multiple of 16
+};
+bool pipe_supported(const tb_shape &sh, int64_t n, int32_t k);
+PipeGeom pipe_geom(const tb_shape &sh, int64_t n);
+cudaError_t launch_pipe_select(const tb_shape &sh, const PipeGeom &g, int agg, int64_t n, const uint16_t *q_imp,
+                               const uint16_t *Kp, PipeRow *ctl, uint32_t *keys, int64_t keys_stride, bool chain,
+                               int32_t *dev_status, cudaStream_t st);
+cudaError_t launch_pipe_bracket(const tb_shape &sh, const PipeGeom &g, int32_t k, int64_t n, PipeRow *ctl,
+                                const uint32_t *keys, int64_t keys_stride, uint2 *cand, int32_t *dev_status,
+                                cudaStream_t st);
+cudaError_t launch_pipe_attend(const tb_shape &sh, const PipeGeom &g, const tb_step_params &p, int64_t n, bool chain,
+                               const uint16_t *q, const uint16_t *q_imp, const uint16_t *K_new, const uint16_t *V_new,
+                               const uint16_t *Wk, uint16_t *K, uint16_t *V, uint16_t *Kp, int32_t *idx, int32_t *sel,
+                               int32_t sel_stride, int32_t *counts, uint16_t *out, PipeRow *ctl, const uint32_t *keys,
+                               int64_t keys_stride, float *part, int32_t *dev_status, cudaStream_t st);
+
 // The predictor MLP for B tokens: h [B, F] = SiLU(x W1^T) (fp32), q_imp [B, O] =
 // RNE(h W2^T). E and F multiples of 8, B <= 16.
 cudaError_t launch_predict(const uint16_t *x, const uint16_t *W1, const uint16_t *W2, int B, int E, int F, int O,

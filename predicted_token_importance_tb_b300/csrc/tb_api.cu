@@ -56,6 +56,49 @@ static WsLayout layout_for(const tb_shape &s, int64_t n_scores, int64_t sel_stri
     return ws_layout(s, n_scores, sel_stride, fused_chunks_max);
 }
 
+// True when K and V are device memory (the bulk copies of the three-kernel
+// step read them; pinned host K/V take the other paths). The answer for the
+// last pair asked is kept per thread.
+static bool kv_on_device(const void *K, const void *V) {
+    static thread_local const void *last_k = nullptr, *last_v = nullptr;
+    static thread_local bool last = false;
+    if (K == last_k && V == last_v) return last;
+    bool ok = true;
+    for (const void *p : {K, V}) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess || at.type != cudaMemoryTypeDevice) {
+            cudaGetLastError();
+            ok = false;
+        }
+    }
+    last_k = K;
+    last_v = V;
+    last = ok;
+    return ok;
+}
+
+// Events that order the multi-layer step's two streams, created once per
+// host thread and device.
+struct StackEvents {
+    int device = -1;
+    cudaEvent_t fork = nullptr, sel = nullptr, join = nullptr;
+};
+static cudaError_t stack_events(StackEvents **out) {
+    static thread_local StackEvents ev[16];
+    const int dev = dev_info().device;
+    if (dev < 0 || dev >= 16) return cudaErrorInvalidDevice;
+    StackEvents &e = ev[dev];
+    if (e.device != dev) {
+        for (cudaEvent_t *x : {&e.fork, &e.sel, &e.join}) {
+            cudaError_t r = cudaEventCreateWithFlags(x, cudaEventDisableTiming);
+            if (r != cudaSuccess) return r;
+        }
+        e.device = dev;
+    }
+    *out = &e;
+    return cudaSuccess;
+}
+
 }  // namespace tb
 
 using namespace tb;
@@ -179,7 +222,7 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     TB_PTR(V);
     TB_PTR(Kp);
     TB_PTR(out);
-    if (p->flags & ~(TB_STEP_UNFUSED | TB_STEP_BUDGET_NEIGHBOURS)) return TB_ERR_INVALID_ARG;
+    if (p->flags & ~(TB_STEP_UNFUSED | TB_STEP_BUDGET_NEIGHBOURS | TB_STEP_PIPELINE)) return TB_ERR_INVALID_ARG;
     const int64_t n_t = n + 1;
     const bool predict = (t % p->T) == 0;
     // centres per prediction: k, or k / (2r + 1) (at least one) when the
@@ -194,8 +237,10 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     if ((int64_t)sel_stride < body + (n_t - np)) return TB_ERR_INVALID_ARG;
     const int rows = shape->B * shape->Hkv;
     const bool one_launch = predict && p->T == 1 && p->r == 0 && !(p->flags & TB_STEP_UNFUSED);
-    const bool fast = one_launch && fused_fast_supported(*shape, n_t, p->k);
-    const bool fused = one_launch && !fast && fused_step_supported(*shape, n_t, p->k);
+    const bool pipe = one_launch && (p->flags & TB_STEP_PIPELINE) && pipe_supported(*shape, n, p->k) &&
+                      kv_on_device(K, V);
+    const bool fast = one_launch && !pipe && fused_fast_supported(*shape, n_t, p->k);
+    const bool fused = one_launch && !pipe && !fast && fused_step_supported(*shape, n_t, p->k);
     const WsLayout L = layout_for(*shape, n_t, sel_stride, (fused || fast) ? fused_chunks(*shape, n_t) : 0);
     if (!ws || ws_bytes < L.total) return TB_ERR_WORKSPACE;
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -204,6 +249,25 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     float *part = reinterpret_cast<float *>(w + L.part_off);
     float *scores = reinterpret_cast<float *>(w + L.scores_off);
     cudaError_t e;
+    if (pipe) {
+        // selection over the n cached tokens, the bracket (the exact cut), then the attention kernel (append,
+        // the new token against the cut, gather, attention); the last two are programmatic dependents
+        const PipeGeom g = pipe_geom(*shape, n);
+        PipeRow *prow = reinterpret_cast<PipeRow *>(w + L.pipe_off);
+        uint32_t *keys = reinterpret_cast<uint32_t *>(w + L.pipe_keys_off);
+        e = launch_pipe_select(*shape, g, p->agg, n, q_imp, Kp, prow, keys, L.pipe_keys_stride, false, dev_status,
+                               stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = launch_pipe_bracket(*shape, g, p->k, n, prow, keys, L.pipe_keys_stride,
+                                reinterpret_cast<uint2 *>(w + L.pipe_cand_off), dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = launch_pipe_attend(*shape, g, *p, n, false, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, sel,
+                               sel_stride, counts, out, prow, keys, L.pipe_keys_stride,
+                               reinterpret_cast<float *>(w + L.pipe_part_off), dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        *n_pred = n_t;
+        return TB_OK;
+    }
     if (fast) {
         FastWs fw;
         fw.ctl = ctl;
@@ -249,6 +313,66 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     // 3. attention over the selection
     e = launch_attn(*shape, q, K, V, sel, counts, sel_stride, p->scale, out, actl, part, dev_status, stream);
     return from_cuda(e);
+}
+
+tb_status tb_decode_layers(const tb_shape *shape, const tb_step_params *p, int64_t n, int32_t L,
+                           const tb_layer_buffers *layers, int32_t sel_stride, int32_t *dev_status, cudaStream_t stream,
+                           cudaStream_t select_stream) {
+    TB_CHECK(check_shape(shape));
+    if (!p || !layers || L < 1) return TB_ERR_INVALID_ARG;
+    if (p->T != 1 || p->r != 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
+    if (p->flags != 0) return TB_ERR_INVALID_ARG;
+    if (n < 0 || n + 1 > shape->cap || p->k > n + 1) return TB_ERR_INVALID_ARG;
+    if (sel_stride < p->k) return TB_ERR_INVALID_ARG;
+    if (!pipe_supported(*shape, n, p->k)) return TB_ERR_UNSUPPORTED;
+    if (select_stream == stream) return TB_ERR_INVALID_ARG;
+    const WsLayout Lw = layout_for(*shape, n + 1, sel_stride, 0);
+    for (int32_t l = 0; l < L; ++l) {
+        const tb_layer_buffers &y = layers[l];
+        TB_PTR(y.q);
+        TB_PTR(y.q_imp);
+        TB_PTR(y.K_new);
+        TB_PTR(y.V_new);
+        TB_PTR(y.Wk);
+        TB_PTR(y.K);
+        TB_PTR(y.V);
+        TB_PTR(y.Kp);
+        TB_PTR(y.out);
+        if (!y.idx_state || !y.sel || !y.counts) return TB_ERR_INVALID_ARG;
+        if (!y.ws || y.ws_bytes < Lw.total) return TB_ERR_WORKSPACE;
+        for (int32_t m = 0; m < l; ++m)
+            if (layers[m].ws == y.ws) return TB_ERR_INVALID_ARG;   // layers overlap on the GPU: one workspace each
+    }
+    for (int32_t l = 0; l < L; ++l)
+        if (!kv_on_device(layers[l].K, layers[l].V)) return TB_ERR_UNSUPPORTED;
+    StackEvents *ev = nullptr;
+    cudaError_t e = stack_events(&ev);
+    if (e != cudaSuccess) return from_cuda(e);
+    const PipeGeom g = pipe_geom(*shape, n);
+    // the selection stream starts after everything already on the caller's stream (the previous step's appends)
+    if ((e = cudaEventRecord(ev->fork, stream)) != cudaSuccess) return from_cuda(e);
+    if ((e = cudaStreamWaitEvent(select_stream, ev->fork, 0)) != cudaSuccess) return from_cuda(e);
+    for (int32_t l = 0; l < L; ++l) {
+        const tb_layer_buffers &y = layers[l];
+        uint8_t *w = static_cast<uint8_t *>(y.ws);
+        PipeRow *prow = reinterpret_cast<PipeRow *>(w + Lw.pipe_off);
+        uint32_t *keys = reinterpret_cast<uint32_t *>(w + Lw.pipe_keys_off);
+        e = launch_pipe_select(*shape, g, p->agg, n, y.q_imp, y.Kp, prow, keys, Lw.pipe_keys_stride, true,
+                               dev_status, select_stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = launch_pipe_bracket(*shape, g, p->k, n, prow, keys, Lw.pipe_keys_stride,
+                                reinterpret_cast<uint2 *>(w + Lw.pipe_cand_off), dev_status, select_stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        if ((e = cudaEventRecord(ev->sel, select_stream)) != cudaSuccess) return from_cuda(e);
+        if ((e = cudaStreamWaitEvent(stream, ev->sel, 0)) != cudaSuccess) return from_cuda(e);
+        e = launch_pipe_attend(*shape, g, *p, n, true, y.q, y.q_imp, y.K_new, y.V_new, y.Wk, y.K, y.V, y.Kp,
+                               y.idx_state, y.sel, sel_stride, y.counts, y.out, prow, keys, Lw.pipe_keys_stride,
+                               reinterpret_cast<float *>(w + Lw.pipe_part_off), dev_status, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    if ((e = cudaEventRecord(ev->join, select_stream)) != cudaSuccess) return from_cuda(e);
+    if ((e = cudaStreamWaitEvent(stream, ev->join, 0)) != cudaSuccess) return from_cuda(e);
+    return TB_OK;
 }
 
 tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_params *p, int64_t t, const int64_t *n_host,

@@ -29,6 +29,27 @@ struct RowCtl {
     uint2 cand[kCandCap];            // (key, token) of the threshold bin's elements
 };
 
+// The three-kernel decode step (pipe_step.cu): per-row control and result
+// block. Zero between calls (the row's last CTAs put back what they used);
+// hist is the row's 12-bit histogram of score keys.
+constexpr int kPipeHBits = 12;
+constexpr int kPipeHBins = 1 << kPipeHBits;
+constexpr int kPipeMaxChunks = 64;            // CTAs that may share one row in the pipeline
+constexpr int kPipeCandCap = 4096;            // threshold-bin entries per row resolved in shared memory
+struct PipeRow {
+    uint32_t done2;                  // bracket CTAs finished with this row
+    uint32_t done3;                  // attention CTAs finished with this row
+    uint32_t ncand;                  // threshold-bin entries appended to the row's candidate list
+    uint32_t overflow;               // more of them than the list holds (the resolver then rescans the keys)
+    uint32_t b1;                     // result: the k-th token's 12-bit bin
+    uint32_t cut_key;                // result: key of the k-th ranked token among [0, n)
+    int32_t cut_idx;                 // result: its index
+    int32_t k1;                      // result: tokens kept among [0, n)
+    uint32_t cab[kPipeMaxChunks];    // per chunk: tokens above the threshold bin
+    int32_t offs[kPipeMaxChunks + 4];// result: output offset of each chunk's kept tokens (offs[C] = k1)
+    uint32_t hist[kPipeHBins];       // 12-bit histogram of the row's score keys
+};
+
 struct WsLayout {
     size_t rowctl_off = 0;   // rows x RowCtl
     size_t attn_ctl_off = 0; // rows x uint32 (split-merge counters)
@@ -37,6 +58,11 @@ struct WsLayout {
     size_t rec_off = 0;      // rows x fused chunks x kFastRecBytes (fast decode step records)
     size_t blk_off = 0;      // rows x blk_stride bytes (fast decode step per-block counts)
     int64_t blk_stride = 0;
+    size_t pipe_off = 0;     // rows x PipeRow (three-kernel step)
+    size_t pipe_keys_off = 0;// rows x pipe_keys_stride uint32 score keys
+    int64_t pipe_keys_stride = 0;
+    size_t pipe_part_off = 0;// rows x kPipeMaxChunks x G x (D + 2) fp32 partials
+    size_t pipe_cand_off = 0;// rows x kPipeCandCap (key, token) threshold-bin entries
     size_t total = 0;
     int64_t max_splits = 0;
 };
@@ -67,6 +93,10 @@ inline WsLayout ws_layout(const tb_shape &s, int64_t n_max, int64_t sel_stride_m
     off = round_up(off + (size_t)rows * sizeof(RowCtl), 256);
     L.attn_ctl_off = off;
     off = round_up(off + (size_t)rows * sizeof(uint32_t), 256);
+    // the three-kernel step's control blocks sit at an offset that depends on the shape only, so a later
+    // call with another token count finds the zeroed counters the previous call left
+    L.pipe_off = off;
+    off = round_up(off + (size_t)rows * sizeof(PipeRow), 256);
     L.part_off = off;
     off = round_up(off + (size_t)rows * splits * G * (s.D + 2) * sizeof(float), 256);
     L.scores_off = off;
@@ -78,6 +108,14 @@ inline WsLayout ws_layout(const tb_shape &s, int64_t n_max, int64_t sel_stride_m
         L.blk_off = off;
         off = round_up(off + (size_t)rows * L.blk_stride, 256);
     }
+    // the three-kernel step's score keys and partials
+    L.pipe_keys_stride = (int64_t)round_up((size_t)(n_max > 0 ? n_max : 1), 4);
+    L.pipe_keys_off = off;
+    off = round_up(off + (size_t)rows * L.pipe_keys_stride * sizeof(uint32_t), 256);
+    L.pipe_part_off = off;
+    off = round_up(off + (size_t)rows * kPipeMaxChunks * G * (s.D + 2) * sizeof(float), 256);
+    L.pipe_cand_off = off;
+    off = round_up(off + (size_t)rows * kPipeCandCap * 8, 256);
     L.total = off;
     return L;
 }

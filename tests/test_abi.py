@@ -232,3 +232,34 @@ def test_noalloc_row_limit_matches_the_header():
     with open(os.path.join(ROOT, "include", "tb.h")) as f:
         m = re.search(r"#define\s+TB_TOPK_NOALLOC_MAX_ROWS\s+(\d+)", f.read())
     assert m and int(m.group(1)) == tb.TB_TOPK_NOALLOC_MAX_ROWS
+
+
+def test_host_validation_of_the_layer_stack(lib_path):
+    # tb_decode_layers refuses bad settings before any CUDA call
+    import predicted_token_importance_tb_b300 as tb
+    lib = tb.load_library()
+    fake = 1 << 20
+    sp = tb.Shape(1, 32, 8, 128, 32, 40000).c()
+    arr = (tb._LayerBuffers * 2)()
+    for i in range(2):
+        arr[i] = tb._LayerBuffers(*([fake] * 12), fake + (i + 1) * 4096, 1 << 30)
+    s1, s2 = ctypes.c_void_p(0x10), ctypes.c_void_p(0x20)
+    cases = [
+        (tb._StepParams(3277, 2, 0, 0, 0.088, 0), 32767, 2, 3277, s1, s2, tb.TB_ERR_INVALID_ARG),   # T != 1
+        (tb._StepParams(3277, 1, 1, 0, 0.088, 0), 32767, 2, 3277, s1, s2, tb.TB_ERR_INVALID_ARG),   # r != 0
+        (tb._StepParams(3277, 1, 0, 0, 0.088, 0), 32767, 0, 3277, s1, s2, tb.TB_ERR_INVALID_ARG),   # no layers
+        (tb._StepParams(3277, 1, 0, 0, 0.088, 0), 32767, 2, 3000, s1, s2, tb.TB_ERR_INVALID_ARG),   # sel_stride < k
+        (tb._StepParams(3277, 1, 0, 0, 0.088, 0), 32767, 2, 3277, s1, s1, tb.TB_ERR_INVALID_ARG),   # one stream
+        (tb._StepParams(3277, 1, 0, 0, 0.088, 0), 500, 2, 3277, s1, s2, tb.TB_ERR_INVALID_ARG),     # k > n + 1
+        (tb._StepParams(300, 1, 0, 0, 0.088, 0), 500, 2, 3277, s1, s2, tb.TB_ERR_UNSUPPORTED),      # n too small
+        (tb._StepParams(3277, 1, 0, 0, 0.088, tb.TB_STEP_PIPELINE), 32767, 2, 3277, s1, s2,
+         tb.TB_ERR_INVALID_ARG),                                                                    # flags
+    ]
+    for params, n, L, stride, a, b, want in cases:
+        st = lib.tb_decode_layers(ctypes.byref(sp), ctypes.byref(params), n, L, arr, stride, None, a, b)
+        assert st == want, (params.T, params.r, n, L, stride, st)
+    # two layers sharing one workspace would overlap on the GPU
+    arr[1].ws = arr[0].ws
+    st = lib.tb_decode_layers(ctypes.byref(sp), ctypes.byref(tb._StepParams(3277, 1, 0, 0, 0.088, 0)), 32767, 2,
+                              arr, 3277, None, s1, s2)
+    assert st == tb.TB_ERR_INVALID_ARG

@@ -22,7 +22,7 @@ def _lib():
 
 
 def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=None, fused=True, agg=0,
-                      layer_hook=None, kv_host=False, budget_neighbours=False):
+                      layer_hook=None, kv_host=False, budget_neighbours=False, pipeline=False):
     """Drive `steps` decode steps per layer on the GPU and check every step against the oracle.
 
     The oracle starts from the GPU-projected prefix of Kp (identical inputs),
@@ -31,7 +31,8 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
     the oracle's expansion of the GPU's prediction, and the output against the
     oracle's attention over the GPU's selection. kv_host: K and V live in
     pinned host memory (the offloaded cache). budget_neighbours: k // (2r+1)
-    centres per prediction.
+    centres per prediction. pipeline: a step with T = 1, r = 0 runs as the
+    three-kernel form rather than the single cooperative kernel.
     """
     k = w.k if k is None else k
     cap = n0 + steps
@@ -47,7 +48,7 @@ def run_decode_parity(w: synth.Workload, n0: int, steps: int, layers=(0,), k=Non
         if kv_host:
             K, V = K.cpu().pin_memory(), V.cpu().pin_memory()
         dec = tb.DecodeLayer(shape, k, T=w.T, r=w.r, agg=agg, scale=w.scale, n_max=cap - 1, fused=fused,
-                             budget_neighbours=budget_neighbours)
+                             budget_neighbours=budget_neighbours, pipeline=pipeline)
         out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
         oK, oV = u16(L["K"]).copy(), u16(L["V"]).copy()
         oKp = u16(Kp).copy()
@@ -113,17 +114,20 @@ def test_decode_small_per_step(fused):
     run_decode_parity(w, n0=w.N - 1, steps=3, fused=fused)
 
 
+@pytest.mark.parametrize("pipeline", [False, True])
 @pytest.mark.parametrize("B,Hq,Hkv,D,dp,N,k,agg", [(2, 8, 2, 128, 32, 5000, 500, 0), (1, 4, 4, 64, 16, 777, 1, 0),
                                                    (1, 8, 2, 128, 32, 3001, 3001, 0), (3, 6, 3, 64, 24, 2500, 99, 1),
                                                    (1, 16, 1, 32, 8, 20000, 6000, 1), (4, 8, 8, 128, 16, 40, 7, 0),
                                                    (1, 16, 1, 128, 32, 20000, 2000, 0), (2, 32, 4, 64, 16, 9000, 900, 1)])
-def test_decode_fused_matches_oracle_shapes(B, Hq, Hkv, D, dp, N, k, agg):
+def test_decode_fused_matches_oracle_shapes(B, Hq, Hkv, D, dp, N, k, agg, pipeline):
+    # (shapes the three-kernel form does not take run the cooperative kernel either way)
     w = synth.small(B=B, Hq=Hq, Hkv=Hkv, D=D, dp=dp, N=N, k=k, seed=N + k, outliers=2)
-    run_decode_parity(w, n0=w.N - 1, steps=2, agg=agg)
+    run_decode_parity(w, n0=w.N - 1, steps=2, agg=agg, pipeline=pipeline)
 
 
 def test_decode_fused_equals_unfused_bitwise_selection():
-    # identical scores on both paths, so identical selections; outputs agree to rounding
+    # identical scores on the cooperative kernel and the separate kernels, so identical selections; outputs
+    # agree to rounding
     w = synth.WORKLOADS[1]
     cap = w.N
     n0 = w.N - 1
@@ -176,6 +180,21 @@ def test_decode_blocky_scores_fall_back_to_the_general_select():
     assert sum(general_select_steps(dec)) > 0
 
 
+def test_decode_blocky_scores_three_kernel_form():
+    # the same hot blocks through the three-kernel form (its selection has no local estimate to miss)
+    w = synth.WORKLOADS[1]
+
+    def hot_blocks(L):
+        g = torch.Generator().manual_seed(77)
+        nblk = L["K"].shape[2] // 32
+        hot = torch.randperm(nblk, generator=g)[: nblk // 10]
+        rows = (hot[:, None] * 32 + torch.arange(32)[None, :]).reshape(-1)
+        rows = rows[rows < L["K"].shape[2]]
+        L["K"][:, :, rows] = L["K"][:, :, rows] * 8
+
+    run_decode_parity(w, n0=w.N - 1, steps=2, layer_hook=hot_blocks, pipeline=True)
+
+
 def test_decode_small_interval_with_neighbours():
     w = synth.small(B=2, Hq=8, Hkv=2, D=128, dp=32, N=3000, k=100, T=4, r=1, seed=31, outliers=4)
     run_decode_parity(w, n0=w.N, steps=10)
@@ -186,15 +205,16 @@ def test_decode_interval_r2_group_of_one():
     run_decode_parity(w, n0=w.N, steps=7)
 
 
-@pytest.mark.parametrize("fused", [True, False])
-def test_decode_llama_layer_step(fused):
+@pytest.mark.parametrize("fused,pipeline", [(True, False), (True, True), (False, False)])
+def test_decode_llama_layer_step(fused, pipeline):
     # the 32K-token Llama-3-8B-shaped layer: one step at N = 32768 after the append
     w = synth.WORKLOADS[1]
-    run_decode_parity(w, n0=w.N - 1, steps=2, fused=fused)
+    run_decode_parity(w, n0=w.N - 1, steps=2, fused=fused, pipeline=pipeline)
 
 
 def test_decode_32layer_stack_interval_sampled_layers():
-    # the 32-layer B=8 stack at full per-layer shape: layers 0 and 31, all 64 steps
+    # the 32-layer B=8 stack at full per-layer shape, two of its 32 layers sampled (0 and 31; every layer runs
+    # the same code on its own seeded data), all 64 steps
     w = synth.WORKLOADS[2]
     run_decode_parity(w, n0=w.N, steps=w.steps, layers=(0, 31))
 
