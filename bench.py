@@ -940,10 +940,11 @@ def run_layers(args, w):
     M = R * max(1, 100 // R)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    g = torch.cuda.CUDAGraph()
+    g = torch.cuda.CUDAGraph(keep_graph=True)
     with torch.cuda.graph(g, stream=s):
         for i in range(M):
             step(i)
+    g.instantiate()
     kernel_nodes = _count_kernel_nodes(g)
     for _ in range(3):
         g.replay()
@@ -991,6 +992,177 @@ def run_layers(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_stack(args, w):
+    """The 32-layer stack workload: every decode step runs tb_decode_step on each of the L layers in turn (B
+    sequences, the prediction every T steps, +-r neighbours, the tail between predictions), for the workload's
+    step count. The layers' caches are generated on the device (seeded; the distributions of the synthetic
+    recipe: K, V ~ N(0, 1) with the outlier key channels scaled, Wk ~ N(0, 1/D), fresh q, q_imp, K_new, V_new
+    ~ N(0, 1) per layer and step). The whole sequence of steps is one CUDA graph; prediction steps and reuse
+    steps are also timed on their own. Bytes come from the realised selection sizes."""
+    import predicted_token_importance_tb_b300 as tb
+
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    tb.load_library()
+    Lc, steps, n0 = w.layers, w.steps, w.N
+    cap = n0 + steps
+    shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, cap)
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    oc = torch.randperm(w.D, generator=torch.Generator().manual_seed(w.seed))[: w.outliers].cuda()
+    layers = []
+    for l in range(Lc):
+        K = torch.zeros((w.B, w.Hkv, cap, w.D), dtype=torch.bfloat16, device="cuda")
+        V = torch.zeros_like(K)
+        Kf = torch.randn((w.B, w.Hkv, n0, w.D), device="cuda", generator=g)
+        Kf[..., oc] *= w.outlier_scale
+        K[:, :, :n0] = Kf.to(torch.bfloat16)
+        del Kf
+        V[:, :, :n0] = torch.randn((w.B, w.Hkv, n0, w.D), device="cuda", generator=g).to(torch.bfloat16)
+        Wk = (torch.randn((w.Hkv, w.D, w.dp), device="cuda", generator=g) * w.D ** -0.5).to(torch.bfloat16)
+        Kp = torch.zeros((w.B, w.Hkv, cap, w.dp), dtype=torch.bfloat16, device="cuda")
+        tb.tb_project_append(shape, K, cap, Wk, Kp, 0, n0)
+        dec = tb.DecodeLayer(shape, w.k, T=w.T, r=w.r, scale=w.scale, n_max=cap - 1)
+        layers.append(dict(K=K, V=V, Wk=Wk, Kp=Kp, dec=dec))
+    ins = []
+    for t in range(steps):
+        row = []
+        for l in range(Lc):
+            kn = torch.randn((w.B, w.Hkv, w.D), device="cuda", generator=g)
+            kn[..., oc] *= w.outlier_scale
+            row.append(dict(q=torch.randn((w.B, w.Hq, w.D), device="cuda", generator=g).to(torch.bfloat16),
+                            q_imp=torch.randn((w.B, w.Hq, w.dp), device="cuda", generator=g).to(torch.bfloat16),
+                            K_new=kn.to(torch.bfloat16),
+                            V_new=torch.randn((w.B, w.Hkv, w.D), device="cuda", generator=g).to(torch.bfloat16)))
+        ins.append(row)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+
+    def one(t, l):
+        y, d = layers[l], ins[t][l]
+        y["dec"].step(t, n0 + t, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"], Wk=y["Wk"], K=y["K"],
+                      V=y["V"], Kp=y["Kp"], out=out)
+
+    # one eager pass: realised selection sizes per step (bytes), status
+    rows = w.B * w.Hkv
+    sel_rows = []
+    for t in range(steps):
+        tot = 0
+        for l in range(Lc):
+            one(t, l)
+            tot += int(layers[l]["dec"].counts.sum().item())
+        sel_rows.append(tot)
+    for y in layers:
+        tb.check_dev_status(y["dec"].status, "stack warm-up")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def capture(ts):
+        gr = torch.cuda.CUDAGraph(keep_graph=True)
+        with torch.cuda.graph(gr, stream=s):
+            for t in ts:
+                for l in range(Lc):
+                    one(t, l)
+        return gr
+
+    g_all = capture(range(steps))
+    g_pred = capture([0])            # a prediction step of every layer
+    g_reuse = capture([w.T - 1])     # the last step of an interval: the longest tail
+    for gr in (g_all, g_pred, g_reuse):
+        gr.instantiate()
+    kernel_nodes = _count_kernel_nodes(g_all)
+
+    def timed(gr, reps):
+        for _ in range(2):
+            gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            gr.replay()
+            e0.record(s)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    reps = max(1, min(20, args.steps // steps))
+    ms_all = timed(g_all, reps)
+    clk = clocks.stop()
+    ms_pred = timed(g_pred, 20)
+    ms_reuse = timed(g_reuse, 20)
+    for y in layers:
+        tb.check_dev_status(y["dec"].status, "stack timed steps")
+    per_step = ms_all / 1e3 / steps
+    kp_pred = rows * w.dp * 2       # per cached token per layer, at a prediction step
+    qio = (w.B * w.Hq * w.D * 2) * 2 + w.B * w.Hq * w.dp * 2
+    append = rows * w.D * 2 * 2 * 2 + w.Hkv * w.D * w.dp * 2 + rows * w.dp * 2
+    total = 0
+    for t in range(steps):
+        total += sel_rows[t] * 2 * w.D * 2 + Lc * (qio + append)
+        if t % w.T == 0:
+            total += Lc * kp_pred * (n0 + t + 1)
+    bytes_per_step = total / steps
+    hbm_peak, peak_kind = _peaks()
+    achieved = bytes_per_step / per_step / 1e9
+    pred_bytes = sel_rows[0] * 2 * w.D * 2 + Lc * (qio + append + kp_pred * (n0 + 1))
+    reuse_bytes = sel_rows[w.T - 1] * 2 * w.D * 2 + Lc * (qio + append)
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = _stack_cpu_baseline(w)
+    line = {
+        "metric": "decode steps/s of the 32-layer stack (B=8, N=16K, k=1024, prediction every T=16 steps, r=1)",
+        "value": 1.0 / per_step, "unit": "decode steps/s", "n_gpus": 1, "steps": steps * reps,
+        "warmup": 2 * steps, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device-generated, seeded)",
+        "config": {"workload": w.name, "layers": Lc, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "dp": w.dp,
+                   "N0": n0, "k": w.k, "T": w.T, "r": w.r, "steps": steps,
+                   "l2_defeat": f"{Lc} layers of {(2 * w.D + w.dp) * 2 * rows * cap / 1e9:.2f} GB each per step"},
+        "tokens_per_s": w.B / per_step, "us_per_layer_step": per_step * 1e6 / Lc,
+        "bytes_per_step": bytes_per_step, "selected_rows_per_step": sum(sel_rows) / steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": peak_kind,
+                     "kernel": "tb_decode_step per layer (prediction: append, score, top-k, expand, attention; "
+                               "reuse: append with the tail entry, attention)"},
+        "prediction_step": {"us": ms_pred * 1e3, "bytes": pred_bytes,
+                            "gbs": pred_bytes / (ms_pred / 1e3) / 1e9,
+                            "frac": pred_bytes / (ms_pred / 1e3) / 1e9 / hbm_peak},
+        "reuse_step": {"us": ms_reuse * 1e3, "bytes": reuse_bytes,
+                       "gbs": reuse_bytes / (ms_reuse / 1e3) / 1e9,
+                       "frac": reuse_bytes / (ms_reuse / 1e3) / 1e9 / hbm_peak},
+        "kernels_per_step": kernel_nodes / steps if kernel_nodes is not None else None,
+        "gpu_launches": int(kernel_nodes * reps) if kernel_nodes is not None else None,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _stack_cpu_baseline(w, layers_sampled: int = 1):
+    """The oracle on a bounded sample of the stack: one layer through one prediction interval (T steps),
+    scaled to whole 32-layer steps."""
+    import oracle
+    cap = w.N + w.T
+    L = synth.make_layer(w, layer=0, cap=cap, n=w.N)
+    oK, oV = oracle.as_u16(L["K"]).copy(), oracle.as_u16(L["V"]).copy()
+    oKp = np.zeros((w.B, w.Hkv, cap, w.dp), dtype=np.uint16)
+    oKp[:, :, :w.N], _ = oracle.project(np.ascontiguousarray(oK[:, :, :w.N]), L["Wk"])
+    st = oracle.DecodeState()
+    ds = [synth.make_step(w, 0, t, L["outlier_ch"]) for t in range(w.T)]
+    t0 = time.perf_counter()
+    for t in range(w.T):
+        d = ds[t]
+        oracle.decode_step(st, t, w.N + t, q=d["q"], q_imp=d["q_imp"], K_new=d["K_new"], V_new=d["V_new"],
+                           Wk=L["Wk"], K=oK, V=oV, Kp=oKp, k=w.k, T=w.T, r=w.r, agg=oracle.AGG_MEAN, scale=w.scale)
+    el = time.perf_counter() - t0
+    per_layer_step = el / w.T
+    return {"value": 1.0 / (per_layer_step * w.layers), "unit": "decode steps/s",
+            "cores": min(oracle.num_threads(), w.B * w.Hq), "kind": "oracle",
+            "sample": f"layer 0 through one prediction interval ({w.T} steps, {el:.1f} s), scaled to "
+                      f"{w.layers}-layer steps"}
+
+
 def main():
     args = _args()
     w = _workload(args.workload)
@@ -1001,6 +1173,8 @@ def main():
         run_reference(args, w)
     elif args.layers:
         run_layers(args, w)
+    elif w.layers > 1:
+        run_stack(args, w)
     elif args.offload:
         run_offload(args, w)
     elif args.buffers:

@@ -73,6 +73,7 @@ struct FFArgs {
     uint8_t *rec;        // rows x C records of kFFRecBytes
     uint8_t *blk_above;  // rows x blk_stride: per 32-token block, tokens above the owner's window
     uint32_t *keys_g;    // rows x keys_stride: keys in token order (general path)
+    const WsDebug *dbg;  // test hook (zero in normal use)
     int32_t *dev_status;
     int64_t cap, n, keys_stride;
     int64_t keep_lo, keep_hi;   // tokens t < keep_lo or t >= keep_hi are always kept (maximal key)
@@ -493,6 +494,10 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     const int row = blockIdx.x / C, c = blockIdx.x % C;
     const int b = row / a.Hkv, h = row % a.Hkv;
     const int64_t n_t = a.n + 1;
+    // the workspace's test hook: a shorter limit for the exchange waits, one CTA of row 0 that leaves out its
+    // arrival (both zero in normal use)
+    const uint64_t wlim = a.dbg->wait_limit_ns ? a.dbg->wait_limit_ns : kWaitLimitNs;
+    const bool skip_arrive = row == 0 && a.dbg->skip_arrive_cta == c + 1;
     const int nblk = (int)((n_t + 31) >> 5);
     const int nb = c < nblk ? (nblk - 1 - c) / C + 1 : 0;   // blocks this CTA owns
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -802,7 +807,8 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
         hd.pad0 = hd.pad1 = hd.pad2 = 0;
         *reinterpret_cast<FFHdr *>(myrec) = hd;
     }
-    group_arrive(&rc->bar);
+    if (!skip_arrive) group_arrive(&rc->bar);
+    else __syncthreads();
 
     // ---- 4b. the attention list: the tokens above the window (every one of
     // them is kept), then the window's kept tokens (wk, known after the
@@ -827,7 +833,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
     gather_rows(0, 0, n_r1);
 
     // ---- 5. the row's exchange; read every record of the row
-    if (!group_wait(&rc->bar, (uint32_t)C, S.abort_flag, a.dev_status)) {
+    if (!group_wait(&rc->bar, (uint32_t)C, S.abort_flag, a.dev_status, wlim)) {
         cp_async_wait_all();
         return;
     }
@@ -1069,7 +1075,7 @@ __global__ void __launch_bounds__(kFFThreads, 1) fused_fast_kernel(const FFArgs 
             }
             if (c == 0 && threadIdx.x == 0) a.counts[row] = a.k;
         }
-        if (!group_wait(&rc->bar, 2u * (uint32_t)C, S.abort_flag, a.dev_status)) return;
+        if (!group_wait(&rc->bar, 2u * (uint32_t)C, S.abort_flag, a.dev_status, wlim)) return;
         uint32_t done_prev = 0;
         if (threadIdx.x == 0) done_prev = atomicAdd(&rc->done, 1u);
         row_merge_slice(prow, C, c, G, DT, a.out + ((int64_t)b * a.Hq + (int64_t)h * G) * DT,
@@ -1216,7 +1222,7 @@ cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64
     a.q = q; a.q_imp = q_imp; a.K_new = K_new; a.V_new = V_new; a.Wk = Wk;
     a.K = K; a.V = V; a.Kp = Kp;
     a.idx = idx_state; a.sel = sel; a.counts = counts; a.out = out;
-    a.ctl = w.ctl; a.part = w.part; a.rec = w.rec; a.blk_above = w.blk_above; a.keys_g = w.keys_g;
+    a.ctl = w.ctl; a.part = w.part; a.rec = w.rec; a.blk_above = w.blk_above; a.keys_g = w.keys_g; a.dbg = w.dbg;
     a.dev_status = dev_status;
     a.cap = sh.cap; a.n = n; a.keys_stride = w.keys_stride;
     a.Hq = sh.Hq; a.Hkv = sh.Hkv; a.D = sh.D; a.k = k_keep > 0 ? k_keep : p.k; a.agg = p.agg;

@@ -75,6 +75,7 @@ struct FastWs {
     int64_t blk_stride;
     uint32_t *keys_g;
     int64_t keys_stride;
+    const WsDebug *dbg;
 };
 bool fused_fast_supported(const tb_shape &sh, int64_t n_tokens, int32_t k);
 cudaError_t launch_fused_fast(const tb_shape &sh, const tb_step_params &p, int64_t n, const uint16_t *q,

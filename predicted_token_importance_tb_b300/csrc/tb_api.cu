@@ -277,6 +277,7 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
         fw.blk_stride = L.blk_stride;
         fw.keys_g = reinterpret_cast<uint32_t *>(scores);
         fw.keys_stride = n_t;
+        fw.dbg = reinterpret_cast<const WsDebug *>(w + L.debug_off);
         e = launch_fused_fast(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, idx_state, sel, counts, out, fw,
                               sel_stride, dev_status, stream);
         if (e != cudaSuccess) return from_cuda(e);
@@ -533,6 +534,7 @@ tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *p
         fw.blk_stride = L.blk_stride;
         fw.keys_g = reinterpret_cast<uint32_t *>(scores);
         fw.keys_stride = n_t;
+        fw.dbg = reinterpret_cast<const WsDebug *>(w + L.debug_off);
         // candidates [S, P): everything outside is forced (with P <= S, everything)
         e = launch_fused_fast(*shape, *p, n, q, q_imp, K_new, V_new, Wk, K, V, Kp, nullptr, sel, counts, out, fw,
                               sel_stride, dev_status, stream, k_keep, S, P > S ? P : S, idx_state, pre, kc);

@@ -68,12 +68,13 @@ __device__ __forceinline__ void group_arrive(uint32_t *ctr) {
 
 // Wait: thread 0 polls with acquire loads, then the CTA barrier passes the
 // acquired view on to every thread of the CTA.
-__device__ __forceinline__ bool group_wait(uint32_t *ctr, uint32_t target, int *abort_flag, int32_t *dev_status) {
+__device__ __forceinline__ bool group_wait(uint32_t *ctr, uint32_t target, int *abort_flag, int32_t *dev_status,
+                                           uint64_t limit_ns = kWaitLimitNs) {
     if (threadIdx.x == 0) {
         if (ld_acquire(ctr) < target) {
             const uint64_t t0 = global_ns();
             while (ld_acquire(ctr) < target) {
-                if (global_ns() - t0 > kWaitLimitNs) {
+                if (global_ns() - t0 > limit_ns) {
                     *abort_flag = 1;
                     set_status(dev_status, TB_ERR_TIMEOUT);
                     break;
@@ -86,9 +87,9 @@ __device__ __forceinline__ bool group_wait(uint32_t *ctr, uint32_t target, int *
 }
 
 __device__ __forceinline__ bool group_barrier(uint32_t *ctr, uint32_t target, int *abort_flag,
-                                              int32_t *dev_status) {
+                                              int32_t *dev_status, uint64_t limit_ns = kWaitLimitNs) {
     group_arrive(ctr);
-    return group_wait(ctr, target, abort_flag, dev_status);
+    return group_wait(ctr, target, abort_flag, dev_status, limit_ns);
 }
 
 // ------------------------------------------------------------------ scans

@@ -50,8 +50,21 @@ struct PipeRow {
     uint32_t hist[kPipeHBins];       // 12-bit histogram of the row's score keys
 };
 
+// Test hook of the single-launch step, at a fixed offset after the row
+// control blocks; zero in normal use (tb_workspace_init clears it). A
+// non-zero wait_limit_ns replaces the limit of the kernel's bounded waits;
+// skip_arrive_cta = c + 1 makes chunk c of row 0 leave out its arrival at the
+// row's exchange, so that row's waits run out and report TB_ERR_TIMEOUT (a
+// barrier that nothing completes, without any fault).
+struct WsDebug {
+    uint64_t wait_limit_ns;
+    int32_t skip_arrive_cta;
+    int32_t pad[61];
+};
+
 struct WsLayout {
     size_t rowctl_off = 0;   // rows x RowCtl
+    size_t debug_off = 0;    // one WsDebug
     size_t attn_ctl_off = 0; // rows x uint32 (split-merge counters)
     size_t part_off = 0;     // rows x max_splits x G x (D + 2) fp32 partials
     size_t scores_off = 0;   // rows x n_max fp32 (decode-step scores; keys of the fast step's re-split)
@@ -91,6 +104,8 @@ inline WsLayout ws_layout(const tb_shape &s, int64_t n_max, int64_t sel_stride_m
     size_t off = 0;
     L.rowctl_off = off;
     off = round_up(off + (size_t)rows * sizeof(RowCtl), 256);
+    L.debug_off = off;
+    off = round_up(off + sizeof(WsDebug), 256);
     L.attn_ctl_off = off;
     off = round_up(off + (size_t)rows * sizeof(uint32_t), 256);
     // the three-kernel step's control blocks sit at an offset that depends on the shape only, so a later
