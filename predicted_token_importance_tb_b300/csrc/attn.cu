@@ -69,6 +69,9 @@ cudaError_t launch_attn(const tb_shape &sh, const uint16_t *q, const uint16_t *K
     const int rows = sh.B * sh.Hkv;
     const int G = sh.Hq / sh.Hkv;
     if (rows <= 0) return cudaSuccess;
+    if (attn_stream_supported(sh) && kv_on_device(K, V))
+        return launch_attn_stream(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials, dev_status,
+                                  st);
     if (attn_mma_supported(sh))
         return launch_attn_mma(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials, dev_status, st);
     const int64_t nsplit = attn_splits(sel_stride);

@@ -37,6 +37,16 @@ cudaError_t launch_attn(const tb_shape &sh, const uint16_t *q, const uint16_t *K
                         const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale, uint16_t *out,
                         uint32_t *attn_ctl, float *partials, int32_t *dev_status, cudaStream_t st);
 
+// The same with up to three rounds of bulk copies in flight per CTA and two
+// CTAs per SM (attn_stream.cu; D = 64 or 128, G <= 16, K/V in device memory).
+bool attn_stream_supported(const tb_shape &sh);
+cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                               const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
+                               uint16_t *out, uint32_t *attn_ctl, float *partials, int32_t *dev_status,
+                               cudaStream_t st);
+// True when K and V are device memory (answer kept per thread for the last pair asked).
+bool kv_on_device(const void *K, const void *V);
+
 // The same on the tensor cores (D = 64 or 128, G <= 16).
 bool attn_mma_supported(const tb_shape &sh);
 cudaError_t launch_attn_mma(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,

@@ -59,7 +59,7 @@ static WsLayout layout_for(const tb_shape &s, int64_t n_scores, int64_t sel_stri
 // True when K and V are device memory (the bulk copies of the three-kernel
 // step read them; pinned host K/V take the other paths). The answer for the
 // last pair asked is kept per thread.
-static bool kv_on_device(const void *K, const void *V) {
+bool kv_on_device(const void *K, const void *V) {
     static thread_local const void *last_k = nullptr, *last_v = nullptr;
     static thread_local bool last = false;
     if (K == last_k && V == last_v) return last;

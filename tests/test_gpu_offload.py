@@ -1,5 +1,7 @@
 """K/V in pinned host memory (the offloaded cache of the TokenButler abstract and the gist.science summary,
-"Significance"): the same calls, the same arithmetic, only the selected rows cross the host link."""
+"Significance"): the same calls and results, only the selected rows cross the host link. (Device-resident K/V
+take the attention kernel that gathers with bulk copies; host-resident K/V the one that gathers with 16-byte
+copies, so the two agree to the fp32 summation order, not bit for bit, where D allows the former.)"""
 import numpy as np
 import pytest
 import torch
@@ -22,8 +24,9 @@ def _lib():
 
 
 @pytest.mark.parametrize("D", [128, 32])
-def test_attention_over_host_kv_equals_device_kv_bitwise(D):
-    # tensor-core kernel (D = 128) and CUDA-core kernel (D = 32): same kernel, same data, same bits
+def test_attention_over_host_kv_equals_device_kv(D):
+    # D = 128: the streaming kernel (device K/V) and the tensor-core kernel with 16-byte copies (host K/V);
+    # D = 32: the CUDA-core kernel for both, so the same bits
     w = synth.small(B=2, Hq=8, Hkv=2, D=D, dp=16, N=3000, k=300, seed=41)
     shape = tb.Shape(w.B, w.Hq, w.Hkv, w.D, w.dp, w.N)
     L = synth.make_layer(w, cap=w.N, n=w.N)
@@ -42,7 +45,10 @@ def test_attention_over_host_kv_equals_device_kv_bitwise(D):
         torch.cuda.synchronize()
         tb.check_dev_status(st)
         outs.append(u16(out))
-    assert np.array_equal(outs[0], outs[1])
+    if D == 32:
+        assert np.array_equal(outs[0], outs[1])
+    else:
+        assert np.abs(oracle.bf16_bits_to_f64(outs[0]) - oracle.bf16_bits_to_f64(outs[1])).max() <= 2e-3
     ref = oracle.attn(d["q"], u16(L["K"]), u16(L["V"]), sel.cpu().numpy(),
                       np.full((w.B, w.Hkv), w.k, dtype=np.int32), w.scale)
     assert np.abs(oracle.bf16_bits_to_f64(outs[1]) - ref).max() <= OUT_ATOL
