@@ -65,6 +65,8 @@ def _args():
     ap.add_argument("--layers", type=int, default=0,
                     help="L: one decode step of L consumer layers of the workload's shape (the selection of later "
                          "layers overlapping the attention of earlier ones); prints its own line, per-layer figures")
+    ap.add_argument("--stack-layers", type=int, default=0,
+                    help="run the stack workload with this many layers instead of all of them")
     ap.add_argument("--budget", type=float, default=0.0,
                     help="budget as a fraction of N (k = ceil(frac N)) instead of the workload's k")
     ap.add_argument("--pipeline", action="store_true",
@@ -1112,7 +1114,7 @@ def run_stack(args, w):
     if not args.no_cpu_baseline:
         cpu = _stack_cpu_baseline(w)
     line = {
-        "metric": "decode steps/s of the 32-layer stack (B=8, N=16K, k=1024, prediction every T=16 steps, r=1)",
+        "metric": f"decode steps/s of the {Lc}-layer stack (B=8, N=16K, k=1024, prediction every T=16 steps, r=1)",
         "value": 1.0 / per_step, "unit": "decode steps/s", "n_gpus": 1, "steps": steps * reps,
         "warmup": 2 * steps, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device-generated, seeded)",
@@ -1169,6 +1171,9 @@ def main():
     if args.budget > 0:
         import dataclasses
         w = dataclasses.replace(w, k=int(math.ceil(args.budget * w.N - 1e-9)))
+    if args.stack_layers > 0:
+        import dataclasses
+        w = dataclasses.replace(w, layers=args.stack_layers)
     if args.impl == "reference":
         run_reference(args, w)
     elif args.layers:

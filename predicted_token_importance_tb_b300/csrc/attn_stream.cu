@@ -3,27 +3,30 @@
 // selected tokens' K/V rows are read; gist.science summary, Optimizations:
 // between predictions the same selection, plus the newest tokens, is reused).
 //
-// Grid (chunks, rows), two CTAs per SM: a CTA takes a contiguous slice of its
-// row's selection and walks it in rounds of kAsRound entries. Every thread
-// of the round issues the bulk copies of one entry's K and V rows into the
-// round's buffer, and up to kAsBufs rounds are in flight while the oldest is
-// attended on the tensor cores (attn_mma.cuh). The CTA's softmax state goes
-// to the workspace and the row's last CTA merges them. Entries outside
-// [0, cap) are reported and masked (their slots read row 0 of the head).
+// Grid (chunks, rows), two CTAs of four warps per SM: a CTA takes a
+// contiguous slice of its row's selection, cut into chunks of 16 entries that
+// its warps take in turn. Each warp streams its own chunks: its lanes issue
+// the bulk copies of the chunk's K and V rows (one row per lane) onto the
+// warp's own barrier, up to three chunks are in flight, and the oldest is
+// attended on the tensor cores (attn_mma.cuh) by that warp alone, so the
+// steady state has no CTA-wide barrier. The warps' softmax states are
+// combined into the CTA's partial and the row's last CTA merges them. Entries
+// outside [0, cap) are reported and masked (their slots read row 0 of the
+// head).
 #include "attn_mma.cuh"
 #include "kernels.cuh"
 
 namespace tb {
 
-constexpr int kAsThreads = 256;
+constexpr int kAsThreads = 128;
 constexpr int kAsWarps = kAsThreads / 32;
-constexpr int kAsRound = 64;   // entries per round
-constexpr int kAsBufs = 3;     // rounds in flight
+constexpr int kAsChunk = 16;   // entries per warp chunk (one tensor-core tile of slots)
+constexpr int kAsSets = 3;     // chunks in flight per warp
 
 __host__ __device__ constexpr int attn_stream_smem_bytes(int DT) {
-    return kAsBufs * kAsRound * (4 * DT + 16)   // round buffers
-           + 16 * (2 * DT + 16)                 // query tile
-           + kAsBufs * kAsRound;                // per-slot flags (valid entry)
+    return kAsSets * kAsWarps * kAsChunk * (4 * DT + 16)   // chunk buffers: set s holds warp w's chunk at w
+           + 16 * (2 * DT + 16)                            // query tile
+           + kAsSets * kAsWarps * kAsChunk;                // per-slot flags (valid entry)
 }
 
 template <int DT>
@@ -33,12 +36,13 @@ __global__ void __launch_bounds__(kAsThreads, 2) attn_stream_kernel(
     int Hkv, float scale, uint16_t *__restrict__ out, uint32_t *__restrict__ attn_ctl, float *__restrict__ part,
     int per_cta, int32_t *dev_status) {
     extern __shared__ __align__(128) uint8_t smb[];
-    __shared__ __align__(8) uint64_t bars[kAsBufs];
-    __shared__ int s_abort, s_cnt[kAsBufs];
+    __shared__ __align__(8) uint64_t bars[kAsSets][kAsWarps];
+    __shared__ int s_abort;
     __shared__ uint32_t s_last;
     constexpr int SB = 4 * DT + 16, CPR = DT / 8, NT = DT / 8, QS = 2 * DT + 16;
+    constexpr int SET = kAsWarps * kAsChunk;   // slots per set
     uint8_t *X = smb;
-    uint8_t *qsm = X + kAsBufs * kAsRound * SB;
+    uint8_t *qsm = X + kAsSets * SET * SB;
     uint8_t *flag = qsm + 16 * QS;
     const int G = Hq / Hkv;
     const int row = blockIdx.y, chunk = blockIdx.x, nchunk = gridDim.x;
@@ -53,53 +57,53 @@ __global__ void __launch_bounds__(kAsThreads, 2) attn_stream_kernel(
     if (tid == 0 && chunk == 0 && (cnt <= 0 || cnt > sel_stride)) set_status(dev_status, TB_ERR_INVALID_ARG);
     const int j0 = chunk * per_cta;
     const int j1 = j0 + per_cta < cnt_c ? j0 + per_cta : cnt_c;
+    const int nch = j1 > j0 ? (j1 - j0 + kAsChunk - 1) / kAsChunk : 0;   // chunks of the CTA's slice
 
     if (tid == 0) {
         s_abort = 0;
-        for (int i = 0; i < kAsBufs; ++i) mbarrier_init(&bars[i], 1);
+        for (int i = 0; i < kAsSets; ++i)
+            for (int w = 0; w < kAsWarps; ++w) mbarrier_init(&bars[i][w], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // query tile: the G heads as rows of a 16-row bf16 tile (zero-padded); round buffers start zeroed, so a
+    // query tile: the G heads as rows of a 16-row bf16 tile (zero-padded); chunk buffers start zeroed, so a
     // padding slot always holds finite values (zeros or an earlier valid row)
-    {
-        const int gq = tid / CPR, cq = tid % CPR;
-        if (tid < 16 * CPR) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (gq < G) v = *reinterpret_cast<const uint4 *>(q + ((int64_t)b * Hq + (int64_t)h * G + gq) * DT + cq * 8);
-            *reinterpret_cast<uint4 *>(qsm + gq * QS + cq * 16) = v;
-        }
-        for (int x = tid; x < kAsBufs * kAsRound * SB / 16; x += kAsThreads)
-            reinterpret_cast<uint4 *>(X)[x] = make_uint4(0u, 0u, 0u, 0u);
+    for (int x = tid; x < 16 * CPR; x += kAsThreads) {
+        const int gq = x / CPR, cq = x % CPR;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (gq < G) v = *reinterpret_cast<const uint4 *>(q + ((int64_t)b * Hq + (int64_t)h * G + gq) * DT + cq * 8);
+        *reinterpret_cast<uint4 *>(qsm + gq * QS + cq * 16) = v;
     }
+    for (int x = tid; x < kAsSets * SET * SB / 16; x += kAsThreads)
+        reinterpret_cast<uint4 *>(X)[x] = make_uint4(0u, 0u, 0u, 0u);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
 
-    uint32_t phase[kAsBufs] = {};
-    int r_issue = 0, r_done = 0, jn = j0;
-    // the next round: entry jn + tid of the slice -> slot tid of buffer r_issue % kAsBufs
+    // every warp streams its own chunks (w, w + kAsWarps, ...) through its own slots of the kAsSets sets,
+    // waiting only on its own barriers: lane l copies the K (even l) or V (odd l) row of entry l / 2
+    uint32_t phase[kAsSets] = {};
+    int c_issue = 0, c_done = 0;   // this warp's chunks issued / consumed
+    const int my_chunks = nch > warp ? (nch - warp + kAsWarps - 1) / kAsWarps : 0;
     auto issue = [&]() {
-        const int buf = r_issue % kAsBufs;
-        const int c = j1 - jn < kAsRound ? j1 - jn : kAsRound;
-        if (tid == 0) {
-            s_cnt[buf] = c;
-            mbarrier_arrive_expect_tx(&bars[buf], (uint32_t)(c * 4 * DT));
-        }
-        if (tid < c) {
-            int64_t t = __ldg(srow + jn + tid);
+        const int set = c_issue % kAsSets;
+        const int e0 = j0 + (warp + c_issue * kAsWarps) * kAsChunk;
+        const int c = j1 - e0 < kAsChunk ? j1 - e0 : kAsChunk;
+        const int slot0 = set * SET + warp * kAsChunk;
+        if (lane == 0) mbarrier_arrive_expect_tx(&bars[set][warp], (uint32_t)(c * 4 * DT));
+        const int ent = lane >> 1;
+        if (ent < c) {
+            int64_t t = __ldg(srow + e0 + ent);
             const bool valid = t >= 0 && t < cap;
-            if (!valid) {
-                set_status(dev_status, TB_ERR_INVALID_ARG);
-                t = 0;
+            if (!valid) t = 0;
+            if ((lane & 1) == 0) {
+                if (!valid) set_status(dev_status, TB_ERR_INVALID_ARG);
+                flag[slot0 + ent] = valid ? 1 : 0;
             }
-            flag[buf * kAsRound + tid] = valid ? 1 : 0;
-            uint8_t *dst = X + ((size_t)buf * kAsRound + tid) * SB;
-            bulk_g2s(dst, Kh + t * DT, 2 * DT, &bars[buf]);
-            bulk_g2s(dst + 2 * DT, Vh + t * DT, 2 * DT, &bars[buf]);
-        } else if (tid < kAsRound) {
-            flag[buf * kAsRound + tid] = 0;
+            uint8_t *dst = X + (size_t)(slot0 + ent) * SB + ((lane & 1) ? 2 * DT : 0);
+            bulk_g2s(dst, ((lane & 1) ? Vh : Kh) + t * DT, 2 * DT, &bars[set][warp]);
+        } else if ((lane & 1) == 0 && ent < kAsChunk) {
+            flag[slot0 + ent] = 0;
         }
-        jn += c;
-        ++r_issue;
+        ++c_issue;
     };
 
     MmaAttn<NT> A;
@@ -108,27 +112,33 @@ __global__ void __launch_bounds__(kAsThreads, 2) attn_stream_kernel(
 #pragma unroll
     for (int t = 0; t < NT; ++t) A.o[t][0] = A.o[t][1] = A.o[t][2] = A.o[t][3] = 0.f;
     const float qscale = scale * kLog2e;
-    while (r_issue - r_done < kAsBufs && jn < j1) issue();
-    while (r_done < r_issue) {
-        const int buf = r_done % kAsBufs;
-        if (!mbarrier_wait_bounded(&bars[buf], phase[buf], kWaitLimitNs)) {
-            s_abort = 1;
+    bool ok = true;
+    while (c_issue < my_chunks && c_issue - c_done < kAsSets) issue();
+    while (c_done < c_issue) {
+        const int set = c_done % kAsSets;
+        if (!mbarrier_wait_bounded(&bars[set][warp], phase[set], kWaitLimitNs)) {
+            ok = false;
             set_status(dev_status, TB_ERR_TIMEOUT);
+            break;
         }
-        __syncthreads();   // (the flags written by the issuing threads are visible too)
-        if (s_abort) break;
-        phase[buf] ^= 1u;
-        mma_attend<DT, kAsWarps, true>(A, X + (size_t)buf * kAsRound * SB, SB, s_cnt[buf], flag, buf * kAsRound,
-                                       qsm, qscale);
-        __syncthreads();   // the buffer is free again
-        ++r_done;
-        if (jn < j1) issue();
+        __syncwarp();
+        phase[set] ^= 1u;
+        const int e0 = j0 + (warp + c_done * kAsWarps) * kAsChunk;
+        const int c = j1 - e0 < kAsChunk ? j1 - e0 : kAsChunk;
+        // the set's tile of warp w is chunk w of the set: this warp attends it alone
+        mma_attend<DT, kAsWarps, true>(A, X + (size_t)set * SET * SB, SB, warp * kAsChunk + c, flag, set * SET, qsm,
+                                       qscale);
+        __syncwarp();   // the chunk's slots are free again
+        ++c_done;
+        if (c_issue < my_chunks) issue();
     }
-    if (s_abort) {
-        for (int r = r_done; r < r_issue; ++r)
-            mbarrier_wait_bounded(&bars[r % kAsBufs], phase[r % kAsBufs], kWaitLimitNs);
-        return;
+    if (!ok) {
+        s_abort = 1;
+        for (int r = c_done; r < c_issue; ++r)
+            mbarrier_wait_bounded(&bars[r % kAsSets][warp], phase[r % kAsSets], kWaitLimitNs);
     }
+    __syncthreads();
+    if (s_abort) return;
 
     // the warps' states -> this chunk's partial (m, l, acc[D]) per head
     A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 1);
@@ -208,7 +218,7 @@ cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint
     const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
     int64_t C = (2 * (int64_t)sms) / rows;
     const int64_t cmax = attn_splits(sel_stride);
-    const int64_t cround = (sel_stride + kAsRound - 1) / kAsRound;
+    const int64_t cround = (sel_stride + kAsChunk * kAsWarps - 1) / (kAsChunk * kAsWarps);
     if (C > cmax) C = cmax;
     if (C > cround) C = cround;
     if (C < 1) C = 1;

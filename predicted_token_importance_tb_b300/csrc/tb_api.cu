@@ -1,11 +1,19 @@
-// C ABI of libtb: argument checks, workspace carving and launches.
+// C ABI of libtb: argument checks, workspace carving and launches. Every
+// entry point opens an NVTX range of its own name (header-only NVTX 3: it
+// costs a pointer test unless a profiling tool is attached).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "kernels.cuh"
 #include "tb_internal.cuh"
 #include "ws_layout.cuh"
 
 namespace tb {
+
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 const DevInfo &dev_info() {
     static thread_local DevInfo info;
@@ -131,6 +139,7 @@ tb_status tb_workspace_size(const tb_shape *shape, int64_t n_max, int32_t k_max,
 }
 
 tb_status tb_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_workspace_init");
     if (!ws || ws_bytes == 0) return TB_ERR_INVALID_ARG;
     return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, stream));
 }
@@ -138,6 +147,7 @@ tb_status tb_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
 tb_status tb_project_append(const tb_shape *shape, const tb_bf16 *K_src, int64_t src_stride, const tb_bf16 *Wk,
                             tb_bf16 *Kp, int64_t pos0, int64_t n_new, void *ws, size_t ws_bytes,
                             int32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_project_append");
     (void)ws;
     (void)ws_bytes;
     TB_CHECK(check_shape(shape));
@@ -153,6 +163,7 @@ tb_status tb_project_append(const tb_shape *shape, const tb_bf16 *K_src, int64_t
 
 tb_status tb_score(const tb_shape *shape, const tb_bf16 *q_imp, const tb_bf16 *Kp, int64_t n, int32_t agg,
                    float *s, int32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_score");
     (void)dev_status;
     TB_CHECK(check_shape(shape));
     if (n < 0 || n > shape->cap) return TB_ERR_INVALID_ARG;
@@ -166,6 +177,7 @@ tb_status tb_score(const tb_shape *shape, const tb_bf16 *q_imp, const tb_bf16 *K
 
 tb_status tb_topk(const tb_shape *shape, const float *s, int64_t n, int32_t k, int32_t *idx, void *ws,
                   size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_topk");
     TB_CHECK(check_shape(shape));
     if (n < 0 || k < 0 || k > n) return TB_ERR_INVALID_ARG;
     if (k == 0) return TB_OK;
@@ -179,6 +191,7 @@ tb_status tb_topk(const tb_shape *shape, const float *s, int64_t n, int32_t k, i
 
 tb_status tb_expand(const tb_shape *shape, const int32_t *idx, int32_t k, int32_t r, int64_t n_pred, int64_t n_t,
                     int32_t *sel, int32_t sel_stride, int32_t *counts, int32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_expand");
     TB_CHECK(check_shape(shape));
     if (k < 0 || r < 0 || n_pred < 0 || n_t < n_pred || sel_stride <= 0 || n_t > shape->cap) return TB_ERR_INVALID_ARG;
     if ((k > 0 && !idx) || !sel || !counts) return TB_ERR_INVALID_ARG;
@@ -190,6 +203,7 @@ tb_status tb_sparse_decode_attn(const tb_shape *shape, const tb_bf16 *q, const t
                                 const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
                                 tb_bf16 *out, void *ws, size_t ws_bytes, int32_t *dev_status,
                                 cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_sparse_decode_attn");
     TB_CHECK(check_shape(shape));
     if (sel_stride <= 0 || !sel) return TB_ERR_INVALID_ARG;
     TB_PTR(q);
@@ -209,6 +223,7 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
                          tb_bf16 *K, tb_bf16 *V, tb_bf16 *Kp, int32_t *idx_state, int64_t *n_pred, int32_t *sel,
                          int32_t sel_stride, int32_t *counts, tb_bf16 *out, void *ws, size_t ws_bytes,
                          int32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_decode_step");
     TB_CHECK(check_shape(shape));
     if (!p || !n_pred || !idx_state || !sel || !counts) return TB_ERR_INVALID_ARG;
     if (p->T < 1 || p->r < 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
@@ -319,6 +334,7 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
 tb_status tb_decode_layers(const tb_shape *shape, const tb_step_params *p, int64_t n, int32_t L,
                            const tb_layer_buffers *layers, int32_t sel_stride, int32_t *dev_status, cudaStream_t stream,
                            cudaStream_t select_stream) {
+    NvtxRange nvtx_range("tb_decode_layers");
     TB_CHECK(check_shape(shape));
     if (!p || !layers || L < 1) return TB_ERR_INVALID_ARG;
     if (p->T != 1 || p->r != 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
@@ -381,6 +397,7 @@ tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_params *p, 
                                 const tb_bf16 *V_new, const tb_bf16 *Wk, tb_bf16 *K, tb_bf16 *V, tb_bf16 *Kp,
                                 int32_t *idx_state, int64_t *n_pred, int32_t *sel, int32_t sel_stride, int32_t *counts,
                                 tb_bf16 *out, void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_decode_step_ragged");
     TB_CHECK(check_shape(shape));
     if (!p || !n_host || !n_dev || !n_pred || !idx_state || !sel || !counts) return TB_ERR_INVALID_ARG;
     if (p->T < 1 || p->r < 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
@@ -450,6 +467,7 @@ tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_params *p, 
 tb_status tb_predict_queries(const tb_bf16 *x, const tb_bf16 *W1, const tb_bf16 *W2, int32_t B, int32_t E,
                              int32_t F, int32_t O, tb_bf16 *q_imp, void *ws, size_t ws_bytes, int32_t *dev_status,
                              cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_predict_queries");
     (void)dev_status;   // nothing on this path is detected on the device
     if (B < 1 || E < 1 || F < 1 || O < 1) return TB_ERR_INVALID_ARG;
     if (B > 16 || E % 8 != 0 || F % 8 != 0) return TB_ERR_UNSUPPORTED;
@@ -469,6 +487,7 @@ tb_status tb_decode_step_buffered(const tb_shape *shape, const tb_step_params *p
                                   tb_bf16 *V, tb_bf16 *Kp, int32_t *idx_state, int64_t *n_pred, int64_t *proj_end,
                                   int32_t *sel, int32_t sel_stride, int32_t *counts, tb_bf16 *out, void *ws,
                                   size_t ws_bytes, int32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("tb_decode_step_buffered");
     TB_CHECK(check_shape(shape));
     if (!p || !bp || !n_pred || !proj_end || !idx_state || !sel || !counts) return TB_ERR_INVALID_ARG;
     if (p->T < 1 || p->r < 0 || p->k < 1 || (p->agg != TB_AGG_MEAN && p->agg != TB_AGG_MAX)) return TB_ERR_INVALID_ARG;
