@@ -6,7 +6,7 @@
 namespace tb {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkLMax = 8192;    // keys per CTA held in shared memory
+constexpr int kTopkLMax = 16384;   // keys per CTA held in shared memory
 
 __host__ __device__ inline size_t topk_smem_bytes(int L) {
     return (size_t)L * 4 + (size_t)kRadixBins * 4 + (size_t)kCandCap * 8 + (size_t)kMaxChunks * 4 + 33 * 4 +
@@ -91,14 +91,20 @@ static TopkPlan plan_topk(int rows, int64_t n) {
     if (C < minC) C = minC;
     if (C < 1) C = 1;
     if (C > kMaxChunks) C = kMaxChunks;
-    int64_t L = (n + C - 1) / C;
-    L = (L + 31) / 32 * 32;
-    C = (n + L - 1) / L;
-    P.L = (int)L;
-    P.C = (int)C;
-    P.smem = topk_smem_bytes(P.L);
-    const int cap = topk_capacity(P.smem);
-    P.rows_per_launch = cap >= P.C ? cap / P.C : 0;
+    // fewer, longer chunks while that lets every row into one cooperative launch (a second launch costs a
+    // whole extra pass over the scores)
+    for (;;) {
+        int64_t L = (n + C - 1) / C;
+        L = (L + 31) / 32 * 32;
+        const int64_t Cq = (n + L - 1) / L;
+        P.L = (int)L;
+        P.C = (int)Cq;
+        P.smem = topk_smem_bytes(P.L);
+        const int cap = topk_capacity(P.smem);
+        P.rows_per_launch = cap >= P.C ? cap / P.C : 0;
+        if (P.rows_per_launch >= rows || Cq <= minC || C <= 1) break;
+        C = Cq - 1;
+    }
     if (P.rows_per_launch > rows) P.rows_per_launch = rows;
     return P;
 }
