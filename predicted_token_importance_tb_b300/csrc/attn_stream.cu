@@ -5,14 +5,15 @@
 //
 // Grid (chunks, rows), two CTAs of four warps per SM: a CTA takes a
 // contiguous slice of its row's selection, cut into chunks of 16 entries that
-// its warps take in turn. Each warp streams its own chunks: its lanes issue
-// the bulk copies of the chunk's K and V rows (one row per lane) onto the
-// warp's own barrier, up to three chunks are in flight, and the oldest is
-// attended on the tensor cores (attn_mma.cuh) by that warp alone, so the
-// steady state has no CTA-wide barrier. The warps' softmax states are
-// combined into the CTA's partial and the row's last CTA merges them. Entries
-// outside [0, cap) are reported and masked (their slots read row 0 of the
-// head).
+// its warps take in turn. Each warp streams its own chunks: its lanes copy the
+// chunk's K and V rows in 16-byte pieces (cp.async, one commit group per
+// chunk), up to three chunks are in flight, and the oldest is attended on the
+// tensor cores (attn_mma.cuh) by that warp alone, so the steady state has no
+// CTA-wide barrier. (One bulk copy per 256-byte row was tried first: the
+// per-copy cost of the bulk-copy unit held each SM to about 20 GB/s.) The
+// warps' softmax states are combined into the CTA's partial and the row's
+// last CTA merges them. Entries outside [0, cap) are reported and masked
+// (their slots read row 0 of the head).
 #include "attn_mma.cuh"
 #include "kernels.cuh"
 
@@ -21,133 +22,328 @@ namespace tb {
 constexpr int kAsThreads = 128;
 constexpr int kAsWarps = kAsThreads / 32;
 constexpr int kAsChunk = 16;   // entries per warp chunk (one tensor-core tile of slots)
-constexpr int kAsSets = 3;     // chunks in flight per warp
+// keys-as-rows form: chunks in flight per warp and CTAs per SM
+constexpr int kAsKtSets = 3;
+constexpr int kAsKtCtas = 2;
 
-__host__ __device__ constexpr int attn_stream_smem_bytes(int DT) {
-    return kAsSets * kAsWarps * kAsChunk * (4 * DT + 16)   // chunk buffers: set s holds warp w's chunk at w
-           + 16 * (2 * DT + 16)                            // query tile
-           + kAsSets * kAsWarps * kAsChunk;                // per-slot flags (valid entry)
+// SETS: chunks in flight per warp.
+__host__ __device__ constexpr int attn_stream_smem_bytes(int DT, int SETS) {
+    return SETS * kAsWarps * kAsChunk * (4 * DT + 16)   // chunk buffers: set s holds warp w's chunk at w
+           + 16 * (2 * DT + 16)                         // query tile
+           + SETS * kAsWarps * kAsChunk;                // per-slot flags (valid entry)
 }
 
+// 16-byte asynchronous copy global -> shared, destination given as a shared-window address.
+__device__ __forceinline__ void cp_async16_sa(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Transpose of an 8x8 b16 matrix held in the mma fragment layout (row lane/4, columns 2(lane%4) and +1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+// Attention state of one warp with the keys as the MMA rows: S^T = K Q^T (16 keys x 8 heads per chunk) and
+// O^T += V^T P^T (DT/16 tiles of 16 dims x 8 heads). Lane l holds heads 2(l%4) and 2(l%4)+1 (at most 8
+// heads, zero-padded), the running maxima of those heads (exp2 domain, equal across the lanes that share
+// l%4) and partial sums over its own keys (summed across lanes at the end).
 template <int DT>
-__global__ void __launch_bounds__(kAsThreads, 2) attn_stream_kernel(
+struct KtAttn {
+    float m0, m1, l0, l1;
+    float o[DT / 16][4];
+    uint32_t qb[DT / 16][2];   // Q^T as the B operand, one pair per 16-dim step
+};
+
+// One chunk of 16 staged slots (K row at xs + s*SB, V row at +2*DT) on the tensor cores; slots whose flag
+// is zero are masked (their V rows must hold finite values).
+template <int DT>
+__device__ __forceinline__ void kt_attend(KtAttn<DT> &A, uint32_t xs, int SB, const uint8_t *flag, float qscale) {
+    constexpr int KS = DT / 16;
+    const int lane = threadIdx.x & 31;
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, t[4] = {0.f, 0.f, 0.f, 0.f};   // even / odd k-steps
+    const uint32_t ka = xs + (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)) * SB + 16 * (lane >> 4);
+#pragma unroll
+    for (int kk = 0; kk < KS; kk += 2) {
+        uint32_t a0, a1, a2, a3, e0, e1, e2, e3;
+        ldsm_x4(ka + kk * 32, a0, a1, a2, a3);
+        ldsm_x4(ka + kk * 32 + 32, e0, e1, e2, e3);
+        mma_bf16_16816(s, a0, a1, a2, a3, A.qb[kk][0], A.qb[kk][1]);
+        mma_bf16_16816(t, e0, e1, e2, e3, A.qb[kk + 1][0], A.qb[kk + 1][1]);
+    }
+    // keys k = lane/4 and k + 8; heads h0 = 2(lane%4), h1 = h0 + 1
+    const int k0 = lane >> 2;
+    const bool f0 = flag[k0] != 0, f8 = flag[k0 + 8] != 0;
+    const float z00 = f0 ? (s[0] + t[0]) * qscale : -INFINITY, z01 = f0 ? (s[1] + t[1]) * qscale : -INFINITY;
+    const float z80 = f8 ? (s[2] + t[2]) * qscale : -INFINITY, z81 = f8 ? (s[3] + t[3]) * qscale : -INFINITY;
+    float mx0 = fmaxf(z00, z80), mx1 = fmaxf(z01, z81);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+    }
+    const float n0 = fmaxf(A.m0, mx0), n1 = fmaxf(A.m1, mx1);
+    const float c0 = n0 == -INFINITY ? 1.f : exp2f(A.m0 - n0);
+    const float c1 = n1 == -INFINITY ? 1.f : exp2f(A.m1 - n1);
+    const float p00 = n0 == -INFINITY ? 0.f : exp2f(z00 - n0), p80 = n0 == -INFINITY ? 0.f : exp2f(z80 - n0);
+    const float p01 = n1 == -INFINITY ? 0.f : exp2f(z01 - n1), p81 = n1 == -INFINITY ? 0.f : exp2f(z81 - n1);
+    A.l0 = A.l0 * c0 + (p00 + p80);
+    A.l1 = A.l1 * c1 + (p01 + p81);
+    A.m0 = n0;
+    A.m1 = n1;
+    if (__any_sync(0xFFFFFFFFu, c0 != 1.f || c1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            A.o[mt][0] *= c0;
+            A.o[mt][1] *= c1;
+            A.o[mt][2] *= c0;
+            A.o[mt][3] *= c1;
+        }
+    }
+    // P^T as the B operand: the transposes of the two 8x8 blocks (keys 0-7, 8-15) of P[key][head]
+    const uint32_t b0 = movmatrix_trans(pack_bf16x2(p00, p01));
+    const uint32_t b1 = movmatrix_trans(pack_bf16x2(p80, p81));
+    // V^T tiles from the V rows by transposed loads: lanes address keys (lane&7) + 8(lane>>4), dims +8((lane>>3)&1)
+    const uint32_t va = xs + (uint32_t)((lane & 7) + 8 * (lane >> 4)) * SB + 2 * DT + 16 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(va + mt * 32, a0, a1, a2, a3);
+        mma_bf16_16816(A.o[mt], a0, a1, a2, a3, b0, b1);
+    }
+}
+
+
+// Merge of nsplit partials (m, l, acc[DT] per head, fp32) into one row's G output heads (bf16). Every thread
+// takes up to four outputs and issues their values of eight partials at once, and the maxima and sums go to
+// shared memory while the first values are in flight, so a merge of up to eight partials is one round trip
+// to L2. sm holds 2 * nsplit * G floats.
+template <int DT>
+__device__ __forceinline__ void stream_merge(const float *__restrict__ part, int nsplit, int G,
+                                             uint16_t *__restrict__ out_rows, int32_t *dev_status, float *sm) {
+    constexpr int kU = 4, kB = 8;
+    const int sg = 2 + DT, tid = threadIdx.x, no = G * DT;
+    float *ms = sm, *ls = sm + nsplit * G;
+    for (int x0 = 0; x0 < no; x0 += kAsThreads * kU) {
+        float M[kU], L[kU], Acc[kU];
+        int g[kU], d[kU];
+        bool act[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int x = x0 + tid + u * kAsThreads;
+            act[u] = x < no;
+            g[u] = act[u] ? x / DT : 0;
+            d[u] = act[u] ? x % DT : 0;
+            M[u] = -INFINITY;
+            L[u] = Acc[u] = 0.f;
+        }
+        for (int s0 = 0; s0 < nsplit; s0 += kB) {
+            float av[kU][kB];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+#pragma unroll
+                for (int b = 0; b < kB; ++b)
+                    av[u][b] = (act[u] && s0 + b < nsplit)
+                                   ? __ldcg(part + ((int64_t)(s0 + b) * G + g[u]) * sg + 2 + d[u])
+                                   : 0.f;
+            if (x0 == 0 && s0 == 0) {   // the maxima and sums, while the first values are in flight
+                for (int i = tid; i < nsplit * G; i += kAsThreads) {
+                    ms[i] = __ldcg(part + (int64_t)i * sg);
+                    ls[i] = __ldcg(part + (int64_t)i * sg + 1);
+                }
+                __syncthreads();
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                float Mb = M[u];
+#pragma unroll
+                for (int b = 0; b < kB; ++b)
+                    if (s0 + b < nsplit) Mb = fmaxf(Mb, ms[(s0 + b) * G + g[u]]);
+                const float r = rescale_w(M[u], Mb);
+                L[u] *= r;
+                Acc[u] *= r;
+#pragma unroll
+                for (int b = 0; b < kB; ++b) {
+                    if (s0 + b < nsplit) {
+                        const float w = rescale_w(ms[(s0 + b) * G + g[u]], Mb);
+                        L[u] = fmaf(w, ls[(s0 + b) * G + g[u]], L[u]);
+                        Acc[u] = fmaf(w, av[u][b], Acc[u]);
+                    }
+                }
+                M[u] = Mb;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (act[u]) {
+                if (!(L[u] > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
+                out_rows[(int64_t)g[u] * DT + d[u]] = f_to_bf16(L[u] > 0.f ? Acc[u] / L[u] : 0.f);
+            }
+        }
+    }
+}
+
+// Grid (C, rows): CTA c of a row takes entries [c * per, (c + 1) * per) of the row's selection (clipped to its
+// count), cut into chunks of 16 that its warps take in turn. The warps' states are combined into the CTA's
+// partial (m, l, acc[D] per head) and the row's last arriving CTA merges the C partials. KT: keys as the MMA
+// rows (G <= 8); otherwise the G heads are the rows (G <= 16).
+template <int DT, bool KT, int SETS, int MINB>
+__global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ K, const uint16_t *__restrict__ V,
     const int32_t *__restrict__ sel, const int32_t *__restrict__ counts, int32_t sel_stride, int64_t cap, int Hq,
-    int Hkv, float scale, uint16_t *__restrict__ out, uint32_t *__restrict__ attn_ctl, float *__restrict__ part,
-    int per_cta, int32_t *dev_status) {
+    int Hkv, int per, float scale, uint16_t *__restrict__ out, uint32_t *__restrict__ attn_ctl,
+    float *__restrict__ part, int32_t *dev_status) {
     extern __shared__ __align__(128) uint8_t smb[];
-    __shared__ __align__(8) uint64_t bars[kAsSets][kAsWarps];
-    __shared__ int s_abort;
     __shared__ uint32_t s_last;
     constexpr int SB = 4 * DT + 16, CPR = DT / 8, NT = DT / 8, QS = 2 * DT + 16;
     constexpr int SET = kAsWarps * kAsChunk;   // slots per set
     uint8_t *X = smb;
-    uint8_t *qsm = X + kAsSets * SET * SB;
+    uint8_t *qsm = X + SETS * SET * SB;
     uint8_t *flag = qsm + 16 * QS;
     const int G = Hq / Hkv;
+    const int sg = 2 + DT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.y, chunk = blockIdx.x, nchunk = gridDim.x;
     const int b = row / Hkv, h = row % Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint16_t *Kh = K + (int64_t)row * cap * DT;
-    const uint16_t *Vh = V + (int64_t)row * cap * DT;
-    const int32_t *srow = sel + (int64_t)row * sel_stride;
 
     const int cnt = counts ? counts[row] : sel_stride;
     const int cnt_c = cnt < 0 ? 0 : (cnt > sel_stride ? sel_stride : cnt);
     if (tid == 0 && chunk == 0 && (cnt <= 0 || cnt > sel_stride)) set_status(dev_status, TB_ERR_INVALID_ARG);
-    const int j0 = chunk * per_cta;
-    const int j1 = j0 + per_cta < cnt_c ? j0 + per_cta : cnt_c;
+    const int j0 = chunk * per;
+    const int j1 = j0 + per < cnt_c ? j0 + per : cnt_c;
     const int nch = j1 > j0 ? (j1 - j0 + kAsChunk - 1) / kAsChunk : 0;   // chunks of the CTA's slice
 
-    if (tid == 0) {
-        s_abort = 0;
-        for (int i = 0; i < kAsSets; ++i)
-            for (int w = 0; w < kAsWarps; ++w) mbarrier_init(&bars[i][w], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    // query tile: the G heads as rows of a 16-row bf16 tile (zero-padded); chunk buffers start zeroed, so a
-    // padding slot always holds finite values (zeros or an earlier valid row)
+    constexpr int P = DT / 8;          // 16-byte pieces of a K or V row
+    constexpr int LPE = 2 * P;         // lanes per entry (its K and V pieces)
+    constexpr int EPI = 32 / LPE;      // entries per copy instruction of the warp
+    const int pr = lane % LPE;
+    const bool pv = pr >= P;
+    const uint32_t xs = smem_addr(X);
+    const uint32_t dst_lane = (uint32_t)((lane / LPE) * SB + (pv ? 2 * DT : 0) + (pv ? pr - P : pr) * 16);
+    const uint16_t *src = (pv ? V : K) + (int64_t)row * cap * DT + (pv ? pr - P : pr) * 8;
+    const int32_t *srow = sel + (int64_t)row * sel_stride;
+    const float qscale = scale * kLog2e;
+
+    // every warp streams its own chunks (w, w + kAsWarps, ...) through its own slots of the SETS sets: the
+    // lanes copy the chunk's K and V rows in 16-byte pieces (cp.async, one commit group per chunk) and wait for
+    // their own groups only. Lane l holds the selection entry l % 16 of the next two chunks to issue, loaded
+    // ahead so that their latency overlaps the copies and the attention before them.
+    int c_issue = 0, c_done = 0;   // this warp's chunks issued / consumed
+    const int my_chunks = nch > warp ? (nch - warp + kAsWarps - 1) / kAsWarps : 0;
+    auto load_idx = [&](int kk) -> int32_t {   // entry lane % 16 of this warp's chunk kk, -1 past the slice
+        const int e = j0 + (warp + kk * kAsWarps) * kAsChunk + (lane & (kAsChunk - 1));
+        return (kk < my_chunks && e < j1) ? __ldg(srow + e) : -1;
+    };
+    int32_t pidx = load_idx(0), pnext = load_idx(1);
+    auto issue = [&]() {
+        const int e0 = j0 + (warp + c_issue * kAsWarps) * kAsChunk;
+        const int cc = j1 - e0 < kAsChunk ? j1 - e0 : kAsChunk;
+        const int slot0 = (c_issue % SETS) * SET + warp * kAsChunk;
+        const bool valid_l = pidx >= 0 && (int64_t)pidx < cap;
+        if (lane < kAsChunk) {
+            if (lane < cc && !valid_l) set_status(dev_status, TB_ERR_INVALID_ARG);
+            flag[slot0 + lane] = (lane < cc && valid_l) ? 1 : 0;
+        }
+        const int32_t tl = valid_l ? pidx : 0;
+        const uint32_t dst0 = xs + (uint32_t)slot0 * SB + dst_lane;
+#pragma unroll
+        for (int it = 0; it < kAsChunk / EPI; ++it) {
+            const int ent = it * EPI + lane / LPE;
+            const int32_t t = __shfl_sync(0xFFFFFFFFu, tl, ent);
+            if (ent < cc)
+                cp_async16_sa(dst0 + (uint32_t)(it * EPI * SB), src + (int64_t)t * DT);
+            else if (pv)   // a padding slot's V row must hold finite values (its weight is zero)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst0 + (uint32_t)(it * EPI * SB)),
+                             "r"(0u)
+                             : "memory");
+        }
+        cp_async_commit();
+        ++c_issue;
+        pidx = pnext;
+        pnext = load_idx(c_issue + 1);
+    };
+
+    // the first chunks are in flight before the query tile is loaded
+    while (c_issue < my_chunks && c_issue - c_done < SETS) issue();
+    // query tile: the G heads as rows of a 16-row bf16 tile (zero-padded)
     for (int x = tid; x < 16 * CPR; x += kAsThreads) {
         const int gq = x / CPR, cq = x % CPR;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (gq < G) v = *reinterpret_cast<const uint4 *>(q + ((int64_t)b * Hq + (int64_t)h * G + gq) * DT + cq * 8);
         *reinterpret_cast<uint4 *>(qsm + gq * QS + cq * 16) = v;
     }
-    for (int x = tid; x < kAsSets * SET * SB / 16; x += kAsThreads)
-        reinterpret_cast<uint4 *>(X)[x] = make_uint4(0u, 0u, 0u, 0u);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
 
-    // every warp streams its own chunks (w, w + kAsWarps, ...) through its own slots of the kAsSets sets,
-    // waiting only on its own barriers: lane l copies the K (even l) or V (odd l) row of entry l / 2
-    uint32_t phase[kAsSets] = {};
-    int c_issue = 0, c_done = 0;   // this warp's chunks issued / consumed
-    const int my_chunks = nch > warp ? (nch - warp + kAsWarps - 1) / kAsWarps : 0;
-    auto issue = [&]() {
-        const int set = c_issue % kAsSets;
-        const int e0 = j0 + (warp + c_issue * kAsWarps) * kAsChunk;
-        const int c = j1 - e0 < kAsChunk ? j1 - e0 : kAsChunk;
-        const int slot0 = set * SET + warp * kAsChunk;
-        if (lane == 0) mbarrier_arrive_expect_tx(&bars[set][warp], (uint32_t)(c * 4 * DT));
-        const int ent = lane >> 1;
-        if (ent < c) {
-            int64_t t = __ldg(srow + e0 + ent);
-            const bool valid = t >= 0 && t < cap;
-            if (!valid) t = 0;
-            if ((lane & 1) == 0) {
-                if (!valid) set_status(dev_status, TB_ERR_INVALID_ARG);
-                flag[slot0 + ent] = valid ? 1 : 0;
-            }
-            uint8_t *dst = X + (size_t)(slot0 + ent) * SB + ((lane & 1) ? 2 * DT : 0);
-            bulk_g2s(dst, ((lane & 1) ? Vh : Kh) + t * DT, 2 * DT, &bars[set][warp]);
-        } else if ((lane & 1) == 0 && ent < kAsChunk) {
-            flag[slot0 + ent] = 0;
-        }
-        ++c_issue;
-    };
-
-    MmaAttn<NT> A;
-    A.m0 = A.m1 = -INFINITY;
-    A.l0 = A.l1 = 0.f;
+    MmaAttn<NT> A{};   // heads-as-rows state (KT = false)
+    KtAttn<DT> B{};    // keys-as-rows state (KT = true)
+    if constexpr (KT) {
+        B.m0 = B.m1 = -INFINITY;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) A.o[t][0] = A.o[t][1] = A.o[t][2] = A.o[t][3] = 0.f;
-    const float qscale = scale * kLog2e;
-    bool ok = true;
-    while (c_issue < my_chunks && c_issue - c_done < kAsSets) issue();
-    while (c_done < c_issue) {
-        const int set = c_done % kAsSets;
-        if (!mbarrier_wait_bounded(&bars[set][warp], phase[set], kWaitLimitNs)) {
-            ok = false;
-            set_status(dev_status, TB_ERR_TIMEOUT);
-            break;
+        for (int mt = 0; mt < DT / 16; ++mt) {
+            const uint8_t *qr = qsm + (lane >> 2) * QS + (mt * 16 + 2 * (lane & 3)) * 2;
+            B.qb[mt][0] = *reinterpret_cast<const uint32_t *>(qr);
+            B.qb[mt][1] = *reinterpret_cast<const uint32_t *>(qr + 16);
         }
-        __syncwarp();
-        phase[set] ^= 1u;
-        const int e0 = j0 + (warp + c_done * kAsWarps) * kAsChunk;
-        const int c = j1 - e0 < kAsChunk ? j1 - e0 : kAsChunk;
+    } else {
+        A.m0 = A.m1 = -INFINITY;
+    }
+    while (c_done < c_issue) {
+        const int set = c_done % SETS;
+        // this lane's pieces of chunk c_done have landed once at most c_issue - c_done - 1 groups are pending
+        const int pend = c_issue - c_done - 1;
+        if (pend >= 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+        else if (pend == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();   // every lane's pieces of the chunk are visible to the warp
         // the set's tile of warp w is chunk w of the set: this warp attends it alone
-        mma_attend<DT, kAsWarps, true>(A, X + (size_t)set * SET * SB, SB, warp * kAsChunk + c, flag, set * SET, qsm,
-                                       qscale);
+        if constexpr (KT) {
+            kt_attend<DT>(B, xs + (uint32_t)(set * SET + warp * kAsChunk) * SB, SB, flag + set * SET + warp * kAsChunk,
+                          qscale);
+        } else {
+            const int e0 = j0 + (warp + c_done * kAsWarps) * kAsChunk;
+            const int cc = j1 - e0 < kAsChunk ? j1 - e0 : kAsChunk;
+            mma_attend<DT, kAsWarps, true>(A, X + (size_t)set * SET * SB, SB, warp * kAsChunk + cc, flag, set * SET,
+                                           qsm, qscale);
+        }
         __syncwarp();   // the chunk's slots are free again
         ++c_done;
         if (c_issue < my_chunks) issue();
     }
-    if (!ok) {
-        s_abort = 1;
-        for (int r = c_done; r < c_issue; ++r)
-            mbarrier_wait_bounded(&bars[r % kAsSets][warp], phase[r % kAsSets], kWaitLimitNs);
-    }
-    __syncthreads();
-    if (s_abort) return;
+    __syncthreads();   // every warp is done with the chunk buffers
 
-    // the warps' states -> this chunk's partial (m, l, acc[D]) per head
-    A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 1);
-    A.l0 += __shfl_xor_sync(0xFFFFFFFFu, A.l0, 2);
-    A.l1 += __shfl_xor_sync(0xFFFFFFFFu, A.l1, 1);
-    A.l1 += __shfl_xor_sync(0xFFFFFFFFu, A.l1, 2);
+    // the warps' states -> shared memory -> this CTA's partial (m, l, acc[D]) per head
     float *ws = reinterpret_cast<float *>(X);
-    const int sg = 2 + DT;
-    {
+    if constexpr (KT) {
+        float l0 = B.l0, l1 = B.l1;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+            l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+        }
+        const int dr = lane >> 2;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int g = 2 * (lane & 3) + j;
+            if (g < G) {
+                float *w = ws + ((int64_t)warp * G + g) * sg;
+                if (lane < 4) {
+                    w[0] = j ? B.m1 : B.m0;
+                    w[1] = j ? l1 : l0;
+                }
+#pragma unroll
+                for (int mt = 0; mt < DT / 16; ++mt) {
+                    w[2 + mt * 16 + dr] = B.o[mt][j];
+                    w[2 + mt * 16 + dr + 8] = B.o[mt][2 + j];
+                }
+            }
+        }
+    } else {
+        float l0 = A.l0, l1 = A.l1;
+        l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+        l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
         const int g0 = lane >> 2, d0 = 2 * (lane & 3);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -156,7 +352,7 @@ __global__ void __launch_bounds__(kAsThreads, 2) attn_stream_kernel(
                 float *w = ws + ((int64_t)warp * G + g) * sg;
                 if ((lane & 3) == 0) {
                     w[0] = half ? A.m1 : A.m0;
-                    w[1] = half ? A.l1 : A.l0;
+                    w[1] = half ? l1 : l0;
                 }
 #pragma unroll
                 for (int t = 0; t < NT; ++t)
@@ -186,7 +382,7 @@ __global__ void __launch_bounds__(kAsThreads, 2) attn_stream_kernel(
         }
         o[2 + d] = Acc;
     }
-    // the last CTA of the row merges the chunks
+    // the last CTA of the row merges the row's partials
     __syncthreads();
     if (tid == 0) {
         __threadfence();
@@ -196,8 +392,8 @@ __global__ void __launch_bounds__(kAsThreads, 2) attn_stream_kernel(
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    attn_merge(prow, nchunk, G, DT, out + ((int64_t)b * Hq + (int64_t)h * G) * DT, dev_status,
-               reinterpret_cast<float *>(X));
+    stream_merge<DT>(prow, nchunk, G, out + ((int64_t)b * Hq + (int64_t)h * G) * DT, dev_status,
+                     reinterpret_cast<float *>(X));
     if (tid == 0) attn_ctl[row] = 0;   // ready for the next call
 }
 
@@ -206,43 +402,57 @@ bool attn_stream_supported(const tb_shape &sh) {
     return (sh.D == 64 || sh.D == 128) && G <= 16;
 }
 
+template <int DT, bool KT, int SETS, int MINB>
+static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                             const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
+                             uint16_t *out, uint32_t *attn_ctl, float *partials, int32_t *dev_status,
+                             cudaStream_t st, int slot) {
+    const int rows = sh.B * sh.Hkv;
+    // CTAs per row: about MINB CTAs per SM over all rows, each at least one round of its warps' chunks, no
+    // more than the workspace's partial slots per row, and few enough that the merge's scratch (2 floats per
+    // head and partial) fits the chunk buffers
+    const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
+    int64_t C = ((int64_t)MINB * sms) / rows;
+    const int64_t cmax = attn_splits(sel_stride);
+    const int64_t cround = (sel_stride + kAsChunk * kAsWarps - 1) / (kAsChunk * kAsWarps);
+    const int64_t cfit = (int64_t)SETS * kAsWarps * kAsChunk * (4 * DT + 16) / (8 * (sh.Hq / sh.Hkv));
+    if (C > cmax) C = cmax;
+    if (C > cround) C = cround;
+    if (C > cfit) C = cfit;
+    if (C < 1) C = 1;
+    const int per = (int)((sel_stride + C - 1) / C);
+    C = (sel_stride + per - 1) / per;
+    const size_t smem = (size_t)attn_stream_smem_bytes(DT, SETS);
+    static thread_local int attr_dev[4] = {-1, -1, -1, -1};
+    auto fn = attn_stream_kernel<DT, KT, SETS, MINB>;
+    if (attr_dev[slot] != dev_info().device) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev[slot] = dev_info().device;
+    }
+    fn<<<dim3((unsigned)C, (unsigned)rows), kAsThreads, smem, st>>>(q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq,
+                                                                    sh.Hkv, per, scale, out, attn_ctl, partials,
+                                                                    dev_status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
                                const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
                                uint16_t *out, uint32_t *attn_ctl, float *partials, int32_t *dev_status,
                                cudaStream_t st) {
     const int rows = sh.B * sh.Hkv;
-    if (rows <= 0) return cudaSuccess;
+    if (rows <= 0 || sel_stride <= 0) return cudaSuccess;
     if (!attn_stream_supported(sh)) return cudaErrorNotSupported;
-    // chunks: about two CTAs per SM over all rows, each at least one round, no more than the workspace's
-    // partial slots (attn_splits(sel_stride) per row)
-    const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
-    int64_t C = (2 * (int64_t)sms) / rows;
-    const int64_t cmax = attn_splits(sel_stride);
-    const int64_t cround = (sel_stride + kAsChunk * kAsWarps - 1) / (kAsChunk * kAsWarps);
-    if (C > cmax) C = cmax;
-    if (C > cround) C = cround;
-    if (C < 1) C = 1;
-    const int per = (int)((sel_stride + C - 1) / C);
-    C = (sel_stride + per - 1) / per;
-    dim3 grid((unsigned)C, (unsigned)rows);
-    const size_t smem = (size_t)attn_stream_smem_bytes(sh.D);
-    static thread_local int attr_dev[2] = {-1, -1};
-    const int slot = sh.D == 64 ? 0 : 1;
-    if (attr_dev[slot] != dev_info().device) {
-        cudaError_t e = sh.D == 64 ? cudaFuncSetAttribute(attn_stream_kernel<64>,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                                   : cudaFuncSetAttribute(attn_stream_kernel<128>,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev[slot] = dev_info().device;
-    }
+    const bool kt = sh.Hq / sh.Hkv <= 8;
     if (sh.D == 64)
-        attn_stream_kernel<64><<<grid, kAsThreads, smem, st>>>(q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq, sh.Hkv,
-                                                               scale, out, attn_ctl, partials, per, dev_status);
-    else
-        attn_stream_kernel<128><<<grid, kAsThreads, smem, st>>>(q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq,
-                                                                sh.Hkv, scale, out, attn_ctl, partials, per, dev_status);
-    return cudaGetLastError();
+        return kt ? launch_as<64, true, kAsKtSets, kAsKtCtas>(sh, q, K, V, sel, counts, sel_stride, scale, out,
+                                                             attn_ctl, partials, dev_status, st, 0)
+                  : launch_as<64, false, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl,
+                                               partials, dev_status, st, 1);
+    return kt ? launch_as<128, true, kAsKtSets, kAsKtCtas>(sh, q, K, V, sel, counts, sel_stride, scale, out,
+                                                          attn_ctl, partials, dev_status, st, 2)
+              : launch_as<128, false, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
+                                            dev_status, st, 3);
 }
 
 }  // namespace tb

@@ -89,9 +89,12 @@ inline int64_t attn_split_tokens(int64_t sel_stride) {
     return t < kAttnSplitTok ? kAttnSplitTok : t;
 }
 
+// Partial slots per row: ceil(sel_stride / kAttnSplitTok), at most kAttnMaxSplits. It never decreases with
+// sel_stride (a workspace sized for a larger stride holds every smaller call's partials) and covers the
+// splits of attn_split_tokens.
 inline int64_t attn_splits(int64_t sel_stride) {
-    const int64_t t = attn_split_tokens(sel_stride);
-    return (sel_stride + t - 1) / t;
+    const int64_t s = (sel_stride + kAttnSplitTok - 1) / kAttnSplitTok;
+    return s < kAttnMaxSplits ? s : kAttnMaxSplits;
 }
 
 inline WsLayout ws_layout(const tb_shape &s, int64_t n_max, int64_t sel_stride_max, int64_t fused_chunks_max) {

@@ -239,6 +239,19 @@ def test_attn_parity_workloads(wi, k):
     assert np.abs(got - ref).max() <= OUT_ATOL
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(16, 2, 128), (10, 2, 64), (32, 2, 64), (24, 2, 128), (3, 3, 128)])
+def test_attn_group_sizes(Hq, Hkv, D):
+    """Group sizes on both sides of the eight heads one tensor-core tile column holds, odd sizes included."""
+    w = synth.small(B=2, Hq=Hq, Hkv=Hkv, D=D, dp=16, N=3000, seed=Hq * 7 + D)
+    rng = np.random.default_rng(Hq)
+    stride = 1100
+    sel = np.stack([np.stack([np.sort(rng.choice(w.N, stride, replace=False)) for _ in range(w.Hkv)])
+                    for _ in range(w.B)]).astype(np.int32)
+    counts = rng.integers(1, stride + 1, size=(w.B, w.Hkv)).astype(np.int32)
+    got, ref, _, _ = _attn_case(w, sel, counts)
+    assert np.abs(got - ref).max() <= OUT_ATOL
+
+
 def test_attn_ragged_counts_and_single_row():
     w = synth.small(B=2, Hq=8, Hkv=2, D=128, dp=32, N=5000, seed=21)
     rng = np.random.default_rng(1)
