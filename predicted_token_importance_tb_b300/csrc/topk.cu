@@ -47,7 +47,23 @@ topk_kernel(const float *__restrict__ s, int64_t lds, int64_t n, uint32_t k, int
     if (threadIdx.x == 0) *S.abort_flag = 0;
     bool nan_seen = false;
     const float *srow = s + (int64_t)row * lds + t0;
-    for (int e = threadIdx.x; e < Lc; e += blockDim.x) S.keys[e] = score_key(__ldg(srow + e), nan_seen);
+    if ((reinterpret_cast<uintptr_t>(srow) & 15) == 0) {   // four scores per load, four loads in flight
+        const int L4 = Lc >> 2;
+        const float4 *s4 = reinterpret_cast<const float4 *>(srow);
+#pragma unroll 4
+        for (int e = threadIdx.x; e < L4; e += blockDim.x) {
+            const float4 v = __ldg(s4 + e);
+            uint4 kv;
+            kv.x = score_key(v.x, nan_seen);
+            kv.y = score_key(v.y, nan_seen);
+            kv.z = score_key(v.z, nan_seen);
+            kv.w = score_key(v.w, nan_seen);
+            reinterpret_cast<uint4 *>(S.keys)[e] = kv;
+        }
+        for (int e = 4 * L4 + threadIdx.x; e < Lc; e += blockDim.x) S.keys[e] = score_key(__ldg(srow + e), nan_seen);
+    } else {
+        for (int e = threadIdx.x; e < Lc; e += blockDim.x) S.keys[e] = score_key(__ldg(srow + e), nan_seen);
+    }
     if (nan_seen) set_status(dev_status, TB_ERR_NONFINITE);
     __syncthreads();
     RowCtl *rc = ctl + row;

@@ -167,21 +167,25 @@ __device__ __forceinline__ SelectBegin group_select_begin(RowCtl *ctl, SelectSme
     uint32_t my_above = 0, my_eq = 0;
     for (int e = threadIdx.x; e < Lc; e += blockDim.x) {
         uint32_t top = S.keys[e] >> shift;   // shift < 32 here
-        if (top > prefix) {
-            ++my_above;
-        } else if (top == prefix) {
-            ++my_eq;
-            if (mode_cand) {
-                uint32_t slot = atomicAdd(&ctl->ncand, 1u);
-                if (slot < (uint32_t)kCandCap) ctl->cand[slot] = make_uint2(S.keys[e], (uint32_t)(c * L + e));
-            }
-        }
+        if (top > prefix) ++my_above;
+        else if (top == prefix) ++my_eq;
     }
     uint32_t tot;
     (void)block_exclusive_scan(my_above, S.scan, tot);
     const uint32_t chunk_above = tot;
-    (void)block_exclusive_scan(my_eq, S.scan, tot);
+    const uint32_t eq_before = block_exclusive_scan(my_eq, S.scan, tot);
     const uint32_t chunk_eq = tot;
+    if (mode_cand) {   // the chunk's candidates, at slots reserved with one atomic per CTA
+        if (threadIdx.x == 0) S.misc[7] = atomicAdd(&ctl->ncand, chunk_eq);
+        __syncthreads();
+        uint32_t slot = S.misc[7] + eq_before;
+        for (int e = threadIdx.x; e < Lc; e += blockDim.x) {
+            if ((S.keys[e] >> shift) == prefix) {
+                if (slot < (uint32_t)kCandCap) ctl->cand[slot] = make_uint2(S.keys[e], (uint32_t)(c * L + e));
+                ++slot;
+            }
+        }
+    }
     if (threadIdx.x == 0) {
         ctl->above[c] = chunk_above;
         ctl->eq[c] = chunk_eq;
@@ -285,29 +289,55 @@ __device__ __forceinline__ bool is_kept(const SelectResult &R, uint32_t key, uin
 
 // Write the kept tokens of this chunk, ascending, to out[R.offset ...] (and
 // to out2 when given). The chunk's keys are in S.keys; token of element e is
-// tok0 + e.
+// tok0 + e. Warp w takes a contiguous run of the chunk in stripes of 32 and
+// counts its kept elements with ballots (in mode 1 the tied elements first,
+// since ties go to the lowest tokens); one block scan over the warps' counts
+// gives each warp its first output slot.
 __device__ __forceinline__ void write_kept(const SelectResult &R, SelectSmem &S, int Lc, uint32_t tok0,
                                           int32_t *out, int32_t *out2 = nullptr) {
-    uint32_t base_kept = 0, base_tied = 0;
-    for (int t0 = 0; t0 < Lc; t0 += blockDim.x) {
-        const int e = t0 + threadIdx.x;
-        uint32_t key = 0;
-        uint32_t tied = 0;
-        if (e < Lc) {
-            key = S.keys[e];
-            tied = (R.mode == 1 && key == R.tkey) ? 1u : 0u;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int per = ((Lc + nw - 1) / nw + 31) & ~31;
+    const int e0 = warp * per, e1 = e0 + per < Lc ? e0 + per : Lc;
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t tot;
+    uint32_t tied_base = 0;
+    if (R.mode == 1) {   // tied elements in the warps before this one
+        uint32_t nt = 0;
+        for (int b = e0; b < e1; b += 32) {
+            const int e = b + lane;
+            nt += __popc(__ballot_sync(0xFFFFFFFFu, e < e1 && S.keys[e] == R.tkey));
         }
-        uint32_t ttot;
-        const uint32_t tied_before = base_tied + block_exclusive_scan(tied, S.scan, ttot);
-        const uint32_t kept = (e < Lc && is_kept(R, key, tok0 + (uint32_t)e, tied_before)) ? 1u : 0u;
-        uint32_t ktot;
-        const uint32_t pos = block_exclusive_scan(kept, S.scan, ktot);
-        if (kept) {
-            out[R.offset + base_kept + pos] = (int32_t)(tok0 + (uint32_t)e);
-            if (out2) out2[R.offset + base_kept + pos] = (int32_t)(tok0 + (uint32_t)e);
+        tied_base = block_exclusive_scan(lane == 0 ? nt : 0u, S.scan, tot);
+        tied_base = __shfl_sync(0xFFFFFFFFu, tied_base, 0);
+    }
+    // kept(e): the element's ballot of the stripe, advancing the tie rank in mode 1
+    auto stripe = [&](int b, uint32_t &run) -> uint32_t {
+        const int e = b + lane;
+        const bool in = e < e1;
+        const uint32_t key = in ? S.keys[e] : 0u;
+        bool kp;
+        if (R.mode == 0) {
+            kp = in && composite(key, tok0 + (uint32_t)e) >= R.compT;
+        } else {
+            const uint32_t tb = __ballot_sync(0xFFFFFFFFu, in && key == R.tkey);
+            kp = in && (key > R.tkey || (key == R.tkey && run + __popc(tb & lt) < R.take));
+            run += __popc(tb);
         }
-        base_kept += ktot;
-        base_tied += ttot;
+        return __ballot_sync(0xFFFFFFFFu, kp);
+    };
+    uint32_t nk = 0, run = tied_base;
+    for (int b = e0; b < e1; b += 32) nk += __popc(stripe(b, run));
+    uint32_t pos = block_exclusive_scan(lane == 0 ? nk : 0u, S.scan, tot);
+    pos = R.offset + __shfl_sync(0xFFFFFFFFu, pos, 0);
+    run = tied_base;
+    for (int b = e0; b < e1; b += 32) {
+        const uint32_t kb = stripe(b, run);
+        if ((kb >> lane) & 1u) {
+            const uint32_t at = pos + __popc(kb & lt);
+            out[at] = (int32_t)(tok0 + (uint32_t)(b + lane));
+            if (out2) out2[at] = (int32_t)(tok0 + (uint32_t)(b + lane));
+        }
+        pos += __popc(kb);
     }
 }
 
