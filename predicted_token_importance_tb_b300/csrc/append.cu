@@ -18,6 +18,9 @@ append_kernel(const uint16_t *__restrict__ K_new, const uint16_t *__restrict__ V
               uint16_t *__restrict__ Kp, int64_t cap, int Hkv, int D, int dp, int64_t pos, int32_t *sel,
               int32_t sel_stride, int32_t *counts, int32_t *dev_status, const int64_t *__restrict__ pos_seq) {
     extern __shared__ float sh[];   // knew[D] then partial[kAppendThreads]
+    // a programmatic dependent (the streamed attention of a step inside an interval) may start now: it does
+    // not read what this kernel writes before it has waited for this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float *knew = sh;
     float *part = sh + D;
     const int row = blockIdx.x;

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ K, const uint16_t *__restrict__ V,
     const int32_t *__restrict__ sel, const int32_t *__restrict__ counts, int32_t sel_stride, int64_t cap, int Hq,
     int Hkv, int per, float scale, uint16_t *__restrict__ out, uint32_t *__restrict__ attn_ctl,
-    float *__restrict__ part, int32_t *dev_status) {
+    float *__restrict__ part, int32_t *dev_status, AttnAppend app) {
     extern __shared__ __align__(128) uint8_t smb[];
     __shared__ uint32_t s_last;
     constexpr int SB = 4 * DT + 16, CPR = DT / 8, NT = DT / 8, QS = 2 * DT + 16;
@@ -207,9 +207,14 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const int row = blockIdx.y, chunk = blockIdx.x, nchunk = gridDim.x;
     const int b = row / Hkv, h = row % Hkv;
 
-    const int cnt = counts ? counts[row] : sel_stride;
+    const int cnt0 = counts ? counts[row] : sel_stride;
+    // with an append, the new token is entry cnt0 (its K/V rows read from K_new / V_new) when there is room
+    const bool room = app.pos >= 0 && cnt0 >= 0 && cnt0 < sel_stride;
+    const int cnt = room ? cnt0 + 1 : cnt0;
+    const int new_e = room ? cnt0 : -1;
     const int cnt_c = cnt < 0 ? 0 : (cnt > sel_stride ? sel_stride : cnt);
-    if (tid == 0 && chunk == 0 && (cnt <= 0 || cnt > sel_stride)) set_status(dev_status, TB_ERR_INVALID_ARG);
+    if (tid == 0 && chunk == 0 && ((app.pos >= 0 && !room) || cnt <= 0 || cnt > sel_stride))
+        set_status(dev_status, TB_ERR_INVALID_ARG);
     const int j0 = chunk * per;
     const int j1 = j0 + per < cnt_c ? j0 + per : cnt_c;
     const int nch = j1 > j0 ? (j1 - j0 + kAsChunk - 1) / kAsChunk : 0;   // chunks of the CTA's slice
@@ -222,6 +227,8 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const uint32_t xs = smem_addr(X);
     const uint32_t dst_lane = (uint32_t)((lane / LPE) * SB + (pv ? 2 * DT : 0) + (pv ? pr - P : pr) * 16);
     const uint16_t *src = (pv ? V : K) + (int64_t)row * cap * DT + (pv ? pr - P : pr) * 8;
+    const uint16_t *src_new = app.pos >= 0 ? (pv ? app.V_new : app.K_new) + (int64_t)row * DT + (pv ? pr - P : pr) * 8
+                                           : src;
     const int32_t *srow = sel + (int64_t)row * sel_stride;
     const float qscale = scale * kLog2e;
 
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const int my_chunks = nch > warp ? (nch - warp + kAsWarps - 1) / kAsWarps : 0;
     auto load_idx = [&](int kk) -> int32_t {   // entry lane % 16 of this warp's chunk kk, -1 past the slice
         const int e = j0 + (warp + kk * kAsWarps) * kAsChunk + (lane & (kAsChunk - 1));
-        return (kk < my_chunks && e < j1) ? __ldg(srow + e) : -1;
+        return (kk < my_chunks && e < j1) ? (e == new_e ? (int32_t)app.pos : __ldg(srow + e)) : -1;
     };
     int32_t pidx = load_idx(0), pnext = load_idx(1);
     auto issue = [&]() {
@@ -252,7 +259,7 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
             const int ent = it * EPI + lane / LPE;
             const int32_t t = __shfl_sync(0xFFFFFFFFu, tl, ent);
             if (ent < cc)
-                cp_async16_sa(dst0 + (uint32_t)(it * EPI * SB), src + (int64_t)t * DT);
+                cp_async16_sa(dst0 + (uint32_t)(it * EPI * SB), e0 + ent == new_e ? src_new : src + (int64_t)t * DT);
             else if (pv)   // a padding slot's V row must hold finite values (its weight is zero)
                 asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst0 + (uint32_t)(it * EPI * SB)),
                              "r"(0u)
@@ -395,6 +402,15 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     stream_merge<DT>(prow, nchunk, G, out + ((int64_t)b * Hq + (int64_t)h * G) * DT, dev_status,
                      reinterpret_cast<float *>(X));
     if (tid == 0) attn_ctl[row] = 0;   // ready for the next call
+    if (app.pos >= 0) {
+        // the append kernel this launch depends on has finished (the grid ends after it); every CTA of the
+        // row has read the old count, so the tail entry joins the selection now
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0 && room) {
+            app.sel[(int64_t)row * sel_stride + cnt0] = (int32_t)app.pos;
+            app.counts[row] = cnt0 + 1;
+        }
+    }
 }
 
 bool attn_stream_supported(const tb_shape &sh) {
@@ -406,7 +422,7 @@ template <int DT, bool KT, int SETS, int MINB>
 static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
                              const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
                              uint16_t *out, uint32_t *attn_ctl, float *partials, int32_t *dev_status,
-                             cudaStream_t st, int slot) {
+                             cudaStream_t st, int slot, const AttnAppend &app) {
     const int rows = sh.B * sh.Hkv;
     // CTAs per row: about MINB CTAs per SM over all rows, each at least one round of its warps' chunks, no
     // more than the workspace's partial slots per row, and few enough that the merge's scratch (2 floats per
@@ -430,29 +446,51 @@ static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16
         if (e != cudaSuccess) return e;
         attr_dev[slot] = dev_info().device;
     }
-    fn<<<dim3((unsigned)C, (unsigned)rows), kAsThreads, smem, st>>>(q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq,
-                                                                    sh.Hkv, per, scale, out, attn_ctl, partials,
-                                                                    dev_status);
-    return cudaGetLastError();
+    if (app.pos < 0) {
+        fn<<<dim3((unsigned)C, (unsigned)rows), kAsThreads, smem, st>>>(q, K, V, sel, counts, sel_stride, sh.cap,
+                                                                        sh.Hq, sh.Hkv, per, scale, out, attn_ctl,
+                                                                        partials, dev_status, app);
+        return cudaGetLastError();
+    }
+    // after the append kernel, as its programmatic dependent: the streaming starts while the append runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, (unsigned)rows);
+    cfg.blockDim = dim3(kAsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq, sh.Hkv, per, scale, out,
+                              attn_ctl, partials, dev_status, app);
 }
 
 cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
                                const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
                                uint16_t *out, uint32_t *attn_ctl, float *partials, int32_t *dev_status,
-                               cudaStream_t st) {
+                               cudaStream_t st, const AttnAppend *app) {
     const int rows = sh.B * sh.Hkv;
     if (rows <= 0 || sel_stride <= 0) return cudaSuccess;
     if (!attn_stream_supported(sh)) return cudaErrorNotSupported;
+    const AttnAppend none;
+    const AttnAppend &ap = app ? *app : none;
+    if (ap.pos >= 0 && (!ap.K_new || !ap.V_new || !ap.sel || !ap.counts || !counts)) return cudaErrorInvalidValue;
     const bool kt = sh.Hq / sh.Hkv <= 8;
     if (sh.D == 64)
         return kt ? launch_as<64, true, kAsKtSets, kAsKtCtas>(sh, q, K, V, sel, counts, sel_stride, scale, out,
-                                                             attn_ctl, partials, dev_status, st, 0)
+                                                             attn_ctl, partials, dev_status, st, 0, ap)
                   : launch_as<64, false, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl,
-                                               partials, dev_status, st, 1);
+                                               partials, dev_status, st, 1, ap);
     return kt ? launch_as<128, true, kAsKtSets, kAsKtCtas>(sh, q, K, V, sel, counts, sel_stride, scale, out,
-                                                          attn_ctl, partials, dev_status, st, 2)
+                                                          attn_ctl, partials, dev_status, st, 2, ap)
               : launch_as<128, false, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
-                                            dev_status, st, 3);
+                                            dev_status, st, 3, ap);
+}
+
+bool attn_stream_serves(const tb_shape &sh, const uint16_t *K, const uint16_t *V) {
+    return attn_stream_supported(sh) && kv_on_device(K, V);
 }
 
 }  // namespace tb

@@ -40,10 +40,21 @@ cudaError_t launch_attn(const tb_shape &sh, const uint16_t *q, const uint16_t *K
 // The same with up to three rounds of bulk copies in flight per CTA and two
 // CTAs per SM (attn_stream.cu; D = 64 or 128, G <= 16, K/V in device memory).
 bool attn_stream_supported(const tb_shape &sh);
+// A step inside a prediction interval whose append kernel (K/V rows and projected key of the new token, no
+// selection entry) was launched just before on the same stream: the streamed attention runs as that kernel's
+// programmatic dependent, reads the new token's K/V rows from K_new / V_new, and adds the tail entry
+// (sel[row][count] = pos, count + 1) once the append has finished. pos < 0: none of this.
+struct AttnAppend {
+    const uint16_t *K_new = nullptr, *V_new = nullptr;
+    int32_t *sel = nullptr, *counts = nullptr;
+    int64_t pos = -1;
+};
 cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint16_t *K, const uint16_t *V,
                                const int32_t *sel, const int32_t *counts, int32_t sel_stride, float scale,
                                uint16_t *out, uint32_t *attn_ctl, float *partials, int32_t *dev_status,
-                               cudaStream_t st);
+                               cudaStream_t st, const AttnAppend *app = nullptr);
+// True when launch_attn (and so launch_attn_stream) serves this shape and K/V placement.
+bool attn_stream_serves(const tb_shape &sh, const uint16_t *K, const uint16_t *V);
 // True when K and V are device memory (answer kept per thread for the last pair asked).
 bool kv_on_device(const void *K, const void *V);
 

@@ -14,6 +14,7 @@
 namespace tb {
 
 constexpr int kScoreThreads = 256;
+constexpr int kScoreMultiMin = 8;   // tiles per CTA below which one tile per CTA is used
 
 template <int NV>
 __device__ __forceinline__ void load_row(const uint4 *p, uint4 (&v)[NV]) {
@@ -33,66 +34,141 @@ __device__ __forceinline__ float dot8(const float *q, uint4 v, float acc) {
     return acc;
 }
 
-// NV = dp/8 known at compile time (0: runtime nv).
+// Scores of one token from its Kp row v (NV 16-byte vectors) against the staged query (MEAN: the group-mean
+// query; MAX: the G queries).
 template <int NV>
-__global__ void __launch_bounds__(kScoreThreads)
-score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp, int64_t cap, int64_t n,
-             int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds, const int64_t *__restrict__ n_seq) {
-    extern __shared__ float qs[];   // [G][dp] (MAX) or [dp] (MEAN)
-    const int row = blockIdx.y;
-    const int b = row / Hkv, h = row % Hkv;
-    const int G = Hq / Hkv;
-    const uint16_t *qrow = q_imp + ((int64_t)b * Hq + (int64_t)h * G) * dp;
+__device__ __forceinline__ float score_of(const float *qs, const uint4 (&v)[NV], int agg, int G, int dp) {
+    if (agg == TB_AGG_MEAN) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc = dot8(qs + 8 * i, v[i], acc);
+        return acc;
+    }
+    float out = -INFINITY;
+    for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc = dot8(qs + g * dp + 8 * i, v[i], acc);
+        out = fmaxf(out, acc);
+    }
+    return out;
+}
+
+// Stage the KV head's importance queries in shared memory as fp32 (MEAN: their group mean).
+__device__ __forceinline__ void stage_queries(const uint16_t *qrow, int agg, int G, int dp, float *qs) {
     if (agg == TB_AGG_MEAN) {
         const float inv = 1.0f / (float)G;
         for (int i = threadIdx.x; i < dp; i += blockDim.x) {
             float a = 0.f;
-            for (int g = 0; g < G; ++g) a += bf16_to_f(qrow[g * dp + i]);
+#pragma unroll 8
+            for (int g = 0; g < G; ++g) a += bf16_to_f(__ldg(qrow + g * dp + i));
             qs[i] = a * inv;
         }
     } else {
-        for (int i = threadIdx.x; i < G * dp; i += blockDim.x) qs[i] = bf16_to_f(qrow[i]);
+        for (int i = threadIdx.x; i < G * dp; i += blockDim.x) qs[i] = bf16_to_f(__ldg(qrow + i));
     }
+}
+
+// NV = dp/8 known at compile time. A CTA scores U tiles of kScoreThreads consecutive tokens of one row; warp w
+// takes tokens [32w, 32w + 32) of a tile, and each of its NV load instructions reads 512 contiguous bytes: the
+// NV 16-byte pieces of 32/NV consecutive rows, lane l holding piece l % NV of one of them. Every lane dots its
+// piece with the matching 8 query dims and the NV lanes of a row add their sums by shuffles. The first tile's
+// rows are requested before the queries are staged and the next tile's while the current one is scored.
+template <int NV, bool MULTI>
+__global__ void __launch_bounds__(kScoreThreads, MULTI ? (NV <= 2 ? 4 : (NV <= 4 ? 3 : 2)) : (NV <= 4 ? 6 : 4))
+score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp, int64_t cap, int64_t n,
+             int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds, const int64_t *__restrict__ n_seq,
+             int U) {
+    extern __shared__ float qs[];   // [G][dp] (MAX) or [dp] (MEAN)
+    constexpr int TPI = 32 / NV;    // rows per load instruction of a warp
+    const int row = blockIdx.y;
+    const int b = row / Hkv, h = row % Hkv;
+    const int G = Hq / Hkv;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, pc = lane % NV;
+    // tokens past this sequence's n_seq[b] + 1 are scored -inf (never selected)
+    const int64_t n_lim = n_seq ? (n_seq[b] + 1 < n ? n_seq[b] + 1 : n) : n;
+    const int64_t w0 = (int64_t)blockIdx.x * U * kScoreThreads + warp * 32;
+    const uint4 *krow = reinterpret_cast<const uint4 *>(Kp + (int64_t)row * cap * dp);
+    float *srow = s + (int64_t)row * lds;
+    uint4 v0[NV], v1[NV];
+    auto load = [&](int u, uint4 (&v)[NV]) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int64_t t = w0 + (int64_t)u * kScoreThreads + j * TPI + lane / NV;
+            if (t < n_lim) v[j] = __ldcs(krow + t * NV + pc);
+        }
+    };
+    load(0, v0);
+    stage_queries(q_imp + ((int64_t)b * Hq + (int64_t)h * G) * dp, agg, G, dp, qs);
+    __syncthreads();
+    float qv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qv[i] = qs[8 * pc + i];   // MEAN: this lane's 8 query dims
+    auto emit = [&](int u, const uint4 (&v)[NV]) {
+        // row j * TPI + lane / NV of the warp's 32: its score, in every lane of its group
+        float mine = 0.f;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            float sc;
+            if (agg == TB_AGG_MEAN) {
+                sc = dot8(qv, v[j], 0.f);
+#pragma unroll
+                for (int o = 1; o < NV; o <<= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, o);
+            } else {
+                sc = -INFINITY;
+                for (int g = 0; g < G; ++g) {
+                    float d = dot8(qs + g * dp + 8 * pc, v[j], 0.f);
+#pragma unroll
+                    for (int o = 1; o < NV; o <<= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
+                    sc = fmaxf(sc, d);
+                }
+            }
+            if (pc == j) mine = sc;
+        }
+        // lane l writes row (l % NV) * TPI + l / NV: the warp's 32 scores in one store
+        const int64_t t = w0 + (int64_t)u * kScoreThreads + pc * TPI + lane / NV;
+        if (t < n) srow[t] = t < n_lim ? mine : -INFINITY;
+    };
+    if constexpr (!MULTI) {   // one tile: no second buffer (fewer registers, more CTAs per SM)
+        emit(0, v0);
+    } else {
+        for (int u = 0; u < U; u += 2) {
+            if (u + 1 < U) load(u + 1, v1);
+            emit(u, v0);
+            if (u + 2 < U) load(u + 2, v0);
+            if (u + 1 < U) emit(u + 1, v1);
+        }
+    }
+}
+
+// Any dp that is a multiple of 8: one token per thread.
+__global__ void __launch_bounds__(kScoreThreads)
+score_kernel_any(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp, int64_t cap, int64_t n,
+                 int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds,
+                 const int64_t *__restrict__ n_seq) {
+    extern __shared__ float qs[];
+    const int row = blockIdx.y;
+    const int b = row / Hkv, h = row % Hkv;
+    const int G = Hq / Hkv;
+    stage_queries(q_imp + ((int64_t)b * Hq + (int64_t)h * G) * dp, agg, G, dp, qs);
     __syncthreads();
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= n) return;
-    if (n_seq && t > n_seq[b]) {   // beyond this sequence's tokens (n_seq[b] + 1 of them): never selected
+    if (n_seq && t > n_seq[b]) {
         s[(int64_t)row * lds + t] = -INFINITY;
         return;
     }
-    const int nv = NV > 0 ? NV : dp / 8;
+    const int nv = dp / 8;
     const uint4 *p = reinterpret_cast<const uint4 *>(Kp + ((int64_t)row * cap + t) * dp);
-    float out;
-    constexpr int NVX = NV > 0 ? NV : 1;
-    if (NV > 0) {
-        uint4 v[NVX];
-        load_row<NVX>(p, v);
-        if (agg == TB_AGG_MEAN) {
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < NVX; ++i) acc = dot8(qs + 8 * i, v[i], acc);
-            out = acc;
-        } else {
-            out = -INFINITY;
-            for (int g = 0; g < G; ++g) {
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < NVX; ++i) acc = dot8(qs + g * dp + 8 * i, v[i], acc);
-                out = fmaxf(out, acc);
-            }
-        }
+    float out = -INFINITY;
+    if (agg == TB_AGG_MEAN) {
+        out = 0.f;
+        for (int i = 0; i < nv; ++i) out = dot8(qs + 8 * i, __ldcs(p + i), out);
     } else {
-        if (agg == TB_AGG_MEAN) {
+        for (int g = 0; g < G; ++g) {
             float acc = 0.f;
-            for (int i = 0; i < nv; ++i) acc = dot8(qs + 8 * i, __ldcs(p + i), acc);
-            out = acc;
-        } else {
-            out = -INFINITY;
-            for (int g = 0; g < G; ++g) {
-                float acc = 0.f;
-                for (int i = 0; i < nv; ++i) acc = dot8(qs + g * dp + 8 * i, __ldcs(p + i), acc);
-                out = fmaxf(out, acc);
-            }
+            for (int i = 0; i < nv; ++i) acc = dot8(qs + g * dp + 8 * i, __ldcs(p + i), acc);
+            out = fmaxf(out, acc);
         }
     }
     s[(int64_t)row * lds + t] = out;
@@ -103,13 +179,24 @@ cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16
     const int rows = sh.B * sh.Hkv;
     if (n <= 0 || rows <= 0) return cudaSuccess;
     const int G = sh.Hq / sh.Hkv;
-    dim3 grid((unsigned)((n + kScoreThreads - 1) / kScoreThreads), (unsigned)rows);
-    size_t smem = (size_t)(agg == TB_AGG_MEAN ? 1 : G) * sh.dp * sizeof(float);
+    const size_t smem = (size_t)(agg == TB_AGG_MEAN ? 1 : G) * sh.dp * sizeof(float);
     const int nv = sh.dp / 8;
-#define TB_SCORE_CASE(NVC)                                                                                 \
-    case NVC:                                                                                              \
-        score_kernel<NVC><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv, sh.dp, agg, \
-                                                             s, lds, n_seq);                                      \
+    // tiles per CTA: one (many light CTAs) unless the stream is long enough to leave several tiles per CTA
+    // at four CTAs per SM; then up to 8
+    const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
+    const int64_t tiles = (n + kScoreThreads - 1) / kScoreThreads;
+    int64_t U = tiles * rows / (4LL * sms);
+    if (U > 8) U = 8;
+    if (U < kScoreMultiMin) U = 1;
+    const dim3 grid((unsigned)((tiles + U - 1) / U), (unsigned)rows);
+#define TB_SCORE_CASE(NVC)                                                                                       \
+    case NVC:                                                                                                    \
+        if (U > 1)                                                                                               \
+            score_kernel<NVC, true><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,      \
+                                                                       sh.dp, agg, s, lds, n_seq, (int)U);       \
+        else                                                                                                     \
+            score_kernel<NVC, false><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,     \
+                                                                        sh.dp, agg, s, lds, n_seq, 1);           \
         break;
     switch (nv) {
         TB_SCORE_CASE(1)
@@ -117,8 +204,8 @@ cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16
         TB_SCORE_CASE(4)
         TB_SCORE_CASE(8)
         default:
-            score_kernel<0><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv, sh.dp, agg, s,
-                                                               lds, n_seq);
+            score_kernel_any<<<dim3((unsigned)tiles, (unsigned)rows), kScoreThreads, smem, st>>>(
+                q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv, sh.dp, agg, s, lds, n_seq);
     }
 #undef TB_SCORE_CASE
     return cudaGetLastError();

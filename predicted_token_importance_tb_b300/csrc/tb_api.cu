@@ -306,8 +306,10 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
         *n_pred = n_t;
         return TB_OK;
     }
-    // 1. append (and, inside an interval, the tail entry of the selection)
-    e = launch_append(*shape, K_new, V_new, Wk, K, V, Kp, n, predict ? nullptr : sel, sel_stride, counts,
+    // 1. append (and, inside an interval, the tail entry of the selection; the streamed attention adds that
+    // entry itself when it serves the call, and starts while the append runs)
+    const bool fold = !predict && attn_stream_serves(*shape, K, V);
+    e = launch_append(*shape, K_new, V_new, Wk, K, V, Kp, n, predict || fold ? nullptr : sel, sel_stride, counts,
                       dev_status, stream);
     if (e != cudaSuccess) return from_cuda(e);
     if (predict) {
@@ -327,7 +329,18 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
         *n_pred = n_t;
     }
     // 3. attention over the selection
-    e = launch_attn(*shape, q, K, V, sel, counts, sel_stride, p->scale, out, actl, part, dev_status, stream);
+    if (fold) {
+        AttnAppend app;
+        app.K_new = K_new;
+        app.V_new = V_new;
+        app.sel = sel;
+        app.counts = counts;
+        app.pos = n;
+        e = launch_attn_stream(*shape, q, K, V, sel, counts, sel_stride, p->scale, out, actl, part, dev_status,
+                               stream, &app);
+    } else {
+        e = launch_attn(*shape, q, K, V, sel, counts, sel_stride, p->scale, out, actl, part, dev_status, stream);
+    }
     return from_cuda(e);
 }
 
