@@ -25,12 +25,28 @@ constexpr int kAsChunk = 16;   // entries per warp chunk (one tensor-core tile o
 // keys-as-rows form: chunks in flight per warp and CTAs per SM
 constexpr int kAsKtSets = 3;
 constexpr int kAsKtCtas = 2;
+constexpr int kAsClusterMax = 8;   // most CTAs per row that merge as one cluster (the portable cluster size; 9-CTA
+                                   // clusters measured slower: they pack poorly onto the GPCs)
 
 // SETS: chunks in flight per warp.
 __host__ __device__ constexpr int attn_stream_smem_bytes(int DT, int SETS) {
     return SETS * kAsWarps * kAsChunk * (4 * DT + 16)   // chunk buffers: set s holds warp w's chunk at w
            + 16 * (2 * DT + 16)                         // query tile
            + SETS * kAsWarps * kAsChunk;                // per-slot flags (valid entry)
+}
+
+// Barrier over the CTAs of a thread-block cluster (release / acquire of their shared memory).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fp32 load from the shared memory of CTA `rank` of this cluster, at the address `a` has in this CTA.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a, int rank) {
+    uint32_t r;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+    return v;
 }
 
 // 16-byte asynchronous copy global -> shared, destination given as a shared-window address.
@@ -186,9 +202,11 @@ __device__ __forceinline__ void stream_merge(const float *__restrict__ part, int
 
 // Grid (C, rows): CTA c of a row takes entries [c * per, (c + 1) * per) of the row's selection (clipped to its
 // count), cut into chunks of 16 that its warps take in turn. The warps' states are combined into the CTA's
-// partial (m, l, acc[D] per head) and the row's last arriving CTA merges the C partials. KT: keys as the MMA
-// rows (G <= 8); otherwise the G heads are the rows (G <= 16).
-template <int DT, bool KT, int SETS, int MINB>
+// partial (m, l, acc[D] per head). CL: the row's C CTAs are one cluster, keep their partials in shared memory
+// and each merges a slice of the outputs through distributed shared memory; otherwise the partials go to the
+// workspace and the row's last arriving CTA merges them. KT: keys as the MMA rows (G <= 8); otherwise the G
+// heads are the rows (G <= 16).
+template <int DT, bool KT, int SETS, int MINB, bool CL>
 __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ K, const uint16_t *__restrict__ V,
     const int32_t *__restrict__ sel, const int32_t *__restrict__ counts, int32_t sel_stride, int64_t cap, int Hq,
@@ -368,6 +386,66 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
         }
     }
     __syncthreads();
+    if constexpr (CL) {
+        float *cp = ws + (int64_t)kAsWarps * G * sg;   // this CTA's partial: (m, l, acc[D]) per head
+        for (int x = tid; x < G * DT; x += kAsThreads) {
+            const int g = x / DT, d = x % DT;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kAsWarps; ++w) M = fmaxf(M, ws[((int64_t)w * G + g) * sg]);
+            float L = 0.f, Acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kAsWarps; ++w) {
+                const float *sw = ws + ((int64_t)w * G + g) * sg;
+                const float wt = rescale_w(sw[0], M);
+                L = fmaf(wt, sw[1], L);
+                Acc = fmaf(wt, sw[2 + d], Acc);
+            }
+            if (d == 0) {
+                cp[g * sg] = M;
+                cp[g * sg + 1] = L;
+            }
+            cp[g * sg + 2 + d] = Acc;
+        }
+        cluster_sync();   // every partial of the row is complete and visible to the cluster
+        if (app.pos >= 0 && chunk == 0) {
+            // the append kernel this launch depends on has finished; every CTA of the row has read the old
+            // count (they passed the barrier), so the tail entry joins the selection now
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (tid == 0 && room) {
+                app.sel[(int64_t)row * sel_stride + cnt0] = (int32_t)app.pos;
+                app.counts[row] = cnt0 + 1;
+            }
+        }
+        // this CTA's slice of the G x D outputs, merged over the cluster's partials
+        const uint32_t cpa = smem_addr(cp);
+        const int span = (G * DT + nchunk - 1) / nchunk;
+        const int x1 = (chunk + 1) * span < G * DT ? (chunk + 1) * span : G * DT;
+        uint16_t *orow = out + ((int64_t)b * Hq + (int64_t)h * G) * DT;
+        for (int x = chunk * span + tid; x < x1; x += kAsThreads) {
+            const int g = x / DT, d = x % DT;
+            float mj[kAsClusterMax];
+            float M = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kAsClusterMax; ++j) {
+                mj[j] = j < nchunk ? ld_cluster_f32(cpa + (uint32_t)(g * sg) * 4u, j) : -INFINITY;
+                M = fmaxf(M, mj[j]);
+            }
+            float L = 0.f, Acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kAsClusterMax; ++j) {
+                if (j < nchunk) {
+                    const float w = rescale_w(mj[j], M);
+                    L = fmaf(w, ld_cluster_f32(cpa + (uint32_t)(g * sg + 1) * 4u, j), L);
+                    Acc = fmaf(w, ld_cluster_f32(cpa + (uint32_t)(g * sg + 2 + d) * 4u, j), Acc);
+                }
+            }
+            if (!(L > 0.f)) set_status(dev_status, TB_ERR_INVALID_ARG);
+            orow[x] = f_to_bf16(L > 0.f ? Acc / L : 0.f);
+        }
+        cluster_sync();   // no CTA leaves while the others still read its partial
+        return;
+    }
     float *prow = part + (int64_t)row * nchunk * G * sg;
     for (int x = tid; x < G * DT; x += kAsThreads) {
         const int g = x / DT, d = x % DT;
@@ -439,30 +517,37 @@ static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16
     const int per = (int)((sel_stride + C - 1) / C);
     C = (sel_stride + per - 1) / per;
     const size_t smem = (size_t)attn_stream_smem_bytes(DT, SETS);
-    static thread_local int attr_dev[4] = {-1, -1, -1, -1};
-    auto fn = attn_stream_kernel<DT, KT, SETS, MINB>;
-    if (attr_dev[slot] != dev_info().device) {
+    // up to kAsClusterMax CTAs per row: the row is one cluster and merges in distributed shared memory
+    const bool cl = C <= kAsClusterMax;
+    static thread_local int attr_dev[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    auto fn = cl ? attn_stream_kernel<DT, KT, SETS, MINB, true> : attn_stream_kernel<DT, KT, SETS, MINB, false>;
+    const int s2 = 2 * slot + (cl ? 1 : 0);
+    if (attr_dev[s2] != dev_info().device) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_dev[slot] = dev_info().device;
+        attr_dev[s2] = dev_info().device;
     }
-    if (app.pos < 0) {
-        fn<<<dim3((unsigned)C, (unsigned)rows), kAsThreads, smem, st>>>(q, K, V, sel, counts, sel_stride, sh.cap,
-                                                                        sh.Hq, sh.Hkv, per, scale, out, attn_ctl,
-                                                                        partials, dev_status, app);
-        return cudaGetLastError();
-    }
-    // after the append kernel, as its programmatic dependent: the streaming starts while the append runs
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)C, (unsigned)rows);
     cfg.blockDim = dim3(kAsThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (cl) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)C;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (app.pos >= 0) {   // after the append kernel, as its programmatic dependent: it streams while the append runs
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, fn, q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq, sh.Hkv, per, scale, out,
                               attn_ctl, partials, dev_status, app);
 }
