@@ -514,6 +514,8 @@ static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16
     if (C > cround) C = cround;
     if (C > cfit) C = cfit;
     if (C < 1) C = 1;
+    // a little above the cluster limit: fewer CTAs per row, but the cluster merge
+    if (C > kAsClusterMax && C <= kAsClusterMax + kAsClusterMax / 2) C = kAsClusterMax;
     const int per = (int)((sel_stride + C - 1) / C);
     C = (sel_stride + per - 1) / per;
     const size_t smem = (size_t)attn_stream_smem_bytes(DT, SETS);
