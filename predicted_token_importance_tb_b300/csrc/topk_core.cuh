@@ -170,11 +170,11 @@ __device__ __forceinline__ SelectBegin group_select_begin(RowCtl *ctl, SelectSme
         if (top > prefix) ++my_above;
         else if (top == prefix) ++my_eq;
     }
+    // one scan of both counts: above in the high half, equal in the low half (a chunk holds < 2^16 keys)
     uint32_t tot;
-    (void)block_exclusive_scan(my_above, S.scan, tot);
-    const uint32_t chunk_above = tot;
-    const uint32_t eq_before = block_exclusive_scan(my_eq, S.scan, tot);
-    const uint32_t chunk_eq = tot;
+    const uint32_t before = block_exclusive_scan((my_above << 16) | my_eq, S.scan, tot);
+    const uint32_t chunk_above = tot >> 16, chunk_eq = tot & 0xFFFFu;
+    const uint32_t eq_before = before & 0xFFFFu;
     if (mode_cand) {   // the chunk's candidates, at slots reserved with one atomic per CTA
         if (threadIdx.x == 0) S.misc[7] = atomicAdd(&ctl->ncand, chunk_eq);
         __syncthreads();
@@ -289,10 +289,10 @@ __device__ __forceinline__ bool is_kept(const SelectResult &R, uint32_t key, uin
 
 // Write the kept tokens of this chunk, ascending, to out[R.offset ...] (and
 // to out2 when given). The chunk's keys are in S.keys; token of element e is
-// tok0 + e. Warp w takes a contiguous run of the chunk in stripes of 32 and
-// counts its kept elements with ballots (in mode 1 the tied elements first,
-// since ties go to the lowest tokens); one block scan over the warps' counts
-// gives each warp its first output slot.
+// tok0 + e; S.keys is overwritten. Warp w takes a contiguous run of the
+// chunk in stripes of 32 and finds its kept elements with ballots (in mode 1
+// the tied elements are counted first, since ties go to the lowest tokens);
+// one block scan over the warps' counts gives each warp its first output slot.
 __device__ __forceinline__ void write_kept(const SelectResult &R, SelectSmem &S, int Lc, uint32_t tok0,
                                           int32_t *out, int32_t *out2 = nullptr) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -325,6 +325,26 @@ __device__ __forceinline__ void write_kept(const SelectResult &R, SelectSmem &S,
         }
         return __ballot_sync(0xFFFFFFFFu, kp);
     };
+    if (R.mode == 0) {
+        // one pass: each warp compacts its kept tokens in place over its own run of S.keys (a kept token is
+        // written at or before the position it was read from); one block scan places the runs
+        uint32_t nk = 0;
+        for (int b = e0; b < e1; b += 32) {
+            const int e = b + lane;
+            const bool kp = e < e1 && composite(S.keys[e], tok0 + (uint32_t)e) >= R.compT;
+            const uint32_t kb = __ballot_sync(0xFFFFFFFFu, kp);
+            __syncwarp();   // the whole stripe is read before any lane writes into it
+            if (kp) S.keys[e0 + nk + __popc(kb & lt)] = tok0 + (uint32_t)e;
+            nk += __popc(kb);
+        }
+        uint32_t wpos = block_exclusive_scan(lane == 0 ? nk : 0u, S.scan, tot);
+        wpos = R.offset + __shfl_sync(0xFFFFFFFFu, wpos, 0);
+        for (uint32_t i = lane; i < nk; i += 32) {
+            out[wpos + i] = (int32_t)S.keys[e0 + i];
+            if (out2) out2[wpos + i] = (int32_t)S.keys[e0 + i];
+        }
+        return;
+    }
     uint32_t nk = 0, run = tied_base;
     for (int b = e0; b < e1; b += 32) nk += __popc(stripe(b, run));
     uint32_t pos = block_exclusive_scan(lane == 0 ? nk : 0u, S.scan, tot);
