@@ -200,8 +200,8 @@ __device__ __forceinline__ void stream_merge(const float *__restrict__ part, int
     }
 }
 
-// Grid (C, rows): CTA c of a row takes entries [c * per, (c + 1) * per) of the row's selection (clipped to its
-// count), cut into chunks of 16 that its warps take in turn. The warps' states are combined into the CTA's
+// Grid (C, rows): CTA c of a row takes the c-th of C equal slices (whole chunks of 16) of the row's selection,
+// cut into chunks of 16 that its warps take in turn. The warps' states are combined into the CTA's
 // partial (m, l, acc[D] per head). CL: the row's C CTAs are one cluster, keep their partials in shared memory
 // and each merges a slice of the outputs through distributed shared memory; otherwise the partials go to the
 // workspace and the row's last arriving CTA merges them. KT: keys as the MMA rows (G <= 8); otherwise the G
@@ -210,7 +210,7 @@ template <int DT, bool KT, int SETS, int MINB, bool CL>
 __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ K, const uint16_t *__restrict__ V,
     const int32_t *__restrict__ sel, const int32_t *__restrict__ counts, int32_t sel_stride, int64_t cap, int Hq,
-    int Hkv, int per, float scale, uint16_t *__restrict__ out, uint32_t *__restrict__ attn_ctl,
+    int Hkv, float scale, uint16_t *__restrict__ out, uint32_t *__restrict__ attn_ctl,
     float *__restrict__ part, int32_t *dev_status, AttnAppend app) {
     extern __shared__ __align__(128) uint8_t smb[];
     __shared__ uint32_t s_last;
@@ -233,6 +233,8 @@ __global__ void __launch_bounds__(kAsThreads, MINB) attn_stream_kernel(
     const int cnt_c = cnt < 0 ? 0 : (cnt > sel_stride ? sel_stride : cnt);
     if (tid == 0 && chunk == 0 && ((app.pos >= 0 && !room) || cnt <= 0 || cnt > sel_stride))
         set_status(dev_status, TB_ERR_INVALID_ARG);
+    // equal slices of the row's realised count, in whole chunks
+    const int per = ((cnt_c + nchunk - 1) / nchunk + kAsChunk - 1) / kAsChunk * kAsChunk;
     const int j0 = chunk * per;
     const int j1 = j0 + per < cnt_c ? j0 + per : cnt_c;
     const int nch = j1 > j0 ? (j1 - j0 + kAsChunk - 1) / kAsChunk : 0;   // chunks of the CTA's slice
@@ -550,7 +552,7 @@ static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, fn, q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq, sh.Hkv, per, scale, out,
+    return cudaLaunchKernelEx(&cfg, fn, q, K, V, sel, counts, sel_stride, sh.cap, sh.Hq, sh.Hkv, scale, out,
                               attn_ctl, partials, dev_status, app);
 }
 
