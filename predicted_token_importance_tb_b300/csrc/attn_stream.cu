@@ -22,9 +22,8 @@ namespace tb {
 constexpr int kAsThreads = 128;
 constexpr int kAsWarps = kAsThreads / 32;
 constexpr int kAsChunk = 16;   // entries per warp chunk (one tensor-core tile of slots)
-// keys-as-rows form: chunks in flight per warp and CTAs per SM
-constexpr int kAsKtSets = 3;
-constexpr int kAsKtCtas = 2;
+// keys-as-rows form: three CTAs per SM with two chunks in flight per warp when a row's CTAs still fit one
+// cluster (more warps per SM stream faster), else two CTAs per SM with three chunks in flight
 constexpr int kAsClusterMax = 8;   // most CTAs per row that merge as one cluster (the portable cluster size; 9-CTA
                                    // clusters measured slower: they pack poorly onto the GPCs)
 
@@ -523,7 +522,7 @@ static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16
     const size_t smem = (size_t)attn_stream_smem_bytes(DT, SETS);
     // up to kAsClusterMax CTAs per row: the row is one cluster and merges in distributed shared memory
     const bool cl = C <= kAsClusterMax;
-    static thread_local int attr_dev[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    static thread_local int attr_dev[12] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
     auto fn = cl ? attn_stream_kernel<DT, KT, SETS, MINB, true> : attn_stream_kernel<DT, KT, SETS, MINB, false>;
     const int s2 = 2 * slot + (cl ? 1 : 0);
     if (attr_dev[s2] != dev_info().device) {
@@ -567,13 +566,22 @@ cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint
     const AttnAppend &ap = app ? *app : none;
     if (ap.pos >= 0 && (!ap.K_new || !ap.V_new || !ap.sel || !ap.counts || !counts)) return cudaErrorInvalidValue;
     const bool kt = sh.Hq / sh.Hkv <= 8;
-    if (sh.D == 64)
-        return kt ? launch_as<64, true, kAsKtSets, kAsKtCtas>(sh, q, K, V, sel, counts, sel_stride, scale, out,
-                                                             attn_ctl, partials, dev_status, st, 0, ap)
+    const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
+    const bool three = kt && (3 * sms) / rows <= kAsClusterMax;
+    if (sh.D == 64) {
+        if (three)
+            return launch_as<64, true, 2, 3>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
+                                             dev_status, st, 4, ap);
+        return kt ? launch_as<64, true, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
+                                              dev_status, st, 0, ap)
                   : launch_as<64, false, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl,
                                                partials, dev_status, st, 1, ap);
-    return kt ? launch_as<128, true, kAsKtSets, kAsKtCtas>(sh, q, K, V, sel, counts, sel_stride, scale, out,
-                                                          attn_ctl, partials, dev_status, st, 2, ap)
+    }
+    if (three)
+        return launch_as<128, true, 2, 3>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
+                                          dev_status, st, 5, ap);
+    return kt ? launch_as<128, true, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
+                                           dev_status, st, 2, ap)
               : launch_as<128, false, 3, 2>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
                                             dev_status, st, 3, ap);
 }
