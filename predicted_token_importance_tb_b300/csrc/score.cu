@@ -78,9 +78,12 @@ template <int NV, bool MULTI>
 __global__ void __launch_bounds__(kScoreThreads, MULTI ? (NV <= 2 ? 4 : (NV <= 4 ? 3 : 2)) : (NV <= 4 ? 6 : 4))
 score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp, int64_t cap, int64_t n,
              int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds, const int64_t *__restrict__ n_seq,
-             int U) {
+             int U, int after_append) {
     extern __shared__ float qs[];   // [G][dp] (MAX) or [dp] (MEAN)
     constexpr int TPI = 32 / NV;    // rows per load instruction of a warp
+    // launched as the append kernel's programmatic dependent: only the row's last CTA reads the appended Kp
+    // row, so only it waits for that kernel to finish
+    if (after_append && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.y;
     const int b = row / Hkv, h = row % Hkv;
     const int G = Hq / Hkv;
@@ -175,7 +178,7 @@ score_kernel_any(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict_
 }
 
 cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16_t *Kp, int64_t n, int agg,
-                         float *s, int64_t lds, cudaStream_t st, const int64_t *n_seq) {
+                         float *s, int64_t lds, cudaStream_t st, const int64_t *n_seq, bool after_append) {
     const int rows = sh.B * sh.Hkv;
     if (n <= 0 || rows <= 0) return cudaSuccess;
     const int G = sh.Hq / sh.Hkv;
@@ -189,15 +192,23 @@ cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16
     if (U > 8) U = 8;
     if (U < kScoreMultiMin) U = 1;
     const dim3 grid((unsigned)((tiles + U - 1) / U), (unsigned)rows);
-#define TB_SCORE_CASE(NVC)                                                                                       \
-    case NVC:                                                                                                    \
-        if (U > 1)                                                                                               \
-            score_kernel<NVC, true><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,      \
-                                                                       sh.dp, agg, s, lds, n_seq, (int)U);       \
-        else                                                                                                     \
-            score_kernel<NVC, false><<<grid, kScoreThreads, smem, st>>>(q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,     \
-                                                                        sh.dp, agg, s, lds, n_seq, 1);           \
-        break;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kScoreThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_append ? 1 : 0;
+    const int aa = after_append ? 1 : 0;
+#define TB_SCORE_CASE(NVC)                                                                                        \
+    case NVC:                                                                                                     \
+        return U > 1 ? cudaLaunchKernelEx(&cfg, score_kernel<NVC, true>, q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,     \
+                                          sh.dp, agg, s, lds, n_seq, (int)U, aa)                                  \
+                     : cudaLaunchKernelEx(&cfg, score_kernel<NVC, false>, q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,    \
+                                          sh.dp, agg, s, lds, n_seq, 1, aa);
     switch (nv) {
         TB_SCORE_CASE(1)
         TB_SCORE_CASE(2)

@@ -314,7 +314,7 @@ tb_status tb_decode_step(const tb_shape *shape, const tb_step_params *p, int64_t
     if (e != cudaSuccess) return from_cuda(e);
     if (predict) {
         // 2. score the n+1 tokens, select, widen
-        e = launch_score(*shape, q_imp, Kp, n_t, p->agg, scores, n_t, stream);
+        e = launch_score(*shape, q_imp, Kp, n_t, p->agg, scores, n_t, stream, nullptr, true);
         if (e != cudaSuccess) return from_cuda(e);
         if (p->r == 0 && p->T == 1) {
             // no neighbours and no tail: the selection is the prediction itself
