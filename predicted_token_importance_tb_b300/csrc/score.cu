@@ -69,13 +69,13 @@ __device__ __forceinline__ void stage_queries(const uint16_t *qrow, int agg, int
     }
 }
 
-// NV = dp/8 known at compile time. A CTA scores U tiles of kScoreThreads consecutive tokens of one row; warp w
-// takes tokens [32w, 32w + 32) of a tile, and each of its NV load instructions reads 512 contiguous bytes: the
-// NV 16-byte pieces of 32/NV consecutive rows, lane l holding piece l % NV of one of them. Every lane dots its
-// piece with the matching 8 query dims and the NV lanes of a row add their sums by shuffles. The first tile's
-// rows are requested before the queries are staged and the next tile's while the current one is scored.
-template <int NV, bool MULTI>
-__global__ void __launch_bounds__(kScoreThreads, MULTI ? (NV <= 2 ? 4 : (NV <= 4 ? 3 : 2)) : (NV <= 4 ? 6 : 4))
+// NV = dp/8 known at compile time. A CTA scores one tile of kScoreThreads consecutive tokens of one row; warp w
+// takes tokens [32w, 32w + 32), and each of its NV load instructions reads 512 contiguous bytes: the NV 16-byte
+// pieces of 32/NV consecutive rows, lane l holding piece l % NV of one of them. Every lane dots its piece with
+// the matching 8 query dims and the NV lanes of a row add their sums by shuffles. The tile's rows are requested
+// before the queries are staged.
+template <int NV>
+__global__ void __launch_bounds__(kScoreThreads, NV <= 4 ? 6 : 4)
 score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp, int64_t cap, int64_t n,
              int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds, const int64_t *__restrict__ n_seq,
              int U, int after_append) {
@@ -93,7 +93,7 @@ score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp
     const int64_t w0 = (int64_t)blockIdx.x * U * kScoreThreads + warp * 32;
     const uint4 *krow = reinterpret_cast<const uint4 *>(Kp + (int64_t)row * cap * dp);
     float *srow = s + (int64_t)row * lds;
-    uint4 v0[NV], v1[NV];
+    uint4 v0[NV];
     auto load = [&](int u, uint4 (&v)[NV]) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
@@ -132,15 +132,88 @@ score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp
         const int64_t t = w0 + (int64_t)u * kScoreThreads + pc * TPI + lane / NV;
         if (t < n) srow[t] = t < n_lim ? mine : -INFINITY;
     };
-    if constexpr (!MULTI) {   // one tile: no second buffer (fewer registers, more CTAs per SM)
-        emit(0, v0);
-    } else {
-        for (int u = 0; u < U; u += 2) {
-            if (u + 1 < U) load(u + 1, v1);
-            emit(u, v0);
-            if (u + 2 < U) load(u + 2, v0);
-            if (u + 1 < U) emit(u + 1, v1);
+    emit(0, v0);
+}
+
+constexpr int kScoreDepth = 4;   // tiles in a warp's ring: three in flight while one is scored
+
+// Long rows: a CTA scores U tiles of kScoreThreads tokens of one row. Each warp keeps a ring of kScoreDepth
+// copies of its 32-token slice of a tile in shared memory, filled by 16-byte cp.async pieces in the same
+// 512-byte-per-instruction order as score_kernel, so three tiles are in flight per warp without holding
+// registers; the scoring is score_kernel's.
+template <int NV>
+__global__ void __launch_bounds__(kScoreThreads, NV <= 2 ? 4 : (NV <= 4 ? 3 : 1))
+score_ring_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp, int64_t cap, int64_t n,
+                  int Hq, int Hkv, int dp, int agg, float *__restrict__ s, int64_t lds,
+                  const int64_t *__restrict__ n_seq, int U, int after_append) {
+    extern __shared__ __align__(16) uint8_t smb[];
+    constexpr int TPI = 32 / NV, WT = 512 * NV;   // rows per load instruction; bytes of a warp's slice
+    if (after_append && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int row = blockIdx.y;
+    const int b = row / Hkv, h = row % Hkv;
+    const int G = Hq / Hkv;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, pc = lane % NV;
+    float *qs = reinterpret_cast<float *>(smb + (kScoreThreads / 32) * kScoreDepth * WT);
+    const uint32_t rb = (uint32_t)__cvta_generic_to_shared(smb + warp * kScoreDepth * WT) + lane * 16;
+    const int64_t n_lim = n_seq ? (n_seq[b] + 1 < n ? n_seq[b] + 1 : n) : n;
+    const int64_t w0 = (int64_t)blockIdx.x * U * kScoreThreads + warp * 32;
+    const uint4 *krow = reinterpret_cast<const uint4 *>(Kp + (int64_t)row * cap * dp);
+    float *srow = s + (int64_t)row * lds;
+    auto issue = [&](int u) {   // this warp's slice of tile u into ring slot u % kScoreDepth
+        const uint32_t dst = rb + (uint32_t)((u % kScoreDepth) * WT);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int64_t t = w0 + (int64_t)u * kScoreThreads + j * TPI + lane / NV;
+            if (t < n_lim)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + j * 512), "l"(krow + t * NV + pc)
+                             : "memory");
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int issued = 0;
+    for (; issued < kScoreDepth - 1 && issued < U; ++issued) issue(issued);
+    stage_queries(q_imp + ((int64_t)b * Hq + (int64_t)h * G) * dp, agg, G, dp, qs);
+    __syncthreads();
+    float qv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qv[i] = qs[8 * pc + i];   // MEAN: this lane's 8 query dims
+    for (int u = 0; u < U; ++u) {
+        // this lane's pieces of tile u have landed once at most issued - u - 1 groups are pending
+        const int pend = issued - u - 1;
+        if (pend >= 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+        else if (pend == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();   // every lane's pieces of the slice are visible to the warp
+        uint4 v[NV];
+        const uint32_t src = rb + (uint32_t)((u % kScoreDepth) * WT);
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
+                         : "r"(src + j * 512));
+        __syncwarp();   // the slot of tile u - 1, refilled next, was read by every lane
+        if (issued < U) issue(issued++);
+        float mine = 0.f;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            float sc;
+            if (agg == TB_AGG_MEAN) {
+                sc = dot8(qv, v[j], 0.f);
+#pragma unroll
+                for (int o = 1; o < NV; o <<= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, o);
+            } else {
+                sc = -INFINITY;
+                for (int g = 0; g < G; ++g) {
+                    float d = dot8(qs + g * dp + 8 * pc, v[j], 0.f);
+#pragma unroll
+                    for (int o = 1; o < NV; o <<= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
+                    sc = fmaxf(sc, d);
+                }
+            }
+            if (pc == j) mine = sc;
+        }
+        const int64_t t = w0 + (int64_t)u * kScoreThreads + pc * TPI + lane / NV;
+        if (t < n) srow[t] = t < n_lim ? mine : -INFINITY;
     }
 }
 
@@ -203,12 +276,23 @@ cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16
     cfg.attrs = attr;
     cfg.numAttrs = after_append ? 1 : 0;
     const int aa = after_append ? 1 : 0;
+    const size_t ring_smem = (size_t)(kScoreThreads / 32) * kScoreDepth * 512 * nv + smem;
 #define TB_SCORE_CASE(NVC)                                                                                        \
     case NVC:                                                                                                     \
-        return U > 1 ? cudaLaunchKernelEx(&cfg, score_kernel<NVC, true>, q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,     \
-                                          sh.dp, agg, s, lds, n_seq, (int)U, aa)                                  \
-                     : cudaLaunchKernelEx(&cfg, score_kernel<NVC, false>, q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv,    \
-                                          sh.dp, agg, s, lds, n_seq, 1, aa);
+        if (U > 1) {                                                                                              \
+            cfg.dynamicSmemBytes = ring_smem;                                                                     \
+            static thread_local int attr_dev_##NVC = -1;                                                          \
+            if (attr_dev_##NVC != dev_info().device) {                                                            \
+                cudaError_t e = cudaFuncSetAttribute(score_ring_kernel<NVC>,                                      \
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_smem); \
+                if (e != cudaSuccess) return e;                                                                   \
+                attr_dev_##NVC = dev_info().device;                                                               \
+            }                                                                                                     \
+            return cudaLaunchKernelEx(&cfg, score_ring_kernel<NVC>, q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv, sh.dp,   \
+                                      agg, s, lds, n_seq, (int)U, aa);                                            \
+        }                                                                                                         \
+        return cudaLaunchKernelEx(&cfg, score_kernel<NVC>, q_imp, Kp, sh.cap, n, sh.Hq, sh.Hkv, sh.dp, agg, s,    \
+                                  lds, n_seq, 1, aa);
     switch (nv) {
         TB_SCORE_CASE(1)
         TB_SCORE_CASE(2)
