@@ -22,8 +22,9 @@ namespace tb {
 constexpr int kAsThreads = 128;
 constexpr int kAsWarps = kAsThreads / 32;
 constexpr int kAsChunk = 16;   // entries per warp chunk (one tensor-core tile of slots)
-// keys-as-rows form: three CTAs per SM with two chunks in flight per warp when a row's CTAs still fit one
-// cluster (more warps per SM stream faster), else two CTAs per SM with three chunks in flight
+// keys-as-rows form: three CTAs per SM with two chunks in flight per warp when a row needs at most twice the
+// cluster limit of CTAs (it then takes one cluster; more warps per SM stream faster), else two CTAs per SM with
+// three chunks in flight
 constexpr int kAsClusterMax = 8;   // most CTAs per row that merge as one cluster (the portable cluster size; 9-CTA
                                    // clusters measured slower: they pack poorly onto the GPCs)
 
@@ -515,8 +516,9 @@ static cudaError_t launch_as(const tb_shape &sh, const uint16_t *q, const uint16
     if (C > cround) C = cround;
     if (C > cfit) C = cfit;
     if (C < 1) C = 1;
-    // a little above the cluster limit: fewer CTAs per row, but the cluster merge
-    if (C > kAsClusterMax && C <= kAsClusterMax + kAsClusterMax / 2) C = kAsClusterMax;
+    // above the cluster limit by a little (or in the three-CTA form, by up to 2x): fewer CTAs per row, but the
+    // cluster merge
+    if (C > kAsClusterMax && (MINB == 3 || C <= kAsClusterMax + kAsClusterMax / 2)) C = kAsClusterMax;
     const int per = (int)((sel_stride + C - 1) / C);
     C = (sel_stride + per - 1) / per;
     const size_t smem = (size_t)attn_stream_smem_bytes(DT, SETS);
@@ -567,7 +569,7 @@ cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint
     if (ap.pos >= 0 && (!ap.K_new || !ap.V_new || !ap.sel || !ap.counts || !counts)) return cudaErrorInvalidValue;
     const bool kt = sh.Hq / sh.Hkv <= 8;
     const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
-    const bool three = kt && (3 * sms) / rows <= kAsClusterMax;
+    const bool three = kt && (3 * sms) / rows <= 2 * kAsClusterMax;
     if (sh.D == 64) {
         if (three)
             return launch_as<64, true, 2, 3>(sh, q, K, V, sel, counts, sel_stride, scale, out, attn_ctl, partials,
