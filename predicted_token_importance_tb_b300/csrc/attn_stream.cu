@@ -3,17 +3,21 @@
 // selected tokens' K/V rows are read; gist.science summary, Optimizations:
 // between predictions the same selection, plus the newest tokens, is reused).
 //
-// Grid (chunks, rows), two CTAs of four warps per SM: a CTA takes a
-// contiguous slice of its row's selection, cut into chunks of 16 entries that
-// its warps take in turn. Each warp streams its own chunks: its lanes copy the
-// chunk's K and V rows in 16-byte pieces (cp.async, one commit group per
-// chunk), up to three chunks are in flight, and the oldest is attended on the
-// tensor cores (attn_mma.cuh) by that warp alone, so the steady state has no
-// CTA-wide barrier. (One bulk copy per 256-byte row was tried first: the
-// per-copy cost of the bulk-copy unit held each SM to about 20 GB/s.) The
-// warps' softmax states are combined into the CTA's partial and the row's
-// last CTA merges them. Entries outside [0, cap) are reported and masked
-// (their slots read row 0 of the head).
+// Grid (C, rows) of four-warp CTAs: the C CTAs of a row split its realised
+// count into equal slices of whole 16-entry chunks that their warps take in
+// turn. Each warp streams its own chunks: its lanes copy the chunk's K and V
+// rows in 16-byte pieces (cp.async, one commit group per chunk) and the oldest
+// landed chunk is attended on the tensor cores by that warp alone, so the
+// steady state has no CTA-wide barrier. (One bulk copy per 256-byte row was
+// tried first: the per-copy cost of the bulk-copy unit held each SM to about
+// 20 GB/s.) With at most eight heads per KV head the keys are the MMA rows
+// (kt_attend); otherwise the heads are (attn_mma.cuh). Three CTAs per SM with
+// two chunks in flight per warp, or two CTAs with three. The warps' softmax
+// states are combined into the CTA's partial; a row of up to eight CTAs is one
+// thread-block cluster that merges the partials through distributed shared
+// memory, a larger row's last CTA merges them from the workspace. Entries
+// outside [0, cap) are reported and masked (their slots read row 0 of the
+// head).
 #include "attn_mma.cuh"
 #include "kernels.cuh"
 
@@ -22,9 +26,6 @@ namespace tb {
 constexpr int kAsThreads = 128;
 constexpr int kAsWarps = kAsThreads / 32;
 constexpr int kAsChunk = 16;   // entries per warp chunk (one tensor-core tile of slots)
-// keys-as-rows form: three CTAs per SM with two chunks in flight per warp when a row needs at most twice the
-// cluster limit of CTAs (it then takes one cluster; more warps per SM stream faster), else two CTAs per SM with
-// three chunks in flight
 constexpr int kAsClusterMax = 8;   // most CTAs per row that merge as one cluster (the portable cluster size; 9-CTA
                                    // clusters measured slower: they pack poorly onto the GPCs)
 
@@ -200,9 +201,10 @@ __device__ __forceinline__ void stream_merge(const float *__restrict__ part, int
     }
 }
 
-// Grid (C, rows): CTA c of a row takes the c-th of C equal slices (whole chunks of 16) of the row's selection,
-// cut into chunks of 16 that its warps take in turn. The warps' states are combined into the CTA's
-// partial (m, l, acc[D] per head). CL: the row's C CTAs are one cluster, keep their partials in shared memory
+// Grid (C, rows): CTA c of a row takes the c-th of C equal slices (whole chunks of 16) of the row's realised
+// count, whose chunks its warps take in turn. The warps' states are combined into the CTA's partial
+// (m, l, acc[D] per head). SETS chunks in flight per warp, MINB CTAs per SM. app.pos >= 0: a step inside a
+// prediction interval (see AttnAppend). CL: the row's C CTAs are one cluster, keep their partials in shared memory
 // and each merges a slice of the outputs through distributed shared memory; otherwise the partials go to the
 // workspace and the row's last arriving CTA merges them. KT: keys as the MMA rows (G <= 8); otherwise the G
 // heads are the rows (G <= 16).
@@ -567,6 +569,9 @@ cudaError_t launch_attn_stream(const tb_shape &sh, const uint16_t *q, const uint
     const AttnAppend none;
     const AttnAppend &ap = app ? *app : none;
     if (ap.pos >= 0 && (!ap.K_new || !ap.V_new || !ap.sel || !ap.counts || !counts)) return cudaErrorInvalidValue;
+    // keys-as-rows form: three CTAs per SM with two chunks in flight per warp when a row needs at most twice
+    // the cluster limit of CTAs (it then takes one cluster; twelve warps per SM stream faster than eight),
+    // else two CTAs per SM with three chunks in flight
     const bool kt = sh.Hq / sh.Hkv <= 8;
     const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
     const bool three = kt && (3 * sms) / rows <= 2 * kAsClusterMax;
