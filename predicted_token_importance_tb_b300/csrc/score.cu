@@ -2,12 +2,15 @@
 // ("TokenButler: Token Importance is Predictable", gist.science summary,
 // Core Architecture, Scoring).
 //
-// HBM-bound stream of Kp (2*dp bytes per token). One thread per token; each
-// thread reads its dp/8 16-byte vectors (consecutive threads read
-// consecutive rows, so a warp's loads cover one contiguous span). The G
-// importance queries of the KV head sit in shared memory as fp32; with the
-// mean aggregation they are folded into their group mean first (the mean of
-// dot products equals the dot product with the mean query).
+// HBM-bound stream of Kp (2*dp bytes per token). A warp scores 32
+// consecutive tokens; each of its dp/8 load instructions reads 512 contiguous
+// bytes and the lanes of a row add their partial dot products by shuffles.
+// Long rows go through a shared-memory ring of cp.async tiles per warp
+// (score_ring_kernel), shorter ones one tile per CTA in registers
+// (score_kernel). The G importance queries of the KV head sit in shared memory
+// as fp32; with the mean aggregation they are folded into their group mean
+// first (the mean of dot products equals the dot product with the mean query).
+// Any other dp (a multiple of 8): one thread per token (score_kernel_any).
 #include "tb_internal.cuh"
 #include "kernels.cuh"
 
@@ -15,12 +18,6 @@ namespace tb {
 
 constexpr int kScoreThreads = 256;
 constexpr int kScoreMultiMin = 8;   // tiles per CTA below which one tile per CTA is used
-
-template <int NV>
-__device__ __forceinline__ void load_row(const uint4 *p, uint4 (&v)[NV]) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = __ldcs(p + i);
-}
 
 __device__ __forceinline__ float dot8(const float *q, uint4 v, float acc) {
     acc = fmaf(q[0], bf16_lo(v.x), acc);
