@@ -12,8 +12,8 @@ namespace tb {
 // n_seq (device, [B], may be null): sequence b holds n_seq[b] + 1 tokens; the
 // scores of its later positions are -inf. after_append: the append kernel was
 // launched just before on the same stream and triggers its dependents at its
-// start; the score kernel runs as its programmatic dependent (only the CTAs
-// that read the appended row n - 1 wait for it).
+// start; the score kernel runs as its programmatic dependent (only the CTA
+// that reads the appended row, the row's or sequence's last, waits for it).
 cudaError_t launch_score(const tb_shape &sh, const uint16_t *q_imp, const uint16_t *Kp, int64_t n, int agg,
                          float *s, int64_t lds, cudaStream_t st, const int64_t *n_seq = nullptr,
                          bool after_append = false);

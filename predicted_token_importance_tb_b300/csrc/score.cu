@@ -78,15 +78,16 @@ score_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict__ Kp
              int U, int after_append) {
     extern __shared__ float qs[];   // [G][dp] (MAX) or [dp] (MEAN)
     constexpr int TPI = 32 / NV;    // rows per load instruction of a warp
-    // launched as the append kernel's programmatic dependent: only the row's last CTA reads the appended Kp
-    // row, so only it waits for that kernel to finish
-    if (after_append && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.y;
     const int b = row / Hkv, h = row % Hkv;
     const int G = Hq / Hkv;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, pc = lane % NV;
     // tokens past this sequence's n_seq[b] + 1 are scored -inf (never selected)
     const int64_t n_lim = n_seq ? (n_seq[b] + 1 < n ? n_seq[b] + 1 : n) : n;
+    // launched as the append kernel's programmatic dependent: only the CTA holding the appended token (the
+    // sequence's last, n_lim - 1) reads what that kernel writes, so only it waits for it to finish
+    if (after_append && blockIdx.x == (n_lim - 1) / ((int64_t)U * kScoreThreads))
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t w0 = (int64_t)blockIdx.x * U * kScoreThreads + warp * 32;
     const uint4 *krow = reinterpret_cast<const uint4 *>(Kp + (int64_t)row * cap * dp);
     float *srow = s + (int64_t)row * lds;
@@ -145,7 +146,6 @@ score_ring_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict
                   const int64_t *__restrict__ n_seq, int U, int after_append) {
     extern __shared__ __align__(16) uint8_t smb[];
     constexpr int TPI = 32 / NV, WT = 512 * NV;   // rows per load instruction; bytes of a warp's slice
-    if (after_append && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.y;
     const int b = row / Hkv, h = row % Hkv;
     const int G = Hq / Hkv;
@@ -153,6 +153,8 @@ score_ring_kernel(const uint16_t *__restrict__ q_imp, const uint16_t *__restrict
     float *qs = reinterpret_cast<float *>(smb + (kScoreThreads / 32) * kScoreDepth * WT);
     const uint32_t rb = (uint32_t)__cvta_generic_to_shared(smb + warp * kScoreDepth * WT) + lane * 16;
     const int64_t n_lim = n_seq ? (n_seq[b] + 1 < n ? n_seq[b] + 1 : n) : n;
+    if (after_append && blockIdx.x == (n_lim - 1) / ((int64_t)U * kScoreThreads))   // see score_kernel
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t w0 = (int64_t)blockIdx.x * U * kScoreThreads + warp * 32;
     const uint4 *krow = reinterpret_cast<const uint4 *>(Kp + (int64_t)row * cap * dp);
     float *srow = s + (int64_t)row * lds;

@@ -458,7 +458,7 @@ tb_status tb_decode_step_ragged(const tb_shape *shape, const tb_step_params *p, 
     if (e != cudaSuccess) return from_cuda(e);
     if (predict) {
         // 2. score up to the longest sequence (later positions of the shorter ones score -inf), select, widen
-        e = launch_score(*shape, q_imp, Kp, nt_hi, p->agg, scores, nt_hi, stream, n_dev);
+        e = launch_score(*shape, q_imp, Kp, nt_hi, p->agg, scores, nt_hi, stream, n_dev, true);
         if (e != cudaSuccess) return from_cuda(e);
         if (p->r == 0 && p->T == 1) {
             e = launch_topk(rows, scores, nt_hi, nt_hi, kc, idx_state, ctl, dev_status, stream, sel, sel_stride, counts);
