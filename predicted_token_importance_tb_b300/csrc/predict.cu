@@ -9,7 +9,9 @@
 // Decode runs it for a handful of tokens, so both layers are GEMVs bound by
 // the weight stream: a warp per output row reads the row once with 16-byte
 // loads and keeps one fp32 accumulator per token; the tokens' inputs sit in
-// shared memory. Two launches (the second needs all of h).
+// shared memory. Two launches (the second needs all of h); the second runs as
+// the first's programmatic dependent and streams its weights while the first
+// still runs.
 #include "tb_internal.cuh"
 #include "kernels.cuh"
 
@@ -47,10 +49,13 @@ __device__ __forceinline__ void unpack_w(const uint4 u, float (&f)[8]) {
     f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
 }
 
-template <typename IN, int BT, bool SILU, bool OUT_BF16>
+// PDL: 1 = the first layer (its dependent may launch at once), 2 = the second layer, launched as that
+// dependent: it requests its first weight pieces, then waits for the first layer before reading h.
+template <typename IN, int BT, bool SILU, bool OUT_BF16, int PDL>
 __global__ void __launch_bounds__(kPredThreads)
 gemv_rows_kernel(const IN *__restrict__ in, const uint16_t *__restrict__ W, int B, int E, int O,
                  void *__restrict__ out) {
+    if (PDL == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(16) uint8_t smem[];
     IN *xs = reinterpret_cast<IN *>(smem);
     constexpr int PER16 = 16 / sizeof(IN);
@@ -66,6 +71,7 @@ gemv_rows_kernel(const IN *__restrict__ in, const uint16_t *__restrict__ W, int 
         }
     };
     fetch(o, 0);
+    if (PDL == 2) asm volatile("griddepcontrol.wait;" ::: "memory");   // h is complete
     for (int x = threadIdx.x; x < B * E / PER16; x += blockDim.x)
         reinterpret_cast<uint4 *>(xs)[x] = reinterpret_cast<const uint4 *>(in)[x];
     __syncthreads();
@@ -113,18 +119,28 @@ gemv_rows_kernel(const IN *__restrict__ in, const uint16_t *__restrict__ W, int 
     }
 }
 
-template <typename IN, bool SILU, bool OUT_BF16>
+template <typename IN, bool SILU, bool OUT_BF16, int PDL>
 static cudaError_t launch_gemv(const IN *in, const uint16_t *W, int B, int E, int O, void *out, cudaStream_t st) {
     const size_t smem = (size_t)B * E * sizeof(IN);
     const int sms = dev_info().sms > 0 ? dev_info().sms : 148;
     int grid = (O + kPredWarps - 1) / kPredWarps;
     if (grid > 8 * sms) grid = 8 * sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kPredThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PDL == 2 ? 1 : 0;
 #define TB_GEMV_CASE(BTV)                                                                                     \
     do {                                                                                                      \
-        cudaError_t e = cudaFuncSetAttribute(gemv_rows_kernel<IN, BTV, SILU, OUT_BF16>,                       \
+        cudaError_t e = cudaFuncSetAttribute(gemv_rows_kernel<IN, BTV, SILU, OUT_BF16, PDL>,                  \
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);         \
         if (e != cudaSuccess) return e;                                                                       \
-        gemv_rows_kernel<IN, BTV, SILU, OUT_BF16><<<grid, kPredThreads, smem, st>>>(in, W, B, E, O, out);     \
+        return cudaLaunchKernelEx(&cfg, gemv_rows_kernel<IN, BTV, SILU, OUT_BF16, PDL>, in, W, B, E, O, out); \
     } while (0)
     if (B <= 1) TB_GEMV_CASE(1);
     else if (B <= 4) TB_GEMV_CASE(4);
@@ -137,9 +153,9 @@ static cudaError_t launch_gemv(const IN *in, const uint16_t *W, int B, int E, in
 cudaError_t launch_predict(const uint16_t *x, const uint16_t *W1, const uint16_t *W2, int B, int E, int F, int O,
                            float *h, uint16_t *q_imp, cudaStream_t st) {
     if (B <= 0) return cudaSuccess;
-    cudaError_t e = launch_gemv<uint16_t, true, false>(x, W1, B, E, F, h, st);
+    cudaError_t e = launch_gemv<uint16_t, true, false, 1>(x, W1, B, E, F, h, st);
     if (e != cudaSuccess) return e;
-    return launch_gemv<float, false, true>(h, W2, B, F, O, q_imp, st);
+    return launch_gemv<float, false, true, 2>(h, W2, B, F, O, q_imp, st);
 }
 
 }  // namespace tb
