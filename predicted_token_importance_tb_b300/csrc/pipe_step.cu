@@ -530,7 +530,6 @@ __host__ __device__ constexpr int pipe_attn_smem_bytes(int DT, int DP) {
 template <int DT, int NV, bool CHAIN>
 __global__ void __maxnreg__(168) pipe_attend_kernel(const PipeAttn a) {
     extern __shared__ __align__(128) uint8_t smb[];
-    __shared__ __align__(8) uint64_t bars[kPipeBufs];
     __shared__ uint32_t scan[40];
     __shared__ __align__(16) uint16_t kpn[64];   // the new token's projected key (bf16 bits), read as uint4
     __shared__ int s_abort, s_cnt[kPipeBufs];
@@ -558,14 +557,9 @@ __global__ void __maxnreg__(168) pipe_attend_kernel(const PipeAttn a) {
     PipeRow *ctl = a.ctl + row;
 
     pdl_trigger();
-    if (tid == 0) {
-        s_abort = 0;
-        for (int i = 0; i < kPipeBufs; ++i) mbarrier_init(&bars[i], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    if (tid == 0) s_abort = 0;
     __syncthreads();
-    uint32_t phase[kPipeBufs] = {};
-    int r_issue = 0, r_done = 0;   // gather rounds issued and consumed (uniform)
+    int r_issue = 0, r_done = 0;   // gather rounds issued and consumed (uniform); one cp.async group each
 
     // this step's own inputs: query tile, the new K/V row (slot 0 of xn), its projected key and score
     uint32_t key_n = 0;
@@ -650,8 +644,9 @@ __global__ void __maxnreg__(168) pipe_attend_kernel(const PipeAttn a) {
         __syncthreads();
     };
 
-    // one round: up to kPipeRound queued tokens' K/V rows into buffer r_issue % kPipeBufs (bulk copies issued
-    // by every thread); padding slots up to a multiple of 16 get zeros (their V rows must be finite)
+    // one round: up to kPipeRound queued tokens' K/V rows into buffer r_issue % kPipeBufs in 16-byte cp.async
+    // pieces from every thread (one bulk copy per 256-byte row, as before, is held back by the bulk-copy unit's
+    // per-copy cost); padding slots up to a multiple of 16 get zeros (their V rows must be finite)
     auto issue = [&](int q0, int cnt) {
         const int buf = r_issue % kPipeBufs;
         uint8_t *Xb = X + (size_t)buf * kPipeRound * SB;
@@ -661,14 +656,14 @@ __global__ void __maxnreg__(168) pipe_attend_kernel(const PipeAttn a) {
                 make_uint4(0u, 0u, 0u, 0u);
         if (tid == 0) s_cnt[buf] = cnt;
         __syncthreads();
-        if (tid == 0) mbarrier_arrive_expect_tx(&bars[buf], (uint32_t)(cnt * 4 * DT));
-        if (tid < cnt) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            const int64_t t = queue[q0 + tid];
-            uint8_t *dst = Xb + (size_t)tid * SB;
-            bulk_g2s(dst, Kh + t * DT, 2 * DT, &bars[buf]);
-            bulk_g2s(dst + 2 * DT, Vh + t * DT, 2 * DT, &bars[buf]);
+        for (int x = tid; x < cnt * 2 * CPR; x += kPipeThreads) {
+            const int ent = x / (2 * CPR), r = x % (2 * CPR);
+            const bool isv = r >= CPR;
+            const int pc = isv ? r - CPR : r;
+            const int64_t t = queue[q0 + ent];
+            cp_async16(Xb + (size_t)ent * SB + (isv ? 2 * DT : 0) + pc * 16, (isv ? Vh : Kh) + t * DT + pc * 8);
         }
+        cp_async_commit();
         ++r_issue;
     };
 
@@ -682,8 +677,12 @@ __global__ void __maxnreg__(168) pipe_attend_kernel(const PipeAttn a) {
     // the oldest round in flight: wait, attend
     auto consume = [&]() -> bool {
         const int buf = r_done % kPipeBufs;
-        if (!pipe_wait(&bars[buf], phase[buf], &s_abort, a.dev_status)) return false;
-        phase[buf] ^= 1u;
+        // this thread's pieces of round r_done have landed once at most r_issue - r_done - 1 groups are pending
+        const int pend = r_issue - r_done - 1;
+        if (pend >= 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+        else if (pend == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();   // every thread's pieces of the round are visible to the CTA
         mma_attend<DT, kPipeWarps, false>(A, X + (size_t)buf * kPipeRound * SB, SB, s_cnt[buf], nullptr, 0, qsm,
                                           qscale);
         __syncthreads();   // the buffer is free again
@@ -843,8 +842,8 @@ __global__ void __maxnreg__(168) pipe_attend_kernel(const PipeAttn a) {
         ok = drain(0, (int)qt, sidx + 1 == nseg);
     }
     if (s_abort || !ok) {
-        // wait, bounded, for the gather rounds still in flight before the CTA exits
-        for (int r = r_done; r < r_issue; ++r) mbarrier_wait_bounded(&bars[r % kPipeBufs], phase[r % kPipeBufs], kWaitLimitNs);
+        // the gather rounds still in flight land before the CTA exits
+        asm volatile("cp.async.wait_all;" ::: "memory");
         return;
     }
     if (owner) {
